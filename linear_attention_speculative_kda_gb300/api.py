@@ -1,0 +1,289 @@
+"""Thin ctypes binding of ``libkda.so`` (the C ABI of ``include/kda.h``).
+
+Argument marshalling only: every function checks dtypes, devices and shapes
+of the torch tensors it is given, fills a ``kda_config`` and passes raw
+device pointers and the current CUDA stream to the entry point of the same
+name.  Every step of the method runs in the library's CUDA kernels; there is
+no fallback of any kind.  If the library has not been built, the first call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIBRARY = os.path.join(_PKG, "libkda.so")
+
+HEAD_DIM = 128
+MAX_WINDOW = 8
+RECORD_STRIDE = 392          # bf16 elements per token record (k, v, g, beta, pad)
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+
+ROW_BAD_LENGTH = 1
+ROW_BAD_SLOT = 2
+ROW_BAD_RECORD = 4
+ROW_BAD_PENDING = 8
+
+EXPORTED = (
+    "kda_records_bytes",
+    "kda_verify",
+    "kda_commit",
+    "kda_flush",
+    "kda_status_string",
+    "kda_abi_version",
+)
+
+
+class KDAError(RuntimeError):
+    """A call into libkda returned a status other than KDA_OK."""
+
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: status {status} ({_status_name(status)})")
+        self.status = status
+
+
+class KdaConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("num_slots", ctypes.c_int32),
+        ("record_slots", ctypes.c_int32),
+        ("use_lower_bound", ctypes.c_int32),
+        ("lower_bound", ctypes.c_float),
+        ("scale", ctypes.c_float),
+        ("stride_q_t", ctypes.c_int64),
+        ("stride_k_t", ctypes.c_int64),
+        ("stride_v_t", ctypes.c_int64),
+        ("stride_g_t", ctypes.c_int64),
+        ("stride_beta_t", ctypes.c_int64),
+    ]
+
+
+_lib_handle = None
+
+
+def library_path() -> str:
+    return _LIBRARY
+
+
+def load_library():
+    """Load libkda.so (once).  Raises if it is missing: there is no fallback."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(_LIBRARY):
+        raise RuntimeError(
+            f"libkda.so not found at {_LIBRARY}; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(_LIBRARY)
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    cfgp = ctypes.POINTER(KdaConfig)
+    lib.kda_records_bytes.restype = ctypes.c_size_t
+    lib.kda_records_bytes.argtypes = [i32, i32, i32]
+    lib.kda_verify.restype = ctypes.c_int
+    lib.kda_verify.argtypes = [cfgp] + [vp] * 10 + [i32] + [vp] * 7
+    lib.kda_commit.restype = ctypes.c_int
+    lib.kda_commit.argtypes = [cfgp] + [vp] * 5 + [i32] + [vp] * 7
+    lib.kda_flush.restype = ctypes.c_int
+    lib.kda_flush.argtypes = [cfgp] + [vp] * 4 + [i32] + [vp] * 5
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_abi_version.restype = i32
+    lib.kda_abi_version.argtypes = []
+    _lib_handle = lib
+    return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load_library().kda_status_string(status).decode()
+    except Exception:  # pragma: no cover - only for messages
+        return "?"
+
+
+def _check(fn: str, status: int) -> None:
+    if status != KDA_OK:
+        raise KDAError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _token_stride(t: torch.Tensor) -> int:
+    # [T, H, D] (or [1, T, H, D]) activation with heads and channels packed
+    if t.dim() == 4:
+        t = t[0]
+    if t.dim() == 3:
+        if t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+            raise ValueError("activations need contiguous [H, D] inside a token")
+    elif t.dim() == 2:
+        if t.stride(1) != 1:
+            raise ValueError("beta needs contiguous heads inside a token")
+    else:
+        raise ValueError("unexpected activation rank")
+    return t.stride(0) if t.shape[0] > 1 else max(t.stride(0), 1)
+
+
+def _req(t, dtype, name, device):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+    return t
+
+
+def _opt(t, dtype, name, device):
+    return None if t is None else _req(t, dtype, name, device)
+
+
+def make_config(num_heads, window, num_slots, record_slots, *, lower_bound=None,
+                scale=None, strides=(1, 1, 1, 1, 1), head_dim=HEAD_DIM) -> KdaConfig:
+    cfg = KdaConfig()
+    cfg.num_heads = num_heads
+    cfg.head_dim = head_dim
+    cfg.window = window
+    cfg.num_slots = num_slots
+    cfg.record_slots = record_slots
+    cfg.use_lower_bound = 0 if lower_bound is None else 1
+    cfg.lower_bound = 0.0 if lower_bound is None else float(lower_bound)
+    cfg.scale = head_dim ** -0.5 if scale is None else float(scale)
+    (cfg.stride_q_t, cfg.stride_k_t, cfg.stride_v_t, cfg.stride_g_t,
+     cfg.stride_beta_t) = [int(s) for s in strides]
+    return cfg
+
+
+def kda_records_bytes(num_heads: int, window: int, record_slots: int) -> int:
+    """Size in bytes of the records buffer (``kda_records_bytes``)."""
+    return int(load_library().kda_records_bytes(num_heads, window, record_slots))
+
+
+def allocate_records(num_heads: int, window: int, record_slots: int, device) -> torch.Tensor:
+    """A records buffer for ``record_slots`` slots plus the scratch row."""
+    nbytes = kda_records_bytes(num_heads, window, record_slots)
+    if nbytes == 0:
+        raise ValueError("invalid record sizes")
+    return torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device)
+
+
+def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
+               state_indices, records, out, *, window: int, record_slots: int,
+               lower_bound=None, scale=None, record_rows=None, pending=None,
+               trajectory_out=None, error_word=None) -> torch.Tensor:
+    """``kda_verify``: speculative verify from each row's checkpoint.
+
+    q, k, v, g_raw: bf16 [T, H, 128] (token stride free, [H, D] packed);
+    beta_raw: bf16 [T, H]; A_log fp32 [H]; g_bias fp32 [H*128];
+    state_pool fp32 [S, H, 128, 128]; cu_seqlens int32 [B+1];
+    state_indices int32 [B]; records: buffer from ``allocate_records``;
+    out: bf16 [T, H, 128] contiguous.  Returns ``out``.
+    """
+    dev = state_pool.device
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    for name, t in (("q", q), ("k", k), ("v", v), ("g_raw", g_raw), ("beta_raw", beta_raw),
+                    ("records", records), ("out", out)):
+        _req(t, bf, name, dev)
+    for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
+        _req(t, f32, name, dev)
+    _req(cu_seqlens, i32, "cu_seqlens", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _opt(record_rows, i32, "record_rows", dev)
+    _opt(pending, i32, "pending", dev)
+    _opt(trajectory_out, f32, "trajectory_out", dev)
+    _opt(error_word, i32, "error_word", dev)
+    if state_pool.dim() != 4 or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    S, H = state_pool.shape[0], state_pool.shape[1]
+    if not out.is_contiguous() or not A_log.is_contiguous() or not g_bias.is_contiguous():
+        raise ValueError("out, A_log and g_bias must be contiguous")
+    for t in (cu_seqlens, state_indices, record_rows, pending):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("metadata tensors must be contiguous")
+    B = state_indices.shape[0]
+    if cu_seqlens.shape[0] != B + 1:
+        raise ValueError("cu_seqlens must have B + 1 entries")
+    strides = (_token_stride(q), _token_stride(k), _token_stride(v), _token_stride(g_raw),
+               _token_stride(beta_raw))
+    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound, scale=scale,
+                      strides=strides, head_dim=state_pool.shape[-1])
+    lib = load_library()
+    st = lib.kda_verify(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+                        _ptr(beta_raw), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
+                        _ptr(cu_seqlens), _ptr(state_indices), B, _ptr(record_rows),
+                        _ptr(pending), _ptr(records), _ptr(out), _ptr(trajectory_out),
+                        _ptr(error_word), _stream_ptr(dev))
+    _check("kda_verify", st)
+    return out
+
+
+def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepted, records,
+               *, window: int, record_slots: int, lower_bound=None, record_rows=None,
+               pending=None, eager=None, error_word=None) -> None:
+    """``kda_commit``: fold each row's accepted tokens into its checkpoint
+    (eager), or store them as pending replays (deferred, ``pending`` given)."""
+    dev = state_pool.device
+    f32, i32 = torch.float32, torch.int32
+    for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
+        _req(t, f32, name, dev)
+    _req(records, torch.bfloat16, "records", dev)
+    _req(cu_seqlens, i32, "cu_seqlens", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _req(num_accepted, i32, "num_accepted", dev)
+    _opt(record_rows, i32, "record_rows", dev)
+    _opt(pending, i32, "pending", dev)
+    _opt(eager, torch.uint8, "eager", dev)
+    _opt(error_word, i32, "error_word", dev)
+    if state_pool.dim() != 4 or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    B = state_indices.shape[0]
+    if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < B:
+        raise ValueError("metadata sizes do not match the batch")
+    S, H = state_pool.shape[0], state_pool.shape[1]
+    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
+                      head_dim=state_pool.shape[-1])
+    lib = load_library()
+    st = lib.kda_commit(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
+                        _ptr(cu_seqlens), _ptr(state_indices), B, _ptr(num_accepted),
+                        _ptr(record_rows), _ptr(records), _ptr(pending), _ptr(eager),
+                        _ptr(error_word), _stream_ptr(dev))
+    _check("kda_commit", st)
+
+
+def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, window: int,
+              record_slots: int, lower_bound=None, record_rows=None, error_word=None) -> None:
+    """``kda_flush``: fold pending replays into the checkpoints in place."""
+    dev = state_pool.device
+    f32, i32 = torch.float32, torch.int32
+    for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
+        _req(t, f32, name, dev)
+    _req(records, torch.bfloat16, "records", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _req(pending, i32, "pending", dev)
+    _opt(record_rows, i32, "record_rows", dev)
+    _opt(error_word, i32, "error_word", dev)
+    if state_pool.dim() != 4 or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    B = state_indices.shape[0]
+    S, H = state_pool.shape[0], state_pool.shape[1]
+    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
+                      head_dim=state_pool.shape[-1])
+    lib = load_library()
+    st = lib.kda_flush(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
+                       _ptr(state_indices), B, _ptr(record_rows), _ptr(records), _ptr(pending),
+                       _ptr(error_word), _stream_ptr(dev))
+    _check("kda_flush", st)

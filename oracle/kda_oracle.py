@@ -1,0 +1,380 @@
+"""CPU oracle of KDA speculative verify and commit (test infrastructure only).
+
+ONLY the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  The product path (the CUDA library and
+its Python binding) never does, and this module imports nothing from the
+product package.
+
+The arithmetic of one window lives in ``kda_window.c`` (double precision,
+the plain definition of the recurrence).  This module adds the bookkeeping
+the pages define around it, each function citing the passage it follows:
+
+* ``verify`` -- the RecoverSSM verify of recoverssm.py (``_verify_kernel``):
+  per (request row, head), read the checkpoint of ``state_indices[b]``, run
+  the row's tokens, write the outputs and record each token's raw k, v,
+  g_raw and beta_raw; never store a state.  Rows whose state index is
+  <= 0 (the null block) or whose token count is 0 are skipped.  With
+  ``pending`` (the deferred commit of the Kimi-K3 page, context.py), the
+  pending replay of the row's record slot is folded in first: the recorded
+  tokens are replayed from the checkpoint, the folded state is written back
+  to the pool, and the new tokens run from it.
+* ``commit`` -- ``_prepare_commit_plan_kernel`` plus the replay in
+  ``Glm5NextRecoverSSMCommitContext.commit``: n = min(max(accepted, 0), T, Q),
+  valid iff the state index is above the null block and n > 0; a valid row's
+  checkpoint becomes the state after its first n recorded tokens.  With
+  ``pending`` (``KDADeferredCommitContext.commit``): rows not in ``eager``
+  only store n as the pending replay of their record slot.
+* ``flush`` -- ``KDADeferredCommitContext.flush``: fold pending replays into
+  the checkpoints in place, leaving ``pending`` as it is.
+
+Readings where the pages are silent (the same list is kept with the design
+notes): a row with T > Q, a state index >= the pool size, a record slot
+outside [-1, R) or a pending count outside [0, Q] is invalid and skipped;
+a record slot of -1 is a scratch row that is written but never replayed;
+the fold of a pending replay happens even when the row has no new tokens;
+``pending`` is rewritten for every row a deferred commit sees (n for valid
+deferred rows, 0 otherwise) and is never written by a verify.
+
+Parity pins: see ``tests/test_oracle_pins.py`` (closed forms, brute force,
+invariants).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import build as _build
+
+_dbl_p = ctypes.POINTER(ctypes.c_double)
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        lib.kda_oracle_window.restype = ctypes.c_int
+        lib.kda_oracle_window.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            _dbl_p,
+            _dbl_p, _dbl_p, _dbl_p,
+            _dbl_p, _dbl_p,
+            ctypes.c_double, _dbl_p,
+            ctypes.c_int, ctypes.c_double, ctypes.c_double,
+            _dbl_p, _dbl_p, _dbl_p,
+        ]
+        lib.kda_oracle_gate.restype = ctypes.c_double
+        lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double,
+                                        ctypes.c_int, ctypes.c_double]
+        lib.kda_oracle_round_bf16.restype = ctypes.c_double
+        lib.kda_oracle_round_bf16.argtypes = [ctypes.c_double]
+        _LIB = lib
+    return _LIB
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    return a.ctypes.data_as(_dbl_p)
+
+
+def _f64(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def gate(x: float, a_log: float, bounded: bool, lower_bound: float) -> float:
+    """Gate value g of one channel for x = g_raw + g_bias (kda.py)."""
+    return _lib().kda_oracle_gate(float(x), float(a_log), int(bool(bounded)),
+                                  float(lower_bound))
+
+
+def round_bf16(x: float) -> float:
+    """Nearest bfloat16 value of x (ties to even)."""
+    return _lib().kda_oracle_round_bf16(float(x))
+
+
+def window(h0, k, v, g_raw, beta_raw, a_log, g_bias, *, q=None,
+           bounded=False, lower_bound=0.0, scale=1.0, want_out=None,
+           want_traj=False):
+    """Run one window of T tokens from state ``h0`` (V x K).
+
+    ``k``, ``g_raw``: T x K; ``v``: T x V; ``beta_raw``: T; ``q``: T x K or
+    None; ``g_bias``: K.  Returns ``(out, traj, h_final)``: ``out`` T x V
+    (None without q), ``traj`` T x V x K (None unless asked), ``h_final``
+    V x K.
+    """
+    h0 = _f64(h0)
+    V, K = h0.shape
+    k = _f64(k).reshape(-1, K)
+    T = k.shape[0]
+    v = _f64(v).reshape(T, V)
+    g_raw = _f64(g_raw).reshape(T, K)
+    beta_raw = _f64(beta_raw).reshape(T)
+    g_bias = _f64(g_bias).reshape(K)
+    if q is not None:
+        q = _f64(q).reshape(T, K)
+    if want_out is None:
+        want_out = q is not None
+    out = np.empty((T, V), np.float64) if want_out else None
+    traj = np.empty((T, V, K), np.float64) if want_traj else None
+    h_final = np.empty((V, K), np.float64)
+    rc = _lib().kda_oracle_window(
+        K, V, T, _ptr(h0), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+        _ptr(beta_raw), float(a_log), _ptr(g_bias), int(bool(bounded)),
+        float(lower_bound), float(scale), _ptr(out), _ptr(traj), _ptr(h_final))
+    if rc != 0:
+        raise ValueError("oracle window: bad sizes")
+    return out, traj, h_final
+
+
+# ---------------------------------------------------------------------------
+# What persists between calls: the state pool, the records and pending.
+# ---------------------------------------------------------------------------
+
+@dataclass
+class Layer:
+    """Gate parameters and sizes of one KDA layer (kda.py: A_log per head,
+    dt_bias per channel, the optional lower bound, scale = head_dim**-0.5)."""
+
+    num_heads: int
+    head_dim: int
+    window: int              # Q = 1 + num_spec
+    a_log: np.ndarray        # [H]
+    g_bias: np.ndarray       # [H, K]
+    bounded: bool
+    lower_bound: float
+    scale: float
+
+
+@dataclass
+class Step:
+    """One step's activations (token-major, float64) and row metadata."""
+
+    q: np.ndarray            # [T_tot, H, K]
+    k: np.ndarray            # [T_tot, H, K]
+    v: np.ndarray            # [T_tot, H, V]
+    g_raw: np.ndarray        # [T_tot, H, K]
+    beta_raw: np.ndarray     # [T_tot, H]
+    cu_seqlens: np.ndarray   # [B+1]
+    state_indices: np.ndarray  # [B]
+    record_rows: np.ndarray | None = None  # [B], -1 = scratch row
+
+
+class Cache:
+    """The oracle's copy of the state pool, records and pending counts.
+
+    The pool is read lazily from a float32 array ``[S, H, V, K]`` (never
+    modified); states the oracle writes are kept as float64 tiles.
+    """
+
+    def __init__(self, pool_f32, record_slots: int, pending=None):
+        self.pool_src = pool_f32
+        self.num_slots = pool_f32.shape[0]
+        self.record_slots = record_slots
+        self.written: dict[tuple[int, int], np.ndarray] = {}
+        self.records: dict[tuple[int, int], dict] = {}
+        if pending is None:
+            pending = np.zeros(record_slots, np.int64)
+        self.pending = np.array(pending, dtype=np.int64, copy=True)
+
+    def state(self, slot: int, head: int) -> np.ndarray:
+        tile = self.written.get((slot, head))
+        if tile is not None:
+            return tile.copy()
+        return np.asarray(self.pool_src[slot, head], dtype=np.float64)
+
+    def set_state(self, slot: int, head: int, tile: np.ndarray) -> None:
+        self.written[(slot, head)] = np.array(tile, dtype=np.float64, copy=True)
+
+
+@dataclass
+class RowIssue:
+    row: int
+    reason: str  # "length", "slot", "record", "pending"
+
+
+@dataclass
+class VerifyResult:
+    out: np.ndarray                         # [T_tot, H, V], NaN where not written
+    traj: dict = field(default_factory=dict)  # (token, head) -> V x K
+    issues: list = field(default_factory=list)
+    rows_run: list = field(default_factory=list)
+
+
+def _row_len(cu, b):
+    return int(cu[b + 1]) - int(cu[b])
+
+
+def _record_slot(record_rows, b):
+    return b if record_rows is None else int(record_rows[b])
+
+
+def _row_checks(layer: Layer, cache: Cache, T: int, slot: int, r: int):
+    """Checks of one row's metadata; returns the reason it is invalid or None."""
+    if T < 0 or T > layer.window:
+        return "length"
+    if slot >= cache.num_slots:
+        return "slot"
+    if r < -1 or r >= cache.record_slots:
+        return "record"
+    return None
+
+
+def _replay_records(layer, cache, slot, head, r, n):
+    """Replay the first n recorded tokens of record slot r from the
+    checkpoint (the commit's replay: q is not needed, so no outputs)."""
+    rec = cache.records[(r, head)]
+    h0 = cache.state(slot, head)
+    _, _, h = window(h0, rec["k"][:n], rec["v"][:n], rec["g"][:n],
+                     rec["beta"][:n], layer.a_log[head], layer.g_bias[head],
+                     bounded=layer.bounded, lower_bound=layer.lower_bound,
+                     scale=layer.scale)
+    return h
+
+
+def _map_rows(fn, rows, threads):
+    if threads and threads > 1 and len(rows) > 1:
+        with ThreadPoolExecutor(max_workers=threads) as pool:
+            return list(pool.map(fn, rows))
+    return [fn(b) for b in rows]
+
+
+def verify(layer: Layer, cache: Cache, step: Step, *, pending: bool = False,
+           rows=None, heads=None, want_traj: bool = False,
+           threads: int = 1) -> VerifyResult:
+    """RecoverSSM verify (recoverssm.py ``_verify_kernel``), optionally
+    folding pending replays first (context.py: the next verify replays the
+    pending count of the row's record slot in the same pass)."""
+    B = len(step.state_indices)
+    H, D = layer.num_heads, layer.head_dim
+    T_tot = step.k.shape[0]
+    res = VerifyResult(out=np.full((T_tot, H, D), np.nan))
+    rows = range(B) if rows is None else rows
+    heads = range(H) if heads is None else heads
+
+    def run(b):
+        T = _row_len(step.cu_seqlens, b)
+        slot = int(step.state_indices[b])
+        r = _record_slot(step.record_rows, b)
+        bad = _row_checks(layer, cache, T, slot, r)
+        if bad:
+            return RowIssue(b, bad)
+        if slot <= 0:          # null block: the row is padding
+            return None
+        p = int(cache.pending[r]) if (pending and r >= 0) else 0
+        if p < 0 or p > layer.window:
+            return RowIssue(b, "pending")
+        if T == 0 and p == 0:
+            return None
+        bos = int(step.cu_seqlens[b])
+        for h in heads:
+            if p > 0:
+                cache.set_state(slot, h, _replay_records(layer, cache, slot, h, r, p))
+            if T == 0:
+                continue
+            sl = slice(bos, bos + T)
+            out, traj, _ = window(
+                cache.state(slot, h), step.k[sl, h], step.v[sl, h],
+                step.g_raw[sl, h], step.beta_raw[sl, h], layer.a_log[h],
+                layer.g_bias[h], q=step.q[sl, h], bounded=layer.bounded,
+                lower_bound=layer.lower_bound, scale=layer.scale,
+                want_traj=want_traj)
+            res.out[sl, h] = out
+            if want_traj:
+                for t in range(T):
+                    res.traj[(bos + t, h)] = traj[t]
+            rec = cache.records.setdefault((r, h), {
+                "k": np.zeros((layer.window, D)), "v": np.zeros((layer.window, D)),
+                "g": np.zeros((layer.window, D)), "beta": np.zeros(layer.window)})
+            rec["k"][:T] = step.k[sl, h]
+            rec["v"][:T] = step.v[sl, h]
+            rec["g"][:T] = step.g_raw[sl, h]
+            rec["beta"][:T] = step.beta_raw[sl, h]
+        return b
+
+    for item in _map_rows(run, list(rows), threads):
+        if isinstance(item, RowIssue):
+            res.issues.append(item)
+        elif item is not None:
+            res.rows_run.append(item)
+    return res
+
+
+def commit_len(num_accepted: int, T: int, Q: int) -> int:
+    """``_prepare_commit_plan_kernel``: accepted count clamped to [0, T] and
+    to the record window Q."""
+    return min(max(int(num_accepted), 0), T, Q)
+
+
+def commit(layer: Layer, cache: Cache, step: Step, num_accepted, *,
+           deferred: bool = False, eager=None, rows=None, heads=None,
+           threads: int = 1) -> list:
+    """Commit after sampling (recoverssm.py commit context; context.py
+    deferred commit).  Returns the list of invalid rows."""
+    B = len(step.state_indices)
+    H = layer.num_heads
+    rows = range(B) if rows is None else rows
+    heads = range(H) if heads is None else heads
+
+    def run(b):
+        T = _row_len(step.cu_seqlens, b)
+        slot = int(step.state_indices[b])
+        r = _record_slot(step.record_rows, b)
+        bad = _row_checks(layer, cache, T, slot, r)
+        if bad:
+            return RowIssue(b, bad)
+        n = commit_len(num_accepted[b], T, layer.window)
+        valid = slot > 0 and n > 0 and r >= 0
+        if deferred:
+            now = bool(eager[b]) if eager is not None else False
+            if r >= 0:
+                cache.pending[r] = n if (valid and not now) else 0
+            if not now:
+                return None
+        if not valid:
+            return None
+        for h in heads:
+            cache.set_state(slot, h, _replay_records(layer, cache, slot, h, r, n))
+        return None
+
+    return [x for x in _map_rows(run, list(rows), threads) if x is not None]
+
+
+def flush(layer: Layer, cache: Cache, step: Step, *, rows=None, heads=None,
+          threads: int = 1) -> list:
+    """``KDADeferredCommitContext.flush``: fold each row's pending replay into
+    its checkpoint in place; pending is left for the next commit to rewrite."""
+    B = len(step.state_indices)
+    H = layer.num_heads
+    rows = range(B) if rows is None else rows
+    heads = range(H) if heads is None else heads
+
+    def run(b):
+        slot = int(step.state_indices[b])
+        r = _record_slot(step.record_rows, b)
+        bad = _row_checks(layer, cache, 0, slot, r)
+        if bad:
+            return RowIssue(b, bad)
+        if slot <= 0 or r < 0:
+            return None
+        p = int(cache.pending[r])
+        if p < 0 or p > layer.window:
+            return RowIssue(b, "pending")
+        if p == 0:
+            return None
+        for h in heads:
+            cache.set_state(slot, h, _replay_records(layer, cache, slot, h, r, p))
+        return None
+
+    return [x for x in _map_rows(run, list(rows), threads) if x is not None]
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)

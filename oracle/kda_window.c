@@ -1,0 +1,182 @@
+/*
+ * CPU oracle of the KDA gated delta-rule recurrence, in double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the package's smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header or
+ * constant with the CUDA library.
+ *
+ * What it computes is the plain definition of one KDA window, written out
+ * step by step in the order of the per-token loop of `_verify_kernel` in
+ * "recipes/docker-images/glm53-kindling/experimental/fixes/recoverssm.py"
+ * (GLM-5.3-Flash KDA speculative verify), for one (request, head) state tile
+ * H (V rows by K columns, row v, column k):
+ *
+ *   q^ = q / sqrt(sum q^2 + 1e-6) * scale        (L2 norm, then the scale)
+ *   k^ = k / sqrt(sum k^2 + 1e-6)
+ *   x  = g_raw + g_bias                           (per K channel)
+ *   g  = lb * sigmoid(exp(A_log) * x)             bounded gate (kda.py)
+ *        -exp(A_log) * softplus(x)                 default gate
+ *   H  = H * diag(exp(g))                          decay along K
+ *   beta = sigmoid(beta_raw)
+ *   v' = beta * (v - H k^)                         delta
+ *   H  = H + v' k^T                                rank-one update
+ *   o  = H q^                                      output, after the update
+ *
+ * Readings of points the pages leave open:
+ *   - softplus(x) = log1p(exp(x)), and x itself for x > 20 (the usual
+ *     threshold; the difference there is below 1e-8 relative);
+ *   - the bounded gate is used exactly when a lower bound is given, the
+ *     softplus gate otherwise (no clamp of the softplus gate);
+ *   - every step is done in double precision on the exact inputs.
+ *
+ * K and V are run-time sizes so that tiny tiles can be checked by brute
+ * force; the library itself only supports K = V = 128.
+ */
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double oracle_softplus(double x)
+{
+    if (x > 20.0)
+        return x;
+    return log1p(exp(x));
+}
+
+static double oracle_sigmoid(double x)
+{
+    return 1.0 / (1.0 + exp(-x));
+}
+
+/* Gate of one channel: x = g_raw + g_bias.  The bounded form is the one
+ * kda.py describes for its FlashKDA prefill and the one the verify kernel of
+ * recoverssm.py evaluates with its LOWER_BOUND constant: the lower bound
+ * times the logistic of exp(A_log) * x.  The unbounded form is the softplus
+ * gate that kda.py names as the layer's default. */
+double kda_oracle_gate(double x, double a_log, int bounded, double lower_bound)
+{
+    double a = exp(a_log);
+    if (bounded)
+        return lower_bound * oracle_sigmoid(a * x);
+    return -a * oracle_softplus(x);
+}
+
+/* One window of T tokens from the state h0 (V x K, row-major, k fastest).
+ *
+ * Token t reads q[t*K..], k[t*K..], v[t*V..], g_raw[t*K..], beta_raw[t];
+ * g_bias has K entries.  q may be NULL (no outputs: the commit replay),
+ * in which case out must be NULL too.
+ * out:     T x V, the output of each token (may be NULL);
+ * traj:    T x V x K, the state after each token (may be NULL);
+ * h_final: V x K, the state after the last token (T == 0: h0).
+ * Returns 0, or -1 if a size is out of range or memory runs out. */
+int kda_oracle_window(int K, int V, int T,
+                      const double *h0,
+                      const double *q, const double *k, const double *v,
+                      const double *g_raw, const double *beta_raw,
+                      double a_log, const double *g_bias,
+                      int bounded, double lower_bound, double scale,
+                      double *out, double *traj, double *h_final)
+{
+    if (K <= 0 || V <= 0 || T < 0)
+        return -1;
+    if (q == NULL && out != NULL)
+        return -1;
+
+    double *H = h_final;
+    memmove(H, h0, sizeof(double) * (size_t)V * (size_t)K);
+
+    double *kh = (double *)malloc(sizeof(double) * (size_t)K);
+    double *qh = (double *)malloc(sizeof(double) * (size_t)K);
+    double *decay = (double *)malloc(sizeof(double) * (size_t)K);
+    if (kh == NULL || qh == NULL || decay == NULL) {
+        free(kh);
+        free(qh);
+        free(decay);
+        return -1;
+    }
+
+    for (int t = 0; t < T; ++t) {
+        const double *kt = k + (size_t)t * K;
+        const double *vt = v + (size_t)t * V;
+        const double *gt = g_raw + (size_t)t * K;
+
+        /* L2 norm of k, eps inside the square root. */
+        double sk = 0.0;
+        for (int c = 0; c < K; ++c)
+            sk += kt[c] * kt[c];
+        double nk = sqrt(sk + 1e-6);
+        for (int c = 0; c < K; ++c)
+            kh[c] = kt[c] / nk;
+
+        /* L2 norm of q, then the scale. */
+        if (q != NULL) {
+            const double *qt = q + (size_t)t * K;
+            double sq = 0.0;
+            for (int c = 0; c < K; ++c)
+                sq += qt[c] * qt[c];
+            double nq = sqrt(sq + 1e-6);
+            for (int c = 0; c < K; ++c)
+                qh[c] = qt[c] / nq * scale;
+        }
+
+        /* Per-channel decay factor exp(g). */
+        for (int c = 0; c < K; ++c)
+            decay[c] = exp(kda_oracle_gate(gt[c] + g_bias[c], a_log, bounded,
+                                           lower_bound));
+
+        double beta = oracle_sigmoid(beta_raw[t]);
+
+        /* Decay: every row scales column c by the same factor. */
+        for (int r = 0; r < V; ++r)
+            for (int c = 0; c < K; ++c)
+                H[(size_t)r * K + c] *= decay[c];
+
+        /* Delta and rank-one update, one row at a time: the row's own
+         * prediction H[r,:] . k^ only involves that row. */
+        for (int r = 0; r < V; ++r) {
+            double *row = H + (size_t)r * K;
+            double u = 0.0;
+            for (int c = 0; c < K; ++c)
+                u += row[c] * kh[c];
+            double vp = beta * (vt[r] - u);
+            for (int c = 0; c < K; ++c)
+                row[c] += vp * kh[c];
+        }
+
+        /* Output after the update. */
+        if (out != NULL) {
+            for (int r = 0; r < V; ++r) {
+                const double *row = H + (size_t)r * K;
+                double o = 0.0;
+                for (int c = 0; c < K; ++c)
+                    o += row[c] * qh[c];
+                out[(size_t)t * V + r] = o;
+            }
+        }
+
+        if (traj != NULL)
+            memcpy(traj + (size_t)t * V * K, H, sizeof(double) * (size_t)V * K);
+    }
+
+    free(kh);
+    free(qh);
+    free(decay);
+    return 0;
+}
+
+/* Round a double to the nearest bfloat16 value (8 significant bits, ties
+ * to even), returned as a double.  Direct from the double, so there is no
+ * double rounding through float.  Values below bfloat16's normal range are
+ * not expected here and are rounded on the same 8-bit grid. */
+double kda_oracle_round_bf16(double x)
+{
+    if (x == 0.0 || isnan(x) || isinf(x))
+        return x;
+    int e;
+    double m = frexp(x, &e);          /* x = m * 2^e, 0.5 <= |m| < 1 */
+    double scaled = ldexp(m, 8);      /* 8 significant bits to the left */
+    double r = nearbyint(scaled);     /* default mode: nearest, ties to even */
+    return ldexp(r, e - 8);
+}
