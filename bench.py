@@ -1,0 +1,562 @@
+"""Benchmark of KDA speculative verify + commit on GB300.
+
+One step is one pass of the whole hot path over one batch.  For the default
+workload (deferred2: B=1024 requests, H=16 heads, Q=4, deferred commit over
+two chained decode steps) a step is the four launches
+    verify(step 1) -> deferred commit(step 1, 10% eager)
+    -> verify(step 2, folding the pending replays) -> commit(step 2, all eager)
+so every step starts and ends with no pending replay.  Other workloads run
+verify -> eager commit.  The metric is (request*head)-steps per second: each
+decode step of each (request, head) pair counts once.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from linear_attention_speculative_kda_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verify+commit (request*head)-steps/s"
+UNIT = "(request*head)-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+STATE_BYTES = 128 * 128 * 4          # one fp32 state tile
+TOKEN_BYTES = 2052                   # q, k, v, g_raw, beta read + out, records written
+RECORD_BYTES = 770                   # raw k, v, g_raw, beta read back by a replay
+
+
+# ---------------------------------------------------------------- helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Weak scaling: every rank draws its own batch of the same shape."""
+    return base_seed + 1000 * rank
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            data = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    return data
+
+
+def hbm_peak():
+    data = measured_peaks()
+    if data:
+        for key in ("hbm_gbs", "hbm_GBs", "hbm"):
+            if key in data and isinstance(data[key], (int, float)):
+                return float(data[key]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_attention_speculative_kda_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as fh:
+            h.update(name.encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch recorded by an ncu capture under profiles/, if the
+    capture was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.gpu_id = self._smi_id(device_index)
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    @staticmethod
+    def _smi_id(device_index: int) -> str:
+        """nvidia-smi id of the torch device (its UUID; the visible-devices
+        list maps torch indices to physical ones)."""
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            if uuid:
+                return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        return ids[device_index] if device_index < len(ids) else str(device_index)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread is not None:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+# ------------------------------------------------------- algorithmic bytes --
+
+def plan_bytes(wl: W.Workload):
+    """Algorithmic bytes of each launch of one step, from the drawn lengths,
+    accepted counts, eager masks and the pending replays they imply."""
+    sp = wl.spec
+    H = sp.H
+    lens = wl.lens.numpy().astype(np.int64)
+    slots = wl.state_indices.numpy()
+    live = slots > 0
+
+    def commit_n(acc):
+        return np.minimum(np.maximum(acc, 0), np.minimum(lens, sp.Q))
+
+    launches = []
+    if not sp.deferred:
+        n = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
+        vb = np.where(live & (lens > 0), STATE_BYTES + lens * TOKEN_BYTES, 0).sum() * H
+        cb = np.where(live & (n > 0), 2 * STATE_BYTES + n * RECORD_BYTES, 0).sum() * H
+        launches = [("verify", float(vb)), ("commit", float(cb))]
+        return launches
+    n1 = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
+    eager1 = wl.steps[0].eager.numpy().astype(bool)
+    n2 = commit_n(wl.steps[1].num_accepted.numpy().astype(np.int64))
+    valid1 = live & (n1 > 0)
+    v1 = np.where(live & (lens > 0), STATE_BYTES + lens * TOKEN_BYTES, 0).sum() * H
+    c1 = np.where(valid1 & eager1, 2 * STATE_BYTES + n1 * RECORD_BYTES, 0).sum() * H
+    pend = np.where(valid1 & ~eager1, n1, 0)
+    v2 = np.where(live & ((lens > 0) | (pend > 0)),
+                  STATE_BYTES + lens * TOKEN_BYTES
+                  + np.where(pend > 0, STATE_BYTES + pend * RECORD_BYTES, 0), 0).sum() * H
+    c2 = np.where(live & (n2 > 0), 2 * STATE_BYTES + n2 * RECORD_BYTES, 0).sum() * H
+    return [("verify", float(v1)), ("commit_deferred", float(c1)),
+            ("verify_fused", float(v2)), ("commit", float(c2))]
+
+
+def units_per_step(wl: W.Workload) -> int:
+    return wl.spec.B * wl.spec.H * wl.spec.steps
+
+
+# ------------------------------------------------------------- GPU engine --
+
+class Engine:
+    """Device-resident buffers of one workload and the step's launches."""
+
+    def __init__(self, wl: W.Workload, device):
+        from linear_attention_speculative_kda_gb300 import api
+        self.api = api
+        self.wl = wl
+        sp = wl.spec
+        d = device
+        self.dev = d
+        self.A_log = wl.A_log.to(d)
+        self.g_bias = wl.g_bias.to(d)
+        self.pool = wl.pool.to(d)
+        self.cu = wl.cu_seqlens.to(d)
+        self.slots = wl.state_indices.to(d)
+        self.rr = None if wl.record_rows is None else wl.record_rows.to(d)
+        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d)
+        self.pending = torch.zeros(sp.record_slots, dtype=torch.int32, device=d)
+        self.err = torch.zeros(1, dtype=torch.int32, device=d)
+        self.all_eager = torch.ones(sp.B, dtype=torch.uint8, device=d)
+        T = wl.total_tokens
+        self.steps = []
+        for st in wl.steps:
+            self.steps.append(dict(
+                qkv=st.qkv.to(d), beta_buf=st.beta_buf.to(d), g_raw=st.g_raw.to(d),
+                num_accepted=st.num_accepted.to(d),
+                eager=None if st.eager is None else st.eager.to(d),
+                out=torch.empty((T, sp.H, sp.D), dtype=torch.bfloat16, device=d)))
+        self.kw = dict(window=sp.Q, record_slots=sp.record_slots,
+                       lower_bound=sp.lower_bound if sp.bounded else None)
+
+    def _verify(self, s, pending):
+        H = self.wl.spec.H
+        self.api.kda_verify(s["qkv"][:, 0], s["qkv"][:, 1], s["qkv"][:, 2], s["g_raw"],
+                            s["beta_buf"][:, :H], self.A_log, self.g_bias, self.pool, self.cu,
+                            self.slots, self.records, s["out"], record_rows=self.rr,
+                            pending=self.pending if pending else None, error_word=self.err,
+                            **self.kw)
+
+    def _commit(self, s, deferred, eager):
+        self.api.kda_commit(self.A_log, self.g_bias, self.pool, self.cu, self.slots,
+                            s["num_accepted"], self.records, record_rows=self.rr,
+                            pending=self.pending if deferred else None,
+                            eager=eager if deferred else None, error_word=self.err, **self.kw)
+
+    def launches(self):
+        """The step as a list of (name, callable)."""
+        if not self.wl.spec.deferred:
+            s = self.steps[0]
+            return [("verify", lambda: self._verify(s, False)),
+                    ("commit", lambda: self._commit(s, False, None))]
+        s1, s2 = self.steps
+        return [("verify", lambda: self._verify(s1, True)),
+                ("commit_deferred", lambda: self._commit(s1, True, s1["eager"])),
+                ("verify_fused", lambda: self._verify(s2, True)),
+                ("commit", lambda: self._commit(s2, True, self.all_eager))]
+
+    def run_step(self, events=None):
+        for i, (_, fn) in enumerate(self.launches()):
+            if events is not None:
+                events[i][0].record()
+            fn()
+            if events is not None:
+                events[i][1].record()
+
+
+class HostIO:
+    """Pinned host copies of each step's inputs and outputs, for the
+    end-to-end measure through the public API."""
+
+    def __init__(self, eng: Engine):
+        self.eng = eng
+        self.h_in = []
+        self.h_out = []
+        for st in eng.steps:
+            ins = {k: st[k].cpu().pin_memory() for k in ("qkv", "beta_buf", "g_raw",
+                                                          "num_accepted")}
+            if st["eager"] is not None:
+                ins["eager"] = st["eager"].cpu().pin_memory()
+            self.h_in.append(ins)
+            self.h_out.append(torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory())
+        self.h2d = sum(t.numel() * t.element_size() for ins in self.h_in for t in ins.values())
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def run_step(self):
+        eng = self.eng
+        for st, ins in zip(eng.steps, self.h_in):
+            for k, t in ins.items():
+                st[k].copy_(t, non_blocking=True)
+        eng.run_step()
+        for st, out in zip(eng.steps, self.h_out):
+            out.copy_(st["out"], non_blocking=True)
+
+
+# -------------------------------------------------------------- CPU side --
+
+def oracle_sample_run(wl: W.Workload, rows, threads: int):
+    """The oracle on a sample of rows of the workload's whole step; returns
+    (units processed, seconds)."""
+    from oracle import kda_oracle as O
+
+    def f64(t):
+        return t.to(torch.float64).numpy()
+
+    sp = wl.spec
+    layer = O.Layer(sp.H, sp.D, sp.Q, f64(wl.A_log), f64(wl.g_bias).reshape(sp.H, sp.D),
+                    sp.bounded, sp.lower_bound if sp.bounded else 0.0, wl.scale)
+    steps = [O.Step(f64(st.q), f64(st.k), f64(st.v), f64(st.g_raw), f64(st.beta_raw),
+                    wl.cu_seqlens.numpy(), wl.state_indices.numpy(),
+                    None if wl.record_rows is None else wl.record_rows.numpy())
+             for st in wl.steps]
+    cache = O.Cache(wl.pool.numpy(), sp.record_slots)
+    t0 = time.perf_counter()
+    if not sp.deferred:
+        O.verify(layer, cache, steps[0], rows=rows, threads=threads)
+        O.commit(layer, cache, steps[0], wl.steps[0].num_accepted.numpy(), rows=rows,
+                 threads=threads)
+    else:
+        st1, st2 = wl.steps
+        O.verify(layer, cache, steps[0], pending=True, rows=rows, threads=threads)
+        O.commit(layer, cache, steps[0], st1.num_accepted.numpy(), deferred=True,
+                 eager=st1.eager.numpy(), rows=rows, threads=threads)
+        O.verify(layer, cache, steps[1], pending=True, rows=rows, threads=threads)
+        O.commit(layer, cache, steps[1], st2.num_accepted.numpy(), deferred=True,
+                 eager=np.ones(sp.B, np.uint8), rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return len(rows) * sp.H * sp.steps, dt
+
+
+def cpu_baseline(wl: W.Workload, budget_s: float):
+    """Time the oracle on growing samples of rows until ``budget_s`` seconds
+    of CPU work have been measured (or the whole batch is done)."""
+    threads = max(1, os.cpu_count() or 1)
+    rng = np.random.default_rng(123)
+    order = rng.permutation(wl.spec.B).tolist()
+    units = 0
+    secs = 0.0
+    done = 0
+    chunk = max(1, threads)
+    while done < len(order) and secs < budget_s:
+        rows = order[done:done + chunk]
+        u, dt = oracle_sample_run(wl, rows, threads)
+        units += u
+        secs += dt
+        done += len(rows)
+        chunk = min(len(order) - done, chunk * 2) if done < len(order) else 0
+        if chunk <= 0:
+            break
+    return {"value": units / secs if secs > 0 else None, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{done} of {wl.spec.B} rows x {wl.spec.H} heads x {wl.spec.steps} "
+                      f"decode step(s) of workload {wl.spec.name}, fp64 C oracle, "
+                      f"{threads} threads, {secs:.1f} s"}
+
+
+# ------------------------------------------------------------------- arms --
+
+def workload_config(wl: W.Workload, world: int):
+    sp = wl.spec
+    return {"workload": sp.name, "requests": sp.B, "heads": sp.H, "head_dim": sp.D,
+            "window": sp.Q, "pool_slots": sp.S, "record_slots": sp.record_slots,
+            "gate": f"bounded lb={sp.lower_bound}" if sp.bounded else "softplus",
+            "decode_steps_per_step": sp.steps, "ranks": world,
+            "tokens_per_decode_step": wl.total_tokens,
+            "l2": "inputs larger than L2 (state pool %.2f GB)" % (
+                wl.pool.numel() * 4 / 1e9)}
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(world, "nccl")
+    wl = W.generate(args.config, seed=shard_seed(args.seed, rank))
+    eng = Engine(wl, device)
+    names = [n for n, _ in eng.launches()]
+    nl = len(names)
+    bytes_per = dict(plan_bytes(wl))
+
+    for _ in range(args.warmup):
+        eng.run_step()
+    torch.cuda.synchronize()
+    if int(eng.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(eng.err.item())} during warm-up")
+
+    stream = torch.cuda.current_stream(device)
+    events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nl)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for k in range(args.steps):
+            eng.run_step(events[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_total, world, device)
+    per_kernel = {n: [] for n in names}
+    for k in range(args.steps):
+        for i, n in enumerate(names):
+            per_kernel[n].append(events[k][i][0].elapsed_time(events[k][i][1]))
+    if int(eng.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(eng.err.item())}")
+
+    units = units_per_step(wl) * args.steps
+    units_all = sum_over_ranks(units, world, device)
+    value = units_all / (ms_total / 1e3)
+    ms_per_step = ms_total / args.steps
+
+    peak, peak_src = hbm_peak()
+    kernels = []
+    for n in names:
+        avg_ms = statistics.mean(per_kernel[n])
+        b = bytes_per[n]
+        kernels.append({"name": n, "launches": args.steps, "avg_us": avg_ms * 1e3,
+                        "bytes_per_launch": b, "gbs": b / (avg_ms / 1e3) / 1e9,
+                        "share": sum(per_kernel[n]) / max(1e-9, sum(sum(v) for v in
+                                                                  per_kernel.values()))})
+    dom = max(kernels, key=lambda x: x["share"])
+    step_bytes = sum(bytes_per.values())
+    kname = "kda_verify" if dom["name"].startswith("verify") else "kda_commit"
+    roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": peak,
+                "unit": "GB/s", "frac": dom["gbs"] / peak,
+                "peak_source": f"{peak_src} ({'of measured' if peak_src == 'measured' else 'of fallback'})",
+                "traffic": profiled_traffic(f"{kname}_{dom['name']}", wl.spec.name),
+                "algorithmic_bytes_per_launch": dom["bytes_per_launch"]}
+    step_gbs = step_bytes * args.steps / (ms_total / 1e3) / 1e9
+
+    # end to end through the public API with host buffers
+    hio = HostIO(eng)
+    for _ in range(2):
+        hio.run_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    e_start.record(stream)
+    for _ in range(args.steps):
+        hio.run_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e_start.elapsed_time(e_stop), world, device)
+    e2e = {"value": units_all / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": hio.h2d,
+           "d2h_bytes_per_step": hio.d2h, "ms_per_step": e_ms / args.steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_budget)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 state, bf16 activations",
+            "data": "synthetic (seeded)", "config": workload_config(wl, world),
+            "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
+            "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
+            "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu}
+    if world > 1:
+        torch.distributed.barrier()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    wl = W.generate(args.config, seed=args.seed)
+    threads = max(1, os.cpu_count() or 1)
+    rng = np.random.default_rng(7)
+    rows_per_step = max(1, min(wl.spec.B, args.reference_rows))
+    times, units = [], 0
+    for k in range(args.warmup + args.steps):
+        rows = sorted(rng.choice(wl.spec.B, size=rows_per_step, replace=False).tolist())
+        u, dt = oracle_sample_run(wl, rows, threads)
+        if k >= args.warmup:
+            times.append(dt)
+            units += u
+    secs = sum(times)
+    value = units / secs
+    sample = (f"{rows_per_step} of {wl.spec.B} rows x {wl.spec.H} heads x {wl.spec.steps} "
+              f"decode step(s) per step, fp64 C oracle, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded)", "config": workload_config(wl, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="deferred2", choices=sorted(W.CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reference-rows", type=int, default=8)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

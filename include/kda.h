@@ -1,0 +1,194 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) KDA speculative verify / commit
+ * library ("RecoverSSM": one checkpoint state per request).
+ *
+ * The pages this follows:
+ *   [GLM]  recipes/docker-images/glm53-kindling/experimental/fixes/recoverssm.py
+ *          (GLM-5.3-Flash KDA speculative verify with one checkpoint state per
+ *          request): `_verify_kernel`, `kda_recoverssm_verify`,
+ *          `_prepare_commit_plan_kernel`, `Glm5NextRecoverSSMCommitContext.commit`.
+ *   [KIMI] vllm.models.kimi_k3.nvidia.specialized_decode.recoverssm.context
+ *          (the deferred fp32 commit): `KDADeferredCommitContext.commit`,
+ *          `.flush`, `KDARecoverSSMDeferred`, `allocate_records`.
+ *   [LAYER] recipes/.../experimental/fixes/kda.py (GLM-5.3-Flash KDA layer):
+ *          the gate (bounded sigmoid or the default softplus) and the layout
+ *          of q, k, v, g_raw and beta_raw.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never allocates, never synchronises the stream and never reads device
+ *   data on the host, so every call is a pure stream-ordered launch.
+ * - Sizes: K = V = head_dim = 128; Q = window = 1 + num_spec, 1..8.
+ * - The recurrent state pool is fp32 [num_slots][H][V][K], K contiguous, one
+ *   64 KiB tile per (slot, head).  Slot 0 is the null block: rows whose state
+ *   index is <= 0 are padding and are skipped entirely ([GLM] verify kernel).
+ * - Activations are bf16.  q, k, v, g_raw: [T_total][H][128] with a token
+ *   stride given in elements (heads contiguous inside a token); beta_raw:
+ *   [T_total][H] with its own token stride.  cu_seqlens is int32 [B + 1]
+ *   (row b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1).
+ * - Records (the verify -> commit scratch of [GLM] `Records` and [KIMI]
+ *   `allocate_records`) hold each token's RAW bf16 k, v, g_raw and beta_raw.
+ *   They are indexed by record slot r in [-1, R): r = -1 is a scratch row
+ *   that rows without a record slot write and nothing ever reads.  Layout
+ *   (internal, sized by kda_records_bytes): bf16
+ *   [R + 1][H][Q][KDA_RECORD_STRIDE] with record slot r at row r + 1, and in
+ *   each token record k at [0,128), v at [128,256), g_raw at [256,384) and
+ *   beta_raw at element 384 (the rest is padding to a 16-byte multiple).
+ * - record_rows: int32 [B], the record slot of each row, or NULL for r = b
+ *   (the GLM per-row layout, which then requires B <= R).
+ * - pending: int32 [R], per record slot, the accepted count whose replay is
+ *   still to be folded ([KIMI] `KDARecoverSSMDeferred.pending`).
+ * - error_word: optional device int32; a kernel that meets bad metadata skips
+ *   the row and ORs a KDA_ROW_* bit into it (no trap, no abort).  NULL: the
+ *   bits are dropped.
+ * - stream: a cudaStream_t passed as void* (NULL: the legacy default stream).
+ * - Return value: KDA_OK after a successful launch (or when there is nothing
+ *   to launch, e.g. B == 0); KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED when a
+ *   host-side check fails (nothing is launched); KDA_ERR_CUDA when the launch
+ *   itself fails (cudaGetLastError after the launch).
+ * - Rows must use distinct state slots and distinct record slots (other than
+ *   -1); two rows sharing one race, as in the pages.
+ */
+#ifndef KDA_GB300_KDA_H
+#define KDA_GB300_KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* a pointer, size, stride or alignment is wrong */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, Q > 8 */
+    KDA_ERR_CUDA = 3          /* the kernel launch failed */
+} kda_status;
+
+/* Bits of *error_word (device-side checks; the row is skipped). */
+#define KDA_ROW_BAD_LENGTH  1  /* token count < 0 or > window */
+#define KDA_ROW_BAD_SLOT    2  /* state index >= num_slots */
+#define KDA_ROW_BAD_RECORD  4  /* record slot outside [-1, record_slots) */
+#define KDA_ROW_BAD_PENDING 8  /* pending count outside [0, window] */
+
+#define KDA_HEAD_DIM 128
+#define KDA_MAX_WINDOW 8
+/* elements (bf16) per token record: k, v, g_raw (3 x 128), beta_raw, padding */
+#define KDA_RECORD_STRIDE 392
+
+typedef struct kda_config {
+    int32_t num_heads;        /* H >= 1 */
+    int32_t head_dim;         /* must be 128 (K = V) */
+    int32_t window;           /* Q = 1 + num_spec, 1..8 */
+    int32_t num_slots;        /* S: slots of the state pool (slot 0 = null) */
+    int32_t record_slots;     /* R: record slots (the scratch row excluded) */
+    int32_t use_lower_bound;  /* 1: bounded sigmoid gate, 0: softplus gate */
+    float lower_bound;        /* < 0, used when use_lower_bound == 1 */
+    float scale;              /* multiplies the normalised q (head_dim^-0.5) */
+    int64_t stride_q_t;       /* token strides in elements; q, k, v and g_raw */
+    int64_t stride_k_t;       /*   need multiples of 4 and 8-byte aligned bases */
+    int64_t stride_v_t;
+    int64_t stride_g_t;
+    int64_t stride_beta_t;    /* any positive stride */
+} kda_config;
+
+/* Bytes of the records buffer for H heads, window Q and R record slots:
+ * (R + 1) * H * Q * KDA_RECORD_STRIDE * 2.  Returns 0 for invalid sizes. */
+size_t kda_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots);
+
+/*
+ * kda_verify -- speculative verify from each row's checkpoint
+ * ([GLM] `_verify_kernel` / `kda_recoverssm_verify`).
+ *
+ * For each row b with T = cu_seqlens[b+1] - cu_seqlens[b] tokens and state
+ * slot s = state_indices[b] > 0, and each head h, starting from the fp32
+ * tile state_pool[s][h]:
+ *   per token: q^ = q/sqrt(|q|^2+1e-6)*scale, k^ = k/sqrt(|k|^2+1e-6),
+ *   x = g_raw + g_bias[h], g = lower_bound*sigmoid(exp(A_log[h])*x) (bounded)
+ *   or -exp(A_log[h])*softplus(x), beta = sigmoid(beta_raw),
+ *   S <- S*diag(exp(g)); v' = beta*(v - S k^); S <- S + v' k^T; o = S q^.
+ * Writes o (bf16, round to nearest even) to out[token][h][:], and the
+ * token's raw k, v, g_raw, beta_raw to record slot r = record_rows[b] (or b),
+ * position t.  The pool is NOT written, except by the deferred fold below.
+ *
+ * Deferred fold ([KIMI]: the next verify replays the pending count in the
+ * same pass): if pending != NULL, r >= 0 and p = pending[r] > 0, the first p
+ * records of slot r (the previous step's accepted tokens) are replayed from
+ * the checkpoint first; the folded state is written back to state_pool[s][h]
+ * and the new tokens run from it.  This happens even when T == 0.  pending is
+ * read, never written: the commit after this step rewrites it.
+ *
+ * trajectory_out (tests only; NULL in production): fp32 [T_total][H][V][K],
+ * the state after every token, i.e. what the full-state path would store.
+ *
+ * q, k, v, g_raw, beta_raw: bf16 inputs (see strides in cfg).
+ * A_log: fp32 [H]; g_bias: fp32 [H * 128] (per channel).
+ * out: bf16 [T_total][H][128], contiguous.  Rows that are skipped leave their
+ * out entries and records untouched.
+ * B: number of rows (B == 0: no launch, KDA_OK).
+ */
+kda_status kda_verify(const kda_config *cfg,
+                      const void *q, const void *k, const void *v,
+                      const void *g_raw, const void *beta_raw,
+                      const float *A_log, const float *g_bias,
+                      float *state_pool,
+                      const int32_t *cu_seqlens, const int32_t *state_indices,
+                      int32_t B,
+                      const int32_t *record_rows, const int32_t *pending,
+                      void *records, void *out, float *trajectory_out,
+                      int32_t *error_word, void *stream);
+
+/*
+ * kda_commit -- fold each row's accepted tokens into its checkpoint
+ * ([GLM] `_prepare_commit_plan_kernel` + `Glm5NextRecoverSSMCommitContext.commit`;
+ * [KIMI] `KDADeferredCommitContext.commit` with record_rows/pending/eager).
+ *
+ * Per row: n = min(max(num_accepted[b], 0), T, Q); the row is valid iff
+ * state_indices[b] > 0, n > 0 and its record slot r >= 0.
+ * Eager mode (pending == NULL): a valid row replays its first n records from
+ * state_pool[s][h] and writes the resulting state once (bit-identical to the
+ * state the verify computed after its n-th token: same kernels, same order).
+ * Deferred mode (pending != NULL): for every row with r >= 0, pending[r] is
+ * set to n if the row is valid and not eager, else 0; rows with
+ * eager[b] != 0 (eager may be NULL: no row) are committed now as above.
+ * num_accepted: int32 [B].  eager: uint8 [B] or NULL.
+ */
+kda_status kda_commit(const kda_config *cfg,
+                      const float *A_log, const float *g_bias,
+                      float *state_pool,
+                      const int32_t *cu_seqlens, const int32_t *state_indices,
+                      int32_t B,
+                      const int32_t *num_accepted,
+                      const int32_t *record_rows, const void *records,
+                      int32_t *pending, const uint8_t *eager,
+                      int32_t *error_word, void *stream);
+
+/*
+ * kda_flush -- fold pending replays into the checkpoints in place
+ * ([KIMI] `KDADeferredCommitContext.flush`), for a verify that does not fold
+ * (pending == NULL) or before exporting a checkpoint.  For each row with
+ * s > 0 and r >= 0 and p = pending[r] > 0, replays p records and writes the
+ * state.  pending is left as it is; the commit after the next step rewrites it.
+ * The rows' token counts play no part, so no cu_seqlens is taken.
+ */
+kda_status kda_flush(const kda_config *cfg,
+                     const float *A_log, const float *g_bias,
+                     float *state_pool,
+                     const int32_t *state_indices, int32_t B,
+                     const int32_t *record_rows, const void *records,
+                     const int32_t *pending,
+                     int32_t *error_word, void *stream);
+
+/* Name of a status code (static string). */
+const char *kda_status_string(kda_status status);
+
+/* ABI version of this header: bumped on any signature or layout change. */
+int32_t kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_KDA_H */

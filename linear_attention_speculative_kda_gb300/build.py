@@ -1,0 +1,74 @@
+"""Compile the CUDA library ``libkda.so`` in-tree for sm_103a.
+
+One translation unit, one ``-gencode`` (compute_103a / sm_103a), the CUDA
+runtime linked statically so the library only needs the driver at run time.
+"""
+
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+SOURCES = [os.path.join(CSRC, "kda_kernels.cu")]
+DEPENDS = SOURCES + [
+    os.path.join(CSRC, "kda_device.cuh"),
+    os.path.join(ROOT, "include", "kda.h"),
+]
+LIBRARY = os.path.join(PKG, "libkda.so")
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc_path() -> str:
+    cand = shutil.which("nvcc")
+    if cand:
+        return cand
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    return os.path.join(cuda_home, "bin", "nvcc")
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIBRARY):
+        return True
+    built = os.path.getmtime(LIBRARY)
+    return any(os.path.getmtime(src) > built for src in DEPENDS)
+
+
+def compile_command(output: str, extra=()) -> list[str]:
+    return [
+        nvcc_path(),
+        *ARCH_FLAGS,
+        "-O3",
+        "-lineinfo",
+        "-std=c++17",
+        "-shared",
+        "-Xcompiler",
+        "-fPIC",
+        "-cudart",
+        "static",
+        "-I",
+        os.path.join(ROOT, "include"),
+        *extra,
+        "-o",
+        output,
+        *SOURCES,
+    ]
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Build ``libkda.so`` if any source is newer than it; return its path."""
+    if not force and not _stale():
+        return LIBRARY
+    tmp = LIBRARY + f".tmp{os.getpid()}"
+    extra = ["-Xptxas", "-v"] if verbose else []
+    subprocess.run(compile_command(tmp, extra), check=True)
+    os.replace(tmp, LIBRARY)
+    return LIBRARY
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -1,0 +1,320 @@
+// Device building blocks of the KDA verify / commit kernels (sm_103a).
+//
+// One CTA owns one (request row, head) state tile S (128 x 128 fp32, row v,
+// column k) for the whole window, in registers.  256 threads = 8 warps; warp
+// w owns rows 16w .. 16w+15.  Inside a warp, lane = 8*g + j: the thread owns
+// the 4 rows 16w + 4g + i (i = 0..3) and, of each row, the 16 columns
+// 32m + 4j + c (m = 0..3, c = 0..3), held as float4 h[i][m].  A row therefore
+// lives in the 8 lanes that share g, and its dot products (S k^, S q^) are
+// reduced across those 8 lanes with shuffles only: no shared memory and no
+// block barrier inside the token loop.
+//
+// The per-token vectors that do not depend on the state (k^, q^, exp(g),
+// beta, v) are computed once per CTA per token by one warp and kept in shared
+// memory; the token loop reads them with conflict-free broadcast loads.
+//
+// Bit-exactness of commit against verify: the verify, the commit replay, the
+// deferred fold and the flush all run `token_step` below with the same thread
+// mapping, the same explicit round-to-nearest intrinsics (no contraction left
+// to the compiler) and the same reduction tree, so the state after token n is
+// the same bits whichever kernel computes it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kD = 128;             // head dim, K = V
+constexpr int kThreads = 256;       // threads per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxQ = 8;            // window limit
+constexpr int kRecStride = 392;     // bf16 elements per token record
+constexpr int kRecV = 128;          // offset of v inside a token record
+constexpr int kRecG = 256;          // offset of g_raw
+constexpr int kRecBeta = 384;       // offset of beta_raw
+constexpr unsigned kFull = 0xffffffffu;
+
+// Row-check bits (same values as the public header's KDA_ROW_* macros).
+constexpr int kBadLength = 1;
+constexpr int kBadSlot = 2;
+constexpr int kBadRecord = 4;
+constexpr int kBadPending = 8;
+
+// Everything a launch needs; passed by value as the kernel parameter.
+struct Params {
+    int H, Q, S, R, B;
+    int bounded;
+    float lower_bound;
+    float scale;
+    long long stride_q, stride_k, stride_v, stride_g, stride_beta;
+    const __nv_bfloat16 *q, *k, *v, *g, *beta;
+    const float *A_log, *g_bias;
+    float *pool;
+    const int *cu_seqlens, *state_indices, *record_rows;
+    const int *pending_in;     // verify fold / flush
+    int *pending_out;          // deferred commit
+    const int *num_accepted;
+    const uint8_t *eager;
+    __nv_bfloat16 *records;
+    __nv_bfloat16 *out;
+    float *traj;
+    int *err;
+};
+
+// Per-token vectors of one window, in shared memory.  Slots [0, p) hold the
+// folded (recorded) tokens, [p, p + T) the new ones; q^ only for new tokens.
+struct TokenSmem {
+    float kh[2 * kMaxQ][kD];
+    float e[2 * kMaxQ][kD];
+    float v[2 * kMaxQ][kD];
+    float qh[kMaxQ][kD];
+    float beta[2 * kMaxQ];
+};
+
+// ---------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
+    float4 f;
+    f.x = __uint_as_float(u.x << 16);
+    f.y = __uint_as_float(u.x & 0xffff0000u);
+    f.z = __uint_as_float(u.y << 16);
+    f.w = __uint_as_float(u.y & 0xffff0000u);
+    return f;
+}
+
+// Butterfly sum over the 32 lanes: every lane ends with the same bits
+// (IEEE addition is commutative, and each step pairs lanes symmetrically).
+__device__ __forceinline__ float warp_allsum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(kFull, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float sumsq4(float4 a) {
+    float s = __fmul_rn(a.x, a.x);
+    s = __fmaf_rn(a.y, a.y, s);
+    s = __fmaf_rn(a.z, a.z, s);
+    s = __fmaf_rn(a.w, a.w, s);
+    return s;
+}
+
+// 1 / sqrt(sum + 1e-6), correctly rounded sqrt and division.
+__device__ __forceinline__ float inv_l2(float sum) {
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(sum, 1e-6f)));
+}
+
+// exp(g) for one channel, x = g_raw + g_bias, a = exp(A_log[h]).
+// Bounded gate: g = lb * sigmoid(a x) = lb / (1 + exp(-a x)).
+// Softplus gate: g = -a * softplus(x), softplus(x) = x for x > 20.
+__device__ __forceinline__ float decay_factor(float x, float a, bool bounded, float lb) {
+    float g;
+    if (bounded) {
+        g = __fdiv_rn(lb, __fadd_rn(1.0f, expf(-__fmul_rn(a, x))));
+    } else {
+        float sp = x > 20.0f ? x : log1pf(expf(x));
+        g = -__fmul_rn(a, sp);
+    }
+    return expf(g);
+}
+
+__device__ __forceinline__ float sigmoidf_rn(float x) {
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
+}
+
+// --------------------------------------------------------- token prologue --
+//
+// One warp prepares one token: lane L owns channels 4L .. 4L+3.  Raw inputs
+// arrive as 4 bf16 per lane (8-byte loads; a token-head row is 256
+// contiguous bytes).  The k^ / q^ norms are warp-wide sums.
+
+struct RawToken {
+    uint2 k, v, g;      // 4 bf16 each
+    uint32_t beta;      // bf16 bits in the low half (lane 0 only)
+};
+
+__device__ __forceinline__ void prep_token(TokenSmem &sm, int slot, const RawToken &raw,
+                                           const float4 bias, float a, bool bounded,
+                                           float lb, int lane) {
+    const float4 k = bf16x4_to_float4(raw.k);
+    const float ik = inv_l2(warp_allsum(sumsq4(k)));
+    float4 kh;
+    kh.x = __fmul_rn(k.x, ik);
+    kh.y = __fmul_rn(k.y, ik);
+    kh.z = __fmul_rn(k.z, ik);
+    kh.w = __fmul_rn(k.w, ik);
+    const float4 g = bf16x4_to_float4(raw.g);
+    float4 e;
+    e.x = decay_factor(__fadd_rn(g.x, bias.x), a, bounded, lb);
+    e.y = decay_factor(__fadd_rn(g.y, bias.y), a, bounded, lb);
+    e.z = decay_factor(__fadd_rn(g.z, bias.z), a, bounded, lb);
+    e.w = decay_factor(__fadd_rn(g.w, bias.w), a, bounded, lb);
+    *reinterpret_cast<float4 *>(&sm.kh[slot][4 * lane]) = kh;
+    *reinterpret_cast<float4 *>(&sm.e[slot][4 * lane]) = e;
+    *reinterpret_cast<float4 *>(&sm.v[slot][4 * lane]) = bf16x4_to_float4(raw.v);
+    if (lane == 0) sm.beta[slot] = sigmoidf_rn(bf16_bits_to_float(raw.beta));
+}
+
+__device__ __forceinline__ void prep_query(TokenSmem &sm, int slot, uint2 qraw, float scale,
+                                           int lane) {
+    const float4 q = bf16x4_to_float4(qraw);
+    const float iq = inv_l2(warp_allsum(sumsq4(q)));
+    float4 qh;
+    qh.x = __fmul_rn(__fmul_rn(q.x, iq), scale);
+    qh.y = __fmul_rn(__fmul_rn(q.y, iq), scale);
+    qh.z = __fmul_rn(__fmul_rn(q.z, iq), scale);
+    qh.w = __fmul_rn(__fmul_rn(q.w, iq), scale);
+    *reinterpret_cast<float4 *>(&sm.qh[slot][4 * lane]) = qh;
+}
+
+__device__ __forceinline__ RawToken load_record(const __nv_bfloat16 *rec, int lane) {
+    RawToken r;
+    const uint2 *base = reinterpret_cast<const uint2 *>(rec);
+    r.k = base[lane];
+    r.v = base[kRecV / 4 + lane];
+    r.g = base[kRecG / 4 + lane];
+    r.beta = lane == 0 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(rec)[kRecBeta])
+                       : 0u;
+    return r;
+}
+
+__device__ __forceinline__ void store_record(__nv_bfloat16 *rec, const RawToken &r, int lane) {
+    uint2 *base = reinterpret_cast<uint2 *>(rec);
+    base[lane] = r.k;
+    base[kRecV / 4 + lane] = r.v;
+    base[kRecG / 4 + lane] = r.g;
+    if (lane == 0) reinterpret_cast<uint16_t *>(rec)[kRecBeta] = static_cast<uint16_t>(r.beta);
+}
+
+// ------------------------------------------------------------ state tile --
+
+struct Lane {
+    int w, g, j, lane;
+    __device__ __forceinline__ int row(int i) const { return 16 * w + 4 * g + i; }
+    __device__ __forceinline__ int col(int m) const { return 32 * m + 4 * j; }
+};
+
+__device__ __forceinline__ void load_tile(float4 (&h)[4][4], const float *tile, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            h[i][m] = *reinterpret_cast<const float4 *>(tile + L.row(i) * kD + L.col(m));
+}
+
+__device__ __forceinline__ void store_tile(const float4 (&h)[4][4], float *tile, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4 *>(tile + L.row(i) * kD + L.col(m)) = h[i][m];
+}
+
+// Row dot products of the thread's 4 rows with a vector x (its 16 columns),
+// in a fixed order: two interleaved partial sums per row (even and odd
+// columns of each float4), then their sum.
+__device__ __forceinline__ void row_partials(const float4 (&h)[4][4], const float4 (&x)[4],
+                                             float (&part)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float a0 = __fmul_rn(h[i][0].x, x[0].x);
+        float a1 = __fmul_rn(h[i][0].y, x[0].y);
+        a0 = __fmaf_rn(h[i][0].z, x[0].z, a0);
+        a1 = __fmaf_rn(h[i][0].w, x[0].w, a1);
+#pragma unroll
+        for (int m = 1; m < 4; ++m) {
+            a0 = __fmaf_rn(h[i][m].x, x[m].x, a0);
+            a1 = __fmaf_rn(h[i][m].y, x[m].y, a1);
+            a0 = __fmaf_rn(h[i][m].z, x[m].z, a0);
+            a1 = __fmaf_rn(h[i][m].w, x[m].w, a1);
+        }
+        part[i] = __fadd_rn(a0, a1);
+    }
+}
+
+// Sum the 4 row partials over the 8 lanes of the row group (lane bits 0..2)
+// by a transpose-reduce: after it, lane j holds the full sum of row
+// R(j) = 2*bit2(j) + bit1(j); lanes j and j^1 hold identical bits.
+__device__ __forceinline__ float reduce_rows(const float (&part)[4], int j) {
+    const bool hi = (j & 4) != 0;
+    const float send0 = hi ? part[0] : part[2];
+    const float send1 = hi ? part[1] : part[3];
+    const float keep0 = hi ? part[2] : part[0];
+    const float keep1 = hi ? part[3] : part[1];
+    const float t0 = __fadd_rn(keep0, __shfl_xor_sync(kFull, send0, 4));
+    const float t1 = __fadd_rn(keep1, __shfl_xor_sync(kFull, send1, 4));
+    const bool mid = (j & 2) != 0;
+    const float send = mid ? t0 : t1;
+    const float keep = mid ? t1 : t0;
+    const float u = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 2));
+    return __fadd_rn(u, __shfl_xor_sync(kFull, u, 1));
+}
+
+__device__ __forceinline__ int reduced_row(int j) { return 2 * ((j >> 2) & 1) + ((j >> 1) & 1); }
+
+// One token of the recurrence on the thread's part of the tile:
+//   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T
+// and, when kOut, o = S q^ written as bf16 to out_row (128 outputs).
+template <bool kOut>
+__device__ __forceinline__ void token_step(float4 (&h)[4][4], const TokenSmem &sm, int slot,
+                                           int qslot, const Lane &L,
+                                           __nv_bfloat16 *out_row) {
+    float4 kk[4], ee[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        kk[m] = *reinterpret_cast<const float4 *>(&sm.kh[slot][L.col(m)]);
+        ee[m] = *reinterpret_cast<const float4 *>(&sm.e[slot][L.col(m)]);
+    }
+    // decay along K
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            h[i][m].x = __fmul_rn(h[i][m].x, ee[m].x);
+            h[i][m].y = __fmul_rn(h[i][m].y, ee[m].y);
+            h[i][m].z = __fmul_rn(h[i][m].z, ee[m].z);
+            h[i][m].w = __fmul_rn(h[i][m].w, ee[m].w);
+        }
+    // u = S k^ for the 4 rows, reduced over the row group
+    float part[4];
+    row_partials(h, kk, part);
+    const float u = reduce_rows(part, L.j);
+    const int R = reduced_row(L.j);
+    const float vr = sm.v[slot][L.row(R)];
+    const float vp = __fmul_rn(sm.beta[slot], __fsub_rn(vr, u));
+    // every lane of the group gets v' of its 4 rows (lanes 2i hold row i)
+    const int base = L.lane & ~7;
+    float vpi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) vpi[i] = __shfl_sync(kFull, vp, base + 2 * i);
+    // rank-one update
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            h[i][m].x = __fmaf_rn(vpi[i], kk[m].x, h[i][m].x);
+            h[i][m].y = __fmaf_rn(vpi[i], kk[m].y, h[i][m].y);
+            h[i][m].z = __fmaf_rn(vpi[i], kk[m].z, h[i][m].z);
+            h[i][m].w = __fmaf_rn(vpi[i], kk[m].w, h[i][m].w);
+        }
+    if constexpr (kOut) {
+        float4 qq[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            qq[m] = *reinterpret_cast<const float4 *>(&sm.qh[qslot][L.col(m)]);
+        float opart[4];
+        row_partials(h, qq, opart);
+        const float o = reduce_rows(opart, L.j);
+        if ((L.j & 1) == 0) out_row[L.row(R)] = __float2bfloat16_rn(o);
+    }
+}
+
+__device__ __forceinline__ void flag_error(int *err, int bits) {
+    if (err != nullptr) atomicOr(err, bits);
+}
+
+}  // namespace kda

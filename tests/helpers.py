@@ -38,3 +38,97 @@ def oracle_step(wl: W.Workload, step: int = 0, cu_seqlens=None, state_indices=No
 
 def oracle_cache(wl: W.Workload) -> O.Cache:
     return O.Cache(wl.pool.numpy(), wl.spec.record_slots)
+
+
+# --------------------------------------------------------------- GPU side --
+
+class GpuRun:
+    """Device copies of a workload plus the buffers the library writes."""
+
+    def __init__(self, wl: W.Workload, device="cuda", with_traj=False, sentinel=True):
+        from linear_attention_speculative_kda_gb300 import api
+        sp = wl.spec
+        self.wl = wl
+        self.dev = torch.device(device)
+        d = self.dev
+        self.A_log = wl.A_log.to(d)
+        self.g_bias = wl.g_bias.to(d)
+        self.pool = wl.pool.to(d)
+        self.pool0 = self.pool.clone()
+        self.cu = wl.cu_seqlens.to(d)
+        self.slots = wl.state_indices.to(d)
+        self.record_rows = None if wl.record_rows is None else wl.record_rows.to(d)
+        self.steps = []
+        for st in wl.steps:
+            self.steps.append(dict(
+                qkv=st.qkv.to(d), beta_buf=st.beta_buf.to(d), g_raw=st.g_raw.to(d),
+                num_accepted=st.num_accepted.to(d),
+                eager=None if st.eager is None else st.eager.to(d)))
+        T = wl.total_tokens
+        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d)
+        self.out = torch.empty((T, sp.H, sp.D), dtype=torch.bfloat16, device=d)
+        if sentinel:
+            self.records.fill_(-7.0)
+            self.out.fill_(-9.0)
+        self.traj = (torch.full((T, sp.H, sp.D, sp.D), float("nan"), device=d)
+                     if with_traj else None)
+        self.pending = torch.zeros(sp.record_slots, dtype=torch.int32, device=d)
+        self.err = torch.zeros(1, dtype=torch.int32, device=d)
+
+    def kw(self):
+        sp = self.wl.spec
+        return dict(window=sp.Q, record_slots=sp.record_slots,
+                    lower_bound=sp.lower_bound if sp.bounded else None)
+
+    def verify(self, step=0, pending=False, cu=None, slots=None, record_rows="default"):
+        from linear_attention_speculative_kda_gb300 import api
+        s = self.steps[step]
+        H = self.wl.spec.H
+        rr = self.record_rows if isinstance(record_rows, str) else record_rows
+        api.kda_verify(s["qkv"][:, 0], s["qkv"][:, 1], s["qkv"][:, 2], s["g_raw"],
+                       s["beta_buf"][:, :H], self.A_log, self.g_bias, self.pool,
+                       self.cu if cu is None else cu, self.slots if slots is None else slots,
+                       self.records, self.out, record_rows=rr,
+                       pending=self.pending if pending else None, trajectory_out=self.traj,
+                       error_word=self.err, **self.kw())
+        return self.out
+
+    def commit(self, step=0, deferred=False, eager="default", num_accepted=None, cu=None,
+               slots=None, record_rows="default"):
+        from linear_attention_speculative_kda_gb300 import api
+        s = self.steps[step]
+        rr = self.record_rows if isinstance(record_rows, str) else record_rows
+        em = s["eager"] if isinstance(eager, str) else eager
+        api.kda_commit(self.A_log, self.g_bias, self.pool, self.cu if cu is None else cu,
+                       self.slots if slots is None else slots,
+                       s["num_accepted"] if num_accepted is None else num_accepted,
+                       self.records, record_rows=rr, pending=self.pending if deferred else None,
+                       eager=em if deferred else None, error_word=self.err, **self.kw())
+
+    def flush(self, slots=None, record_rows="default"):
+        from linear_attention_speculative_kda_gb300 import api
+        rr = self.record_rows if isinstance(record_rows, str) else record_rows
+        api.kda_flush(self.A_log, self.g_bias, self.pool, self.slots if slots is None else slots,
+                      self.records, self.pending, record_rows=rr, error_word=self.err,
+                      **self.kw())
+
+
+def assert_out_close(gpu_out: torch.Tensor, oracle_out: np.ndarray, rows_tokens=None,
+                     atol=2e-3):
+    """bf16 outputs: |gpu - oracle| <= 2e-3 element by element, on the entries
+    the oracle wrote (NaN elsewhere)."""
+    g = f64(gpu_out)
+    mask = ~np.isnan(oracle_out)
+    assert mask.any()
+    diff = np.abs(g[mask] - oracle_out[mask])
+    assert diff.max() <= atol, f"max |out - oracle| = {diff.max():.3e} > {atol}"
+    return float(diff.max())
+
+
+def assert_state_close(gpu_tile: np.ndarray, oracle_tile: np.ndarray, rel=1e-5):
+    """fp32 states, normwise per (slot, head) tile:
+    max |gpu - oracle| <= rel * max |oracle|."""
+    err = np.abs(gpu_tile - oracle_tile).max()
+    ref = np.abs(oracle_tile).max()
+    assert err <= rel * ref, f"state error {err:.3e} > {rel} * {ref:.3e}"
+    return float(err / ref) if ref > 0 else 0.0

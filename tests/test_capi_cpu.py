@@ -1,0 +1,105 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every entry
+point ``include/kda.h`` declares, and its host-side argument checks return
+the documented status codes.  No case here reaches a kernel launch: each one
+fails a host check (or has B == 0), so nothing touches a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_speculative_kda_gb300 import api
+from linear_attention_speculative_kda_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return api.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert set(names) == set(api.EXPORTED)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert lib.kda_abi_version() == 1
+    assert lib.kda_status_string(api.KDA_ERR_CUDA) == b"KDA_ERR_CUDA"
+
+
+def test_records_bytes(lib):
+    assert api.kda_records_bytes(16, 4, 1024) == 1025 * 16 * 4 * 392 * 2
+    assert api.kda_records_bytes(1, 8, 0) == 1 * 8 * 392 * 2
+    assert api.kda_records_bytes(0, 4, 4) == 0
+    assert api.kda_records_bytes(4, 9, 4) == 0
+    assert api.kda_records_bytes(4, 4, -1) == 0
+
+
+FAKE = 0x100000  # an aligned address that is never dereferenced
+
+
+def _cfg(**kw):
+    base = dict(num_heads=2, window=4, num_slots=8, record_slots=4, lower_bound=None,
+                strides=(3 * 2 * 128, 3 * 2 * 128, 3 * 2 * 128, 2 * 128, 10))
+    base.update(kw)
+    return api.make_config(base["num_heads"], base["window"], base["num_slots"],
+                           base["record_slots"], lower_bound=base["lower_bound"],
+                           strides=base["strides"], head_dim=base.get("head_dim", 128))
+
+
+def _verify(lib, cfg, B=3, **ptrs):
+    p = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, beta=FAKE, a_log=FAKE, g_bias=FAKE, pool=FAKE,
+             cu=FAKE, slots=FAKE, rr=None, pending=None, records=FAKE, out=FAKE, traj=None,
+             err=None)
+    p.update(ptrs)
+    cfgp = None if cfg is None else ctypes.byref(cfg)
+    return lib.kda_verify(cfgp, p["q"], p["k"], p["v"], p["g"], p["beta"], p["a_log"],
+                          p["g_bias"], p["pool"], p["cu"], p["slots"], B, p["rr"],
+                          p["pending"], p["records"], p["out"], p["traj"], p["err"], None)
+
+
+def test_verify_host_checks(lib):
+    assert _verify(lib, None) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(head_dim=64)) == api.KDA_ERR_UNSUPPORTED
+    assert _verify(lib, _cfg(window=9)) == api.KDA_ERR_UNSUPPORTED
+    assert _verify(lib, _cfg(window=0)) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(num_heads=0)) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(), B=-1) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(), q=None) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(), out=None) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(), q=FAKE + 2) == api.KDA_ERR_INVALID_ARG       # not 8-byte aligned
+    assert _verify(lib, _cfg(), pool=FAKE + 4) == api.KDA_ERR_INVALID_ARG    # not 16-byte aligned
+    assert _verify(lib, _cfg(), traj=FAKE + 8) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(strides=(770, 768, 768, 256, 1))) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(strides=(768, 768, 768, 256, 0))) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(lower_bound=0.5)) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(lower_bound=float("-inf"))) == api.KDA_ERR_INVALID_ARG
+    assert _verify(lib, _cfg(record_slots=2), B=3) == api.KDA_ERR_INVALID_ARG  # B > R, no rr
+    # nothing to do: OK without any launch
+    assert _verify(lib, _cfg(), B=0) == api.KDA_OK
+
+
+def test_commit_and_flush_host_checks(lib):
+    cfg = _cfg()
+    c = ctypes.byref(cfg)
+    # eager mask without pending is meaningless
+    assert lib.kda_commit(c, FAKE, FAKE, FAKE, FAKE, FAKE, 3, FAKE, None, FAKE, None, FAKE,
+                          None, None) == api.KDA_ERR_INVALID_ARG
+    assert lib.kda_commit(c, FAKE, FAKE, FAKE, FAKE, FAKE, 3, None, None, FAKE, None, None,
+                          None, None) == api.KDA_ERR_INVALID_ARG
+    assert lib.kda_commit(c, FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, None, FAKE, None, None,
+                          None, None) == api.KDA_OK
+    assert lib.kda_flush(c, FAKE, FAKE, FAKE, FAKE, 3, None, FAKE, None, None,
+                         None) == api.KDA_ERR_INVALID_ARG
+    assert lib.kda_flush(c, FAKE, FAKE, FAKE, FAKE, 0, None, FAKE, FAKE, None,
+                         None) == api.KDA_OK
