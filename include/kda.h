@@ -127,7 +127,8 @@ size_t kda_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots
  * A_log: fp32 [H]; g_bias: fp32 [H * 128] (per channel).
  * out: bf16 [T_total][H][128], contiguous.  Rows that are skipped leave their
  * out entries and records untouched.
- * B: number of rows (B == 0: no launch, KDA_OK).
+ * B: number of rows (B == 0: KDA_OK without a launch, and no pointer is
+ * inspected, so empty tensors with NULL data pointers are accepted).
  */
 kda_status kda_verify(const kda_config *cfg,
                       const void *q, const void *k, const void *v,

@@ -237,7 +237,6 @@ Params base_params(const kda_config *cfg, int32_t B) {
 kda_status check_common(const kda_config *cfg, const float *A_log, const float *g_bias,
                         const float *pool, const int32_t *state_indices, int32_t B,
                         const int32_t *record_rows, const void *records) {
-    if (B < 0) return KDA_ERR_INVALID_ARG;
     if (!A_log || !g_bias || !pool || !state_indices || !records) return KDA_ERR_INVALID_ARG;
     if (!aligned(g_bias, 16) || !aligned(pool, 16) || !aligned(A_log, 4) ||
         !aligned(state_indices, 4) || !aligned(records, 16))
@@ -270,6 +269,8 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
                       int32_t *error_word, void *stream) {
     kda_status st = check_config(cfg);
     if (st != KDA_OK) return st;
+    if (B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
     st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
     if (st != KDA_OK) return st;
     if (!q || !k || !v || !g_raw || !beta_raw || !cu_seqlens || !out) return KDA_ERR_INVALID_ARG;
@@ -282,7 +283,6 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     for (int64_t s : strides)
         if (s < 1 || (s & 3) != 0) return KDA_ERR_INVALID_ARG;
     if (cfg->stride_beta_t < 1) return KDA_ERR_INVALID_ARG;
-    if (B == 0) return KDA_OK;
 
     Params p = base_params(cfg, B);
     p.q = static_cast<const __nv_bfloat16 *>(q);
@@ -318,13 +318,14 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
                       int32_t *error_word, void *stream) {
     kda_status st = check_config(cfg);
     if (st != KDA_OK) return st;
+    if (B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
     st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
     if (st != KDA_OK) return st;
     if (!cu_seqlens || !num_accepted) return KDA_ERR_INVALID_ARG;
     if (!aligned(cu_seqlens, 4) || !aligned(num_accepted, 4)) return KDA_ERR_INVALID_ARG;
     if (pending != nullptr && !aligned(pending, 4)) return KDA_ERR_INVALID_ARG;
     if (pending == nullptr && eager != nullptr) return KDA_ERR_INVALID_ARG;
-    if (B == 0) return KDA_OK;
 
     Params p = base_params(cfg, B);
     p.A_log = A_log;
@@ -355,10 +356,11 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
                      int32_t *error_word, void *stream) {
     kda_status st = check_config(cfg);
     if (st != KDA_OK) return st;
+    if (B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
     st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
     if (st != KDA_OK) return st;
     if (!pending || !aligned(pending, 4)) return KDA_ERR_INVALID_ARG;
-    if (B == 0) return KDA_OK;
 
     Params p = base_params(cfg, B);
     p.A_log = A_log;

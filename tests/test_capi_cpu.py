@@ -85,8 +85,10 @@ def test_verify_host_checks(lib):
     assert _verify(lib, _cfg(lower_bound=0.5)) == api.KDA_ERR_INVALID_ARG
     assert _verify(lib, _cfg(lower_bound=float("-inf"))) == api.KDA_ERR_INVALID_ARG
     assert _verify(lib, _cfg(record_slots=2), B=3) == api.KDA_ERR_INVALID_ARG  # B > R, no rr
-    # nothing to do: OK without any launch
+    # nothing to do: OK without any launch, pointers not inspected
     assert _verify(lib, _cfg(), B=0) == api.KDA_OK
+    assert _verify(lib, _cfg(), B=0, q=None, slots=None, cu=None) == api.KDA_OK
+    assert _verify(lib, _cfg(window=9), B=0) == api.KDA_ERR_UNSUPPORTED
 
 
 def test_commit_and_flush_host_checks(lib):
