@@ -109,45 +109,41 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch recorded by an ncu capture under profiles/, if the
+def profiled_traffic(launch: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    recorded from an ncu capture in profiles/ncu_<workload>.md, if that
     capture was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"ncu_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    m = re.search(r"traffic\[" + re.escape(launch) + r"\]:\s*([0-9.eE+]+)", text)
     if not m or not s or s.group(1) != kernel_source_hash():
         return None
     return float(m.group(1))
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling around the timed region.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Started before the warm-up so the sampler is running when the timed
+    region begins; ``mark(start, stop)`` gives the host wall-clock bounds of
+    the timed region and ``summary()`` keeps the samples taken inside it
+    (or the nearest one when the region is shorter than the 200 ms period).
+    """
+
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
         self.gpu_id = self._smi_id(device_index)
         self.proc = None
-        self.lines: list[str] = []
+        self.samples: list[tuple[float, list[str]]] = []
         self.thread = None
-
-    def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except (OSError, ValueError):
-            self.proc = None
-        return self
+        self.window = None
 
     @staticmethod
     def _smi_id(device_index: int) -> str:
@@ -163,12 +159,28 @@ class ClockSampler:
         ids = [v.strip() for v in vis.split(",") if v.strip()]
         return ids[device_index] if device_index < len(ids) else str(device_index)
 
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.samples.append((time.time(), [p.strip() for p in line.split(",")]))
+
+    def mark(self, start: float, stop: float):
+        self.window = (start, stop)
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.25)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -178,12 +190,17 @@ class ClockSampler:
                 self.thread.join(timeout=2)
 
     def summary(self):
+        rows = [(t, p) for t, p in self.samples if len(p) >= 9]
+        if self.window and rows:
+            lo, hi = self.window
+            inside = [(t, p) for t, p in rows if lo <= t <= hi + 0.2]
+            if not inside:
+                mid = 0.5 * (lo + hi)
+                inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+            rows = inside
         sms, maxes, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        for _, parts in rows:
             try:
                 sms.append(float(parts[1]))
                 maxes.append(float(parts[2]))
@@ -419,6 +436,7 @@ def run_ours(args):
     nl = len(names)
     bytes_per = dict(plan_bytes(wl))
 
+    clocks = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         eng.run_step()
     torch.cuda.synchronize()
@@ -432,12 +450,14 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        start.record(stream)
-        for k in range(args.steps):
-            eng.run_step(events[k])
-        stop.record(stream)
-        torch.cuda.synchronize()
+    t_start = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        eng.run_step(events[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(t_start, time.time())
+    clocks.__exit__(None, None, None)
     if world > 1:
         torch.distributed.barrier()
     ms_total = start.elapsed_time(stop)
@@ -465,11 +485,10 @@ def run_ours(args):
                                                                   per_kernel.values()))})
     dom = max(kernels, key=lambda x: x["share"])
     step_bytes = sum(bytes_per.values())
-    kname = "kda_verify" if dom["name"].startswith("verify") else "kda_commit"
     roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dom["gbs"] / peak,
                 "peak_source": f"{peak_src} ({'of measured' if peak_src == 'measured' else 'of fallback'})",
-                "traffic": profiled_traffic(f"{kname}_{dom['name']}", wl.spec.name),
+                "traffic": profiled_traffic(dom["name"], wl.spec.name),
                 "algorithmic_bytes_per_launch": dom["bytes_per_launch"]}
     step_gbs = step_bytes * args.steps / (ms_total / 1e3) / 1e9
 
@@ -542,7 +561,7 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="deferred2", choices=sorted(W.CONFIGS))
