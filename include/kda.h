@@ -72,6 +72,10 @@ typedef enum kda_status {
 #define KDA_ROW_BAD_SLOT    2  /* state index >= num_slots */
 #define KDA_ROW_BAD_RECORD  4  /* record slot outside [-1, record_slots) */
 #define KDA_ROW_BAD_PENDING 8  /* pending count outside [0, window] */
+/* A kernel gave up waiting (about 2 s) for one of its own asynchronous copies
+ * into shared memory and returned early; its remaining rows were not
+ * processed.  Not expected in normal operation. */
+#define KDA_ERR_WAIT_TIMEOUT 16
 
 #define KDA_HEAD_DIM 128
 #define KDA_MAX_WINDOW 8

@@ -31,6 +31,7 @@ ROW_BAD_LENGTH = 1
 ROW_BAD_SLOT = 2
 ROW_BAD_RECORD = 4
 ROW_BAD_PENDING = 8
+ERR_WAIT_TIMEOUT = 16
 
 EXPORTED = (
     "kda_records_bytes",

@@ -17,6 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "kda_kernels.cu")]
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "kda_device.cuh"),
+    os.path.join(CSRC, "kda_async.cuh"),
     os.path.join(ROOT, "include", "kda.h"),
 ]
 LIBRARY = os.path.join(PKG, "libkda.so")

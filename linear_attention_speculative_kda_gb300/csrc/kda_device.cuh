@@ -35,11 +35,12 @@ constexpr int kRecG = 256;          // offset of g_raw
 constexpr int kRecBeta = 384;       // offset of beta_raw
 constexpr unsigned kFull = 0xffffffffu;
 
-// Row-check bits (same values as the public header's KDA_ROW_* macros).
+// Error-word bits (same values as the public header's macros).
 constexpr int kBadLength = 1;
 constexpr int kBadSlot = 2;
 constexpr int kBadRecord = 4;
 constexpr int kBadPending = 8;
+constexpr int kErrWaitTimeout = 16;
 
 // Everything a launch needs; passed by value as the kernel parameter.
 struct Params {

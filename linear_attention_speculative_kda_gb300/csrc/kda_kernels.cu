@@ -15,6 +15,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "kda_async.cuh"
 #include "kda_device.cuh"
 #include "../../include/kda.h"
 
@@ -24,8 +25,9 @@ static_assert(kRecStride == KDA_RECORD_STRIDE, "record layout mismatch");
 static_assert(kD == KDA_HEAD_DIM, "head dim mismatch");
 static_assert(kMaxQ == KDA_MAX_WINDOW, "window mismatch");
 static_assert(kBadLength == KDA_ROW_BAD_LENGTH && kBadSlot == KDA_ROW_BAD_SLOT &&
-                  kBadRecord == KDA_ROW_BAD_RECORD && kBadPending == KDA_ROW_BAD_PENDING,
-              "row-check bits mismatch");
+                  kBadRecord == KDA_ROW_BAD_RECORD && kBadPending == KDA_ROW_BAD_PENDING &&
+                  kErrWaitTimeout == KDA_ERR_WAIT_TIMEOUT,
+              "error-word bits mismatch");
 
 // Row metadata shared by all kernels: token range, slot and record slot,
 // with the device-side checks.  Returns the error bits (0: usable row).
@@ -53,141 +55,283 @@ __device__ __forceinline__ __nv_bfloat16 *record_base(const Params &p, int r, in
     return p.records + ((size_t)(r + 1) * p.H + head) * (size_t)p.Q * kRecStride;
 }
 
-// Prepare `count` recorded tokens into smem slots [0, count).
-__device__ __forceinline__ void prep_records(TokenSmem &sm, const __nv_bfloat16 *rec, int count,
-                                             const float4 bias, float a, bool bounded, float lb,
-                                             int warp, int lane) {
-    for (int t = warp; t < count; t += kWarps) {
-        const RawToken raw = load_record(rec + (size_t)t * kRecStride, lane);
-        prep_token(sm, t, raw, bias, a, bounded, lb, lane);
-    }
-}
+// ------------------------------------------------------------- work items --
+//
+// A work item is one (row, head) tile with something to do.  Mode decides
+// what: the verify runs `p` folded (pending) record tokens then `T` new
+// tokens; the commit and the flush replay `p` record tokens.  Every mode
+// stores the state when p > 0.
 
-// ------------------------------------------------------------------ verify --
+enum class Mode { kVerify, kCommit, kFlush };
 
-template <bool kBounded>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const Params p) {
-    __shared__ __align__(16) TokenSmem sm;
-    const int b = blockIdx.x / p.H;
-    const int head = blockIdx.x - b * p.H;
-    const int tid = threadIdx.x;
-    Lane L;
-    L.lane = tid & 31;
-    L.w = tid >> 5;
-    L.g = L.lane >> 3;
-    L.j = L.lane & 7;
+struct Work {
+    int tile;  // -1: no more work for this CTA
+    int head, slot, r, bos, T, p;
+};
 
+// Plan one tile: row checks, the commit plan (n = clamp(accepted, 0,
+// min(T, Q)), valid iff slot > 0, n > 0, r >= 0), the deferred commit's
+// pending write.  Side effects (error bits, pending writes) only when
+// `side`; they are idempotent, so a tile planned twice is harmless.
+template <Mode kMode>
+__device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, Work &w) {
+    const int b = tile / p.H;
+    const int head = tile - b * p.H;
     Row row;
-    const int bad = read_row(p, b, true, row);
+    const int bad = read_row(p, b, kMode != Mode::kFlush, row);
     if (bad) {
-        if (head == 0 && tid == 0) flag_error(p.err, bad);
-        return;
+        if (side && head == 0) flag_error(p.err, bad);
+        return false;
     }
-    if (row.slot <= 0) return;  // null block: padding row
-    int pend = 0;
-    if (p.pending_in != nullptr && row.r >= 0) {
-        pend = p.pending_in[row.r];
-        if (pend < 0 || pend > p.Q) {
-            if (head == 0 && tid == 0) flag_error(p.err, kBadPending);
-            return;
+    int fold = 0, T = 0;
+    if constexpr (kMode == Mode::kVerify) {
+        if (row.slot <= 0) return false;  // null block: padding row
+        if (p.pending_in != nullptr && row.r >= 0) {
+            fold = p.pending_in[row.r];
+            if (fold < 0 || fold > p.Q) {
+                if (side && head == 0) flag_error(p.err, kBadPending);
+                return false;
+            }
         }
-    }
-    if (row.T == 0 && pend == 0) return;
-
-    float *tile = p.pool + ((size_t)row.slot * p.H + head) * (size_t)(kD * kD);
-    float4 h[4][4];
-    load_tile(h, tile, L);  // in flight while the token vectors are prepared
-
-    const float a = expf(p.A_log[head]);
-    const float4 bias = *reinterpret_cast<const float4 *>(p.g_bias + head * kD + 4 * L.lane);
-    __nv_bfloat16 *rec = record_base(p, row.r, head);
-
-    if (pend > 0) {  // the recorded tokens must be read before they are overwritten
-        prep_records(sm, rec, pend, bias, a, kBounded, p.lower_bound, L.w, L.lane);
-        __syncthreads();
-    }
-    for (int t = L.w; t < row.T; t += kWarps) {
-        const size_t tok = (size_t)(row.bos + t);
-        RawToken raw;
-        raw.k = *reinterpret_cast<const uint2 *>(p.k + tok * p.stride_k + head * kD + 4 * L.lane);
-        raw.v = *reinterpret_cast<const uint2 *>(p.v + tok * p.stride_v + head * kD + 4 * L.lane);
-        raw.g = *reinterpret_cast<const uint2 *>(p.g + tok * p.stride_g + head * kD + 4 * L.lane);
-        raw.beta = L.lane == 0
-                       ? (uint32_t) reinterpret_cast<const uint16_t *>(p.beta)[tok * p.stride_beta + head]
-                       : 0u;
-        const uint2 qraw =
-            *reinterpret_cast<const uint2 *>(p.q + tok * p.stride_q + head * kD + 4 * L.lane);
-        prep_token(sm, pend + t, raw, bias, a, kBounded, p.lower_bound, L.lane);
-        prep_query(sm, t, qraw, p.scale, L.lane);
-        store_record(rec + (size_t)t * kRecStride, raw, L.lane);
-    }
-    __syncthreads();
-
-    // deferred fold: replay the pending records, store the folded checkpoint
-    for (int t = 0; t < pend; ++t) token_step<false>(h, sm, t, 0, L, nullptr);
-    if (pend > 0) store_tile(h, tile, L);
-
-    for (int t = 0; t < row.T; ++t) {
-        const size_t tok = (size_t)(row.bos + t);
-        token_step<true>(h, sm, pend + t, t, L, p.out + (tok * p.H + head) * kD);
-        if (p.traj != nullptr) store_tile(h, p.traj + (tok * p.H + head) * (size_t)(kD * kD), L);
-    }
-}
-
-// --------------------------------------------------------- commit / flush --
-
-enum class Replay { kCommit, kFlush };
-
-template <bool kBounded, Replay kMode>
-__global__ void __launch_bounds__(kThreads, 2) replay_kernel(const Params p) {
-    __shared__ __align__(16) TokenSmem sm;
-    const int b = blockIdx.x / p.H;
-    const int head = blockIdx.x - b * p.H;
-    const int tid = threadIdx.x;
-    Lane L;
-    L.lane = tid & 31;
-    L.w = tid >> 5;
-    L.g = L.lane >> 3;
-    L.j = L.lane & 7;
-
-    Row row;
-    const int bad = read_row(p, b, kMode == Replay::kCommit, row);
-    if (bad) {
-        if (head == 0 && tid == 0) flag_error(p.err, bad);
-        return;
-    }
-    int n;
-    if constexpr (kMode == Replay::kCommit) {
-        // commit plan: accepted count clamped to [0, T] and to the window
-        n = min(max(p.num_accepted[b], 0), min(row.T, p.Q));
+        T = row.T;
+        if (T == 0 && fold == 0) return false;
+    } else if constexpr (kMode == Mode::kCommit) {
+        const int n = min(max(p.num_accepted[b], 0), min(row.T, p.Q));
         const bool valid = row.slot > 0 && n > 0 && row.r >= 0;
         if (p.pending_out != nullptr) {
             const bool now = p.eager != nullptr && p.eager[b] != 0;
-            if (head == 0 && tid == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
-            if (!now) return;
+            if (side && head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
+            if (!now) return false;
         }
-        if (!valid) return;
+        if (!valid) return false;
+        fold = n;
     } else {
-        if (row.slot <= 0 || row.r < 0) return;
-        n = p.pending_in[row.r];
+        if (row.slot <= 0 || row.r < 0) return false;
+        const int n = p.pending_in[row.r];
         if (n < 0 || n > p.Q) {
-            if (head == 0 && tid == 0) flag_error(p.err, kBadPending);
+            if (side && head == 0) flag_error(p.err, kBadPending);
+            return false;
+        }
+        if (n == 0) return false;
+        fold = n;
+    }
+    w.tile = tile;
+    w.head = head;
+    w.slot = row.slot;
+    w.r = row.r;
+    w.bos = row.bos;
+    w.T = T;
+    w.p = fold;
+    return true;
+}
+
+// The next work item of this CTA at or after tile `from` (tiles from,
+// from + stride, ...).  Each warp plans 32 candidate tiles at once, one per
+// lane, and takes the first that has work, so skipping idle tiles costs one
+// round of metadata loads per 32 of them.  All warps compute the same answer;
+// warp 0 alone performs the side effects.
+template <Mode kMode>
+__device__ __forceinline__ Work next_work(const Params &p, int from, int stride, int num_tiles,
+                                          int warp, int lane) {
+    Work w;
+    w.tile = -1;
+    for (int base = from; base < num_tiles; base += 32 * stride) {
+        const int t = base + lane * stride;
+        Work mine;
+        const bool has = t < num_tiles && plan_tile<kMode>(p, t, warp == 0, mine);
+        const unsigned ballot = __ballot_sync(kFull, has);
+        if (ballot != 0u) {
+            const int src = __ffs(ballot) - 1;
+            w.tile = __shfl_sync(kFull, mine.tile, src);
+            w.head = __shfl_sync(kFull, mine.head, src);
+            w.slot = __shfl_sync(kFull, mine.slot, src);
+            w.r = __shfl_sync(kFull, mine.r, src);
+            w.bos = __shfl_sync(kFull, mine.bos, src);
+            w.T = __shfl_sync(kFull, mine.T, src);
+            w.p = __shfl_sync(kFull, mine.p, src);
+            return w;
+        }
+    }
+    return w;
+}
+
+// ---------------------------------------------------------- shared memory --
+
+// Raw bf16 inputs of one work item, brought in by cp.async: slots [0, p)
+// are the folded record tokens, [p, p + T) the new tokens.
+struct RawSmem {
+    uint2 k[2 * kMaxQ][32];
+    uint2 v[2 * kMaxQ][32];
+    uint2 g[2 * kMaxQ][32];
+    uint2 q[kMaxQ][32];
+    uint2 tail[kMaxQ];          // record tails: beta_raw bits in the low half
+    uint32_t beta_new[kMaxQ];   // beta_raw bits of the new tokens
+};
+
+struct __align__(16) StepSmem {
+    float state[kD * kD];       // staging of the next tile's checkpoint (TMA)
+    TokenSmem tok;              // per-token vectors of the current item
+    RawSmem raw;                // raw inputs of the current / next item
+    uint64_t bar;               // completion of the staging copy
+    int ok;
+};
+
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
+
+__device__ __forceinline__ void issue_state(const Params &p, const Work &w, StepSmem &sm) {
+    const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
+    mbar_arrive_expect_tx(&sm.bar, kD * kD * 4);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        bulk_load(sm.state + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, &sm.bar);
+}
+
+template <Mode kMode>
+__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSmem &raw, int warp,
+                                          int lane) {
+    const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
+    for (int c = warp; c < 3 * w.p; c += kWarps) {
+        const int u = c / 3;
+        const int part = c - 3 * u;
+        const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
+        uint2 *dst = part == 0 ? raw.k[u] : (part == 1 ? raw.v[u] : raw.g[u]);
+        cp_async8(dst + lane, src + lane);
+    }
+    if (warp == kWarps - 1 && lane < w.p)
+        cp_async8(&raw.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
+    if constexpr (kMode == Mode::kVerify) {
+        for (int c = warp; c < 4 * w.T; c += kWarps) {
+            const int t = c >> 2;
+            const int part = c & 3;
+            const size_t tok = (size_t)(w.bos + t);
+            const __nv_bfloat16 *src;
+            uint2 *dst;
+            if (part == 0) {
+                src = p.k + tok * p.stride_k;
+                dst = raw.k[w.p + t];
+            } else if (part == 1) {
+                src = p.v + tok * p.stride_v;
+                dst = raw.v[w.p + t];
+            } else if (part == 2) {
+                src = p.g + tok * p.stride_g;
+                dst = raw.g[w.p + t];
+            } else {
+                src = p.q + tok * p.stride_q;
+                dst = raw.q[t];
+            }
+            cp_async8(dst + lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
+        }
+    }
+    cp_async_commit();
+}
+
+// ------------------------------------------------------------------ kernel --
+//
+// Persistent: gridDim.x CTAs (two per SM) walk the tiles b*H + head with a
+// stride of gridDim.x.  While a CTA computes one item from registers, the
+// next item's checkpoint streams into shared memory through the TMA unit and
+// its raw inputs through cp.async, so memory and arithmetic overlap.
+
+template <Mode kMode, bool kBounded>
+__global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int num_tiles) {
+    extern __shared__ __align__(128) unsigned char smem_bytes[];
+    StepSmem &sm = *reinterpret_cast<StepSmem *>(smem_bytes);
+    const int tid = threadIdx.x;
+    Lane L;
+    L.lane = tid & 31;
+    L.w = tid >> 5;
+    L.g = L.lane >> 3;
+    L.j = L.lane & 7;
+    const int stride = gridDim.x;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    Work cur = next_work<kMode>(p, blockIdx.x, stride, num_tiles, L.w, L.lane);
+    if (cur.tile < 0) return;
+    if (tid == 0) issue_state(p, cur, sm);
+    fetch_raw<kMode>(p, cur, sm.raw, L.w, L.lane);
+    uint32_t beta_next = 0;
+    if (kMode == Mode::kVerify && tid < cur.T)
+        beta_next = reinterpret_cast<const uint16_t *>(
+            p.beta)[(size_t)(cur.bos + tid) * p.stride_beta + cur.head];
+    uint32_t phase = 0;
+
+    while (true) {
+        // raw inputs of `cur` have landed (each thread waits for its own
+        // copies; the barrier publishes them and frees the token vectors)
+        cp_async_wait_all();
+        if (kMode == Mode::kVerify && tid < cur.T) sm.raw.beta_new[tid] = beta_next;
+        __syncthreads();
+
+        // per-token vectors of `cur`; the verify also writes its records
+        const float a = expf(p.A_log[cur.head]);
+        const float4 bias =
+            *reinterpret_cast<const float4 *>(p.g_bias + cur.head * kD + 4 * L.lane);
+        __nv_bfloat16 *rec = record_base(p, cur.r, cur.head);
+        for (int u = L.w; u < cur.p + cur.T; u += kWarps) {
+            RawToken rt;
+            rt.k = sm.raw.k[u][L.lane];
+            rt.v = sm.raw.v[u][L.lane];
+            rt.g = sm.raw.g[u][L.lane];
+            rt.beta = u < cur.p ? (sm.raw.tail[u].x & 0xffffu) : sm.raw.beta_new[u - cur.p];
+            prep_token(sm.tok, u, rt, bias, a, kBounded, p.lower_bound, L.lane);
+            if constexpr (kMode == Mode::kVerify) {
+                if (u >= cur.p) {
+                    const int t = u - cur.p;
+                    prep_query(sm.tok, t, sm.raw.q[t][L.lane], p.scale, L.lane);
+                    store_record(rec + (size_t)t * kRecStride, rt, L.lane);
+                }
+            }
+        }
+
+        // checkpoint of `cur`: staged by the TMA unit
+        if (tid == 0) sm.ok = mbar_wait_bounded(&sm.bar, phase, kWaitBudget) ? 1 : 0;
+        __syncthreads();
+        if (!sm.ok) {
+            if (tid == 0) {
+                flag_error(p.err, kErrWaitTimeout);
+                mbar_wait_bounded(&sm.bar, phase, kWaitBudget);
+            }
             return;
         }
-        if (n == 0) return;
+        mbar_try_wait(&sm.bar, phase);  // completed phase: acquires the staged bytes
+        phase ^= 1u;
+        float4 h[4][4];
+        load_tile(h, sm.state, L);
+        __syncthreads();  // staging buffer and raw inputs free
+
+        // start the next item's copies before computing this one
+        const Work nxt = next_work<kMode>(p, cur.tile + stride, stride, num_tiles, L.w, L.lane);
+        if (nxt.tile >= 0) {
+            if (tid == 0) {
+                fence_proxy_async_smem();
+                issue_state(p, nxt, sm);
+            }
+            fetch_raw<kMode>(p, nxt, sm.raw, L.w, L.lane);
+            if (kMode == Mode::kVerify && tid < nxt.T)
+                beta_next = reinterpret_cast<const uint16_t *>(
+                    p.beta)[(size_t)(nxt.bos + tid) * p.stride_beta + nxt.head];
+        }
+
+        // replay the folded / accepted records, store the state once
+        float *tile = p.pool + ((size_t)cur.slot * p.H + cur.head) * (size_t)(kD * kD);
+        for (int u = 0; u < cur.p; ++u) token_step<false>(h, sm.tok, u, 0, L, nullptr);
+        if (cur.p > 0) store_tile(h, tile, L);
+        if constexpr (kMode == Mode::kVerify) {
+            for (int t = 0; t < cur.T; ++t) {
+                const size_t tok = (size_t)(cur.bos + t);
+                token_step<true>(h, sm.tok, cur.p + t, t, L, p.out + (tok * p.H + cur.head) * kD);
+                if (p.traj != nullptr)
+                    store_tile(h, p.traj + (tok * p.H + cur.head) * (size_t)(kD * kD), L);
+            }
+        }
+        if (nxt.tile < 0) break;
+        cur = nxt;
     }
-
-    float *tile = p.pool + ((size_t)row.slot * p.H + head) * (size_t)(kD * kD);
-    float4 h[4][4];
-    load_tile(h, tile, L);
-
-    const float a = expf(p.A_log[head]);
-    const float4 bias = *reinterpret_cast<const float4 *>(p.g_bias + head * kD + 4 * L.lane);
-    prep_records(sm, record_base(p, row.r, head), n, bias, a, kBounded, p.lower_bound, L.w,
-                 L.lane);
-    __syncthreads();
-    for (int t = 0; t < n; ++t) token_step<false>(h, sm, t, 0, L, nullptr);
-    store_tile(h, tile, L);
 }
 
 }  // namespace kda
@@ -251,6 +395,39 @@ kda_status finish_launch() {
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// Launch the persistent step kernel: two CTAs per SM (or one per tile when
+// there are fewer tiles), each with the StepSmem layout in dynamic shared
+// memory.
+template <kda::Mode M>
+kda_status launch_step(const Params &p, bool bounded, cudaStream_t stream) {
+    const long long tiles = (long long)p.B * p.H;
+    const int sms = sm_count();
+    if (sms <= 0) return KDA_ERR_CUDA;
+    const int grid = (int)(tiles < 2LL * sms ? tiles : 2LL * sms);
+    const size_t smem = sizeof(kda::StepSmem);
+    void (*kern)(const Params, int) =
+        bounded ? kda::step_kernel<M, true> : kda::step_kernel<M, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    kern<<<grid, kda::kThreads, smem, stream>>>(p, (int)tiles);
+    return finish_launch();
+}
+
 }  // namespace
 
 extern "C" {
@@ -302,13 +479,8 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     p.traj = trajectory_out;
     p.err = error_word;
 
-    const dim3 grid((unsigned)(B * cfg->num_heads));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cfg->use_lower_bound)
-        kda::verify_kernel<true><<<grid, kda::kThreads, 0, s>>>(p);
-    else
-        kda::verify_kernel<false><<<grid, kda::kThreads, 0, s>>>(p);
-    return finish_launch();
+    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0,
+                                           static_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_bias,
@@ -340,14 +512,8 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     p.eager = eager;
     p.err = error_word;
 
-    const dim3 grid((unsigned)(B * cfg->num_heads));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    using kda::Replay;
-    if (cfg->use_lower_bound)
-        kda::replay_kernel<true, Replay::kCommit><<<grid, kda::kThreads, 0, s>>>(p);
-    else
-        kda::replay_kernel<false, Replay::kCommit><<<grid, kda::kThreads, 0, s>>>(p);
-    return finish_launch();
+    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0,
+                                           static_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_bias,
@@ -372,14 +538,8 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
     p.pending_in = pending;
     p.err = error_word;
 
-    const dim3 grid((unsigned)(B * cfg->num_heads));
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    using kda::Replay;
-    if (cfg->use_lower_bound)
-        kda::replay_kernel<true, Replay::kFlush><<<grid, kda::kThreads, 0, s>>>(p);
-    else
-        kda::replay_kernel<false, Replay::kFlush><<<grid, kda::kThreads, 0, s>>>(p);
-    return finish_launch();
+    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0,
+                                          static_cast<cudaStream_t>(stream));
 }
 
 const char *kda_status_string(kda_status status) {

@@ -263,3 +263,16 @@ def test_full_size_sampled(name):
         for b in range(sp.B):
             if p[rr[b]] > 0:
                 assert torch.equal(pool[int(slots[b])], g.pool0[int(slots[b])])
+
+
+def test_all_rows_idle_and_more_ctas_than_work():
+    # every row null or empty: the persistent CTAs find no work and write nothing
+    wl = W.custom(B=40, H=16, Q=4, lens=[0, 4] * 20, S=48, seed=17,
+                  slots=[0 if i % 2 else i + 1 for i in range(40)])
+    g = GpuRun(wl)
+    g.verify()
+    g.commit()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(g.pool, g.pool0)
+    assert (f64(g.out) == -9.0).all()
