@@ -215,25 +215,50 @@ __device__ __forceinline__ void store_tile(const float4 (&h)[4][4], float *tile,
             *reinterpret_cast<float4 *>(tile + L.row(i) * kD + L.col(m)) = h[i][m];
 }
 
+// Packed pairs of fp32 operations (Blackwell's f32x2 forms): each lane does
+// two independent round-to-nearest multiplies or fused multiply-adds per
+// instruction, bit-identical to two scalar __fmul_rn / __fmaf_rn.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ float2 mul2(float ax, float ay, float bx, float by) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(pack2(ax, ay)), "l"(pack2(bx, by)));
+    return unpack2(d);
+}
+
+__device__ __forceinline__ float2 fma2(float ax, float ay, float bx, float by, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(d)
+        : "l"(pack2(ax, ay)), "l"(pack2(bx, by)), "l"(pack2(c.x, c.y)));
+    return unpack2(d);
+}
+
 // Row dot products of the thread's 4 rows with a vector x (its 16 columns),
-// in a fixed order: two interleaved partial sums per row (even and odd
-// columns of each float4), then their sum.
+// in a fixed order: two interleaved partial sums per row (the even and the
+// odd columns of each float4, one packed pair), then their sum.
 __device__ __forceinline__ void row_partials(const float4 (&h)[4][4], const float4 (&x)[4],
                                              float (&part)[4]) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        float a0 = __fmul_rn(h[i][0].x, x[0].x);
-        float a1 = __fmul_rn(h[i][0].y, x[0].y);
-        a0 = __fmaf_rn(h[i][0].z, x[0].z, a0);
-        a1 = __fmaf_rn(h[i][0].w, x[0].w, a1);
+        float2 a = mul2(h[i][0].x, h[i][0].y, x[0].x, x[0].y);
+        a = fma2(h[i][0].z, h[i][0].w, x[0].z, x[0].w, a);
 #pragma unroll
         for (int m = 1; m < 4; ++m) {
-            a0 = __fmaf_rn(h[i][m].x, x[m].x, a0);
-            a1 = __fmaf_rn(h[i][m].y, x[m].y, a1);
-            a0 = __fmaf_rn(h[i][m].z, x[m].z, a0);
-            a1 = __fmaf_rn(h[i][m].w, x[m].w, a1);
+            a = fma2(h[i][m].x, h[i][m].y, x[m].x, x[m].y, a);
+            a = fma2(h[i][m].z, h[i][m].w, x[m].z, x[m].w, a);
         }
-        part[i] = __fadd_rn(a0, a1);
+        part[i] = __fadd_rn(a.x, a.y);
     }
 }
 
@@ -275,10 +300,9 @@ __device__ __forceinline__ void token_step(float4 (&h)[4][4], const TokenSmem &s
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            h[i][m].x = __fmul_rn(h[i][m].x, ee[m].x);
-            h[i][m].y = __fmul_rn(h[i][m].y, ee[m].y);
-            h[i][m].z = __fmul_rn(h[i][m].z, ee[m].z);
-            h[i][m].w = __fmul_rn(h[i][m].w, ee[m].w);
+            const float2 lo = mul2(h[i][m].x, h[i][m].y, ee[m].x, ee[m].y);
+            const float2 hi = mul2(h[i][m].z, h[i][m].w, ee[m].z, ee[m].w);
+            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     // u = S k^ for the 4 rows, reduced over the row group
     float part[4];
@@ -297,10 +321,11 @@ __device__ __forceinline__ void token_step(float4 (&h)[4][4], const TokenSmem &s
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-            h[i][m].x = __fmaf_rn(vpi[i], kk[m].x, h[i][m].x);
-            h[i][m].y = __fmaf_rn(vpi[i], kk[m].y, h[i][m].y);
-            h[i][m].z = __fmaf_rn(vpi[i], kk[m].z, h[i][m].z);
-            h[i][m].w = __fmaf_rn(vpi[i], kk[m].w, h[i][m].w);
+            const float2 lo =
+                fma2(vpi[i], vpi[i], kk[m].x, kk[m].y, make_float2(h[i][m].x, h[i][m].y));
+            const float2 hi =
+                fma2(vpi[i], vpi[i], kk[m].z, kk[m].w, make_float2(h[i][m].z, h[i][m].w));
+            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     if constexpr (kOut) {
         float4 qq[4];
