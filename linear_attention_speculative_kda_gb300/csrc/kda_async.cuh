@@ -1,8 +1,8 @@
 // Asynchronous copy helpers (inline PTX, sm_90+ / sm_103a):
 //  - 1-D bulk copies global -> shared through the TMA unit, completing on an
 //    mbarrier transaction count (cp.async.bulk ... mbarrier::complete_tx);
-//  - 8-byte cp.async (LDGSTS) global -> shared, grouped and waited on per
-//    thread;
+//  - 4-, 8- and 16-byte cp.async (LDGSTS) global -> shared, grouped and
+//    waited on per thread;
 //  - a bounded mbarrier wait: it gives up after a clock budget instead of
 //    spinning forever, so a lost transaction becomes an error bit, not a hang.
 #pragma once
@@ -72,6 +72,18 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 
 __device__ __forceinline__ void cp_async8(void *dst_smem, const void *src_gmem) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)),
+                 "l"(src_gmem)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async4(void *dst_smem, const void *src_gmem) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)),
+                 "l"(src_gmem)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src_gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)),
                  "l"(src_gmem)
                  : "memory");
 }

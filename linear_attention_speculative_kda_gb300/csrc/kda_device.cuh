@@ -10,8 +10,8 @@
 // block barrier inside the token loop.
 //
 // The per-token vectors that do not depend on the state (k^, q^, exp(g),
-// beta, v) are computed once per CTA per token by one warp and kept in shared
-// memory; the token loop reads them with conflict-free broadcast loads.
+// beta, v) are computed once per CTA per token and kept in shared memory; the
+// token loop reads them with conflict-free broadcast loads.
 //
 // Bit-exactness of commit against verify: the verify, the commit replay, the
 // deferred fold and the flush all run `token_step` below with the same thread
@@ -79,13 +79,8 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
     return __uint_as_float(bits16 << 16);
 }
 
-__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
-    float4 f;
-    f.x = __uint_as_float(u.x << 16);
-    f.y = __uint_as_float(u.x & 0xffff0000u);
-    f.z = __uint_as_float(u.y << 16);
-    f.w = __uint_as_float(u.y & 0xffff0000u);
-    return f;
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
 }
 
 // Butterfly sum over the 32 lanes: every lane ends with the same bits
@@ -94,14 +89,6 @@ __device__ __forceinline__ float warp_allsum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_xor_sync(kFull, x, o));
     return x;
-}
-
-__device__ __forceinline__ float sumsq4(float4 a) {
-    float s = __fmul_rn(a.x, a.x);
-    s = __fmaf_rn(a.y, a.y, s);
-    s = __fmaf_rn(a.z, a.z, s);
-    s = __fmaf_rn(a.w, a.w, s);
-    return s;
 }
 
 // 1 / sqrt(sum + 1e-6), correctly rounded sqrt and division.
@@ -125,70 +112,6 @@ __device__ __forceinline__ float decay_factor(float x, float a, bool bounded, fl
 
 __device__ __forceinline__ float sigmoidf_rn(float x) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
-}
-
-// --------------------------------------------------------- token prologue --
-//
-// One warp prepares one token: lane L owns channels 4L .. 4L+3.  Raw inputs
-// arrive as 4 bf16 per lane (8-byte loads; a token-head row is 256
-// contiguous bytes).  The k^ / q^ norms are warp-wide sums.
-
-struct RawToken {
-    uint2 k, v, g;      // 4 bf16 each
-    uint32_t beta;      // bf16 bits in the low half (lane 0 only)
-};
-
-__device__ __forceinline__ void prep_token(TokenSmem &sm, int slot, const RawToken &raw,
-                                           const float4 bias, float a, bool bounded,
-                                           float lb, int lane) {
-    const float4 k = bf16x4_to_float4(raw.k);
-    const float ik = inv_l2(warp_allsum(sumsq4(k)));
-    float4 kh;
-    kh.x = __fmul_rn(k.x, ik);
-    kh.y = __fmul_rn(k.y, ik);
-    kh.z = __fmul_rn(k.z, ik);
-    kh.w = __fmul_rn(k.w, ik);
-    const float4 g = bf16x4_to_float4(raw.g);
-    float4 e;
-    e.x = decay_factor(__fadd_rn(g.x, bias.x), a, bounded, lb);
-    e.y = decay_factor(__fadd_rn(g.y, bias.y), a, bounded, lb);
-    e.z = decay_factor(__fadd_rn(g.z, bias.z), a, bounded, lb);
-    e.w = decay_factor(__fadd_rn(g.w, bias.w), a, bounded, lb);
-    *reinterpret_cast<float4 *>(&sm.kh[slot][4 * lane]) = kh;
-    *reinterpret_cast<float4 *>(&sm.e[slot][4 * lane]) = e;
-    *reinterpret_cast<float4 *>(&sm.v[slot][4 * lane]) = bf16x4_to_float4(raw.v);
-    if (lane == 0) sm.beta[slot] = sigmoidf_rn(bf16_bits_to_float(raw.beta));
-}
-
-__device__ __forceinline__ void prep_query(TokenSmem &sm, int slot, uint2 qraw, float scale,
-                                           int lane) {
-    const float4 q = bf16x4_to_float4(qraw);
-    const float iq = inv_l2(warp_allsum(sumsq4(q)));
-    float4 qh;
-    qh.x = __fmul_rn(__fmul_rn(q.x, iq), scale);
-    qh.y = __fmul_rn(__fmul_rn(q.y, iq), scale);
-    qh.z = __fmul_rn(__fmul_rn(q.z, iq), scale);
-    qh.w = __fmul_rn(__fmul_rn(q.w, iq), scale);
-    *reinterpret_cast<float4 *>(&sm.qh[slot][4 * lane]) = qh;
-}
-
-__device__ __forceinline__ RawToken load_record(const __nv_bfloat16 *rec, int lane) {
-    RawToken r;
-    const uint2 *base = reinterpret_cast<const uint2 *>(rec);
-    r.k = base[lane];
-    r.v = base[kRecV / 4 + lane];
-    r.g = base[kRecG / 4 + lane];
-    r.beta = lane == 0 ? static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(rec)[kRecBeta])
-                       : 0u;
-    return r;
-}
-
-__device__ __forceinline__ void store_record(__nv_bfloat16 *rec, const RawToken &r, int lane) {
-    uint2 *base = reinterpret_cast<uint2 *>(rec);
-    base[lane] = r.k;
-    base[kRecV / 4 + lane] = r.v;
-    base[kRecG / 4 + lane] = r.g;
-    if (lane == 0) reinterpret_cast<uint16_t *>(rec)[kRecBeta] = static_cast<uint16_t>(r.beta);
 }
 
 // ------------------------------------------------------------ state tile --

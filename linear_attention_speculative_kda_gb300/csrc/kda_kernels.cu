@@ -71,16 +71,16 @@ struct Work {
 
 // Plan one tile: row checks, the commit plan (n = clamp(accepted, 0,
 // min(T, Q)), valid iff slot > 0, n > 0, r >= 0), the deferred commit's
-// pending write.  Side effects (error bits, pending writes) only when
-// `side`; they are idempotent, so a tile planned twice is harmless.
+// pending write.  Side effects (error bits, pending writes) are made by the
+// one thread that plans the tile.
 template <Mode kMode>
-__device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, Work &w) {
+__device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
     const int b = tile / p.H;
     const int head = tile - b * p.H;
     Row row;
     const int bad = read_row(p, b, kMode != Mode::kFlush, row);
     if (bad) {
-        if (side && head == 0) flag_error(p.err, bad);
+        if (head == 0) flag_error(p.err, bad);
         return false;
     }
     int fold = 0, T = 0;
@@ -89,7 +89,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, 
         if (p.pending_in != nullptr && row.r >= 0) {
             fold = p.pending_in[row.r];
             if (fold < 0 || fold > p.Q) {
-                if (side && head == 0) flag_error(p.err, kBadPending);
+                if (head == 0) flag_error(p.err, kBadPending);
                 return false;
             }
         }
@@ -100,7 +100,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, 
         const bool valid = row.slot > 0 && n > 0 && row.r >= 0;
         if (p.pending_out != nullptr) {
             const bool now = p.eager != nullptr && p.eager[b] != 0;
-            if (side && head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
+            if (head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
             if (!now) return false;
         }
         if (!valid) return false;
@@ -109,7 +109,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, 
         if (row.slot <= 0 || row.r < 0) return false;
         const int n = p.pending_in[row.r];
         if (n < 0 || n > p.Q) {
-            if (side && head == 0) flag_error(p.err, kBadPending);
+            if (head == 0) flag_error(p.err, kBadPending);
             return false;
         }
         if (n == 0) return false;
@@ -125,58 +125,124 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, bool side, 
     return true;
 }
 
-// The next work item of this CTA at or after tile `from` (tiles from,
-// from + stride, ...).  Each warp plans 32 candidate tiles at once, one per
-// lane, and takes the first that has work, so skipping idle tiles costs one
-// round of metadata loads per 32 of them.  All warps compute the same answer;
-// warp 0 alone performs the side effects.
-template <Mode kMode>
-__device__ __forceinline__ Work next_work(const Params &p, int from, int stride, int num_tiles,
-                                          int warp, int lane) {
-    Work w;
-    w.tile = -1;
-    for (int base = from; base < num_tiles; base += 32 * stride) {
-        const int t = base + lane * stride;
-        Work mine;
-        const bool has = t < num_tiles && plan_tile<kMode>(p, t, warp == 0, mine);
-        const unsigned ballot = __ballot_sync(kFull, has);
-        if (ballot != 0u) {
-            const int src = __ffs(ballot) - 1;
-            w.tile = __shfl_sync(kFull, mine.tile, src);
-            w.head = __shfl_sync(kFull, mine.head, src);
-            w.slot = __shfl_sync(kFull, mine.slot, src);
-            w.r = __shfl_sync(kFull, mine.r, src);
-            w.bos = __shfl_sync(kFull, mine.bos, src);
-            w.T = __shfl_sync(kFull, mine.T, src);
-            w.p = __shfl_sync(kFull, mine.p, src);
-            return w;
-        }
-    }
-    return w;
-}
-
 // ---------------------------------------------------------- shared memory --
 
-// Raw bf16 inputs of one work item, brought in by cp.async: slots [0, p)
-// are the folded record tokens, [p, p + T) the new tokens.
+constexpr int kPlanThreads = 128;   // candidates planned per round
+constexpr int kListCap = kPlanThreads;
+
+// The CTA's work list: candidate k of this CTA is tile blockIdx.x + k *
+// gridDim.x.  A planning round plans kPlanThreads candidates at once, one per
+// thread, and compacts the ones with work, in order, into the list.
+struct WorkList {
+    int tile[kListCap];
+    int slot[kListCap];
+    int r[kListCap];
+    int bos[kListCap];
+    int tp[kListCap];   // T | p << 8
+    int warp_count[kPlanThreads / 32];
+    int count;
+};
+
+// Raw bf16 inputs and gate parameters of one work item, brought in by
+// cp.async: token slots [0, p) are the folded record tokens, [p, p + T) the
+// new tokens.  Stored as channel pairs (one 32-bit word = 2 bf16).
 struct RawSmem {
-    uint2 k[2 * kMaxQ][32];
-    uint2 v[2 * kMaxQ][32];
-    uint2 g[2 * kMaxQ][32];
-    uint2 q[kMaxQ][32];
+    uint32_t k[2 * kMaxQ][kD / 2];
+    uint32_t v[2 * kMaxQ][kD / 2];
+    uint32_t g[2 * kMaxQ][kD / 2];
+    uint32_t q[kMaxQ][kD / 2];
     uint2 tail[kMaxQ];          // record tails: beta_raw bits in the low half
+    float bias[kD];             // g_bias of the item's head
+    float a_log;                // A_log of the item's head
     uint32_t beta_new[kMaxQ];   // beta_raw bits of the new tokens
 };
 
 struct __align__(16) StepSmem {
-    float state[kD * kD];       // staging of the next tile's checkpoint (TMA)
+    float state[kD * kD];       // staging of the next item's checkpoint (TMA)
     TokenSmem tok;              // per-token vectors of the current item
     RawSmem raw;                // raw inputs of the current / next item
+    float red_k[2 * kMaxQ][2];  // per-warp halves of |k|^2
+    float red_q[kMaxQ][2];      // per-warp halves of |q|^2
+    WorkList list;
     uint64_t bar;               // completion of the staging copy
     int ok;
 };
 
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
+
+__device__ __forceinline__ int num_candidates(int num_tiles) {
+    const int first = (int)blockIdx.x;
+    return first < num_tiles ? (num_tiles - first + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
+// One planning round over candidates [k0, k0 + kPlanThreads); all threads
+// take part (it contains barriers).  Returns the number of listed items.
+template <Mode kMode>
+__device__ int plan_round(const Params &p, StepSmem &sm, int k0, int num_tiles, int tid) {
+    const int K = num_candidates(num_tiles);
+    Work w;
+    bool has = false;
+    if (tid < kPlanThreads) {
+        const int k = k0 + tid;
+        if (k < K) has = plan_tile<kMode>(p, (int)blockIdx.x + k * (int)gridDim.x, w);
+    }
+    const unsigned ballot = __ballot_sync(kFull, has);
+    const int lane = tid & 31, warp = tid >> 5;
+    if (tid < kPlanThreads && lane == 0) sm.list.warp_count[warp] = __popc(ballot);
+    __syncthreads();
+    int before = 0, total = 0;
+#pragma unroll
+    for (int i = 0; i < kPlanThreads / 32; ++i) {
+        const int c = sm.list.warp_count[i];
+        if (i < warp) before += c;
+        total += c;
+    }
+    if (has) {
+        const int pos = before + __popc(ballot & ((1u << lane) - 1u));
+        sm.list.tile[pos] = w.tile;
+        sm.list.slot[pos] = w.slot;
+        sm.list.r[pos] = w.r;
+        sm.list.bos[pos] = w.bos;
+        sm.list.tp[pos] = w.T | (w.p << 8);
+    }
+    __syncthreads();
+    return total;
+}
+
+__device__ __forceinline__ Work list_item(const StepSmem &sm, int i, int H) {
+    Work w;
+    w.tile = sm.list.tile[i];
+    w.head = w.tile % H;
+    w.slot = sm.list.slot[i];
+    w.r = sm.list.r[i];
+    w.bos = sm.list.bos[i];
+    const int tp = sm.list.tp[i];
+    w.T = tp & 0xff;
+    w.p = tp >> 8;
+    return w;
+}
+
+// Cursor over the CTA's work: the list of the current round and where the
+// next round starts.  Uniform across the CTA.
+struct Cursor {
+    int idx, count, next_k;
+};
+
+// Advance to the next listed item (planning a new round when the list is
+// used up).  Returns its list index, or -1 when the CTA has no more work.
+// The item stays readable in the list until the following call.
+template <Mode kMode>
+__device__ __forceinline__ int next_item(const Params &p, StepSmem &sm, Cursor &c, int num_tiles,
+                                         int tid) {
+    const int K = num_candidates(num_tiles);
+    while (c.idx >= c.count) {
+        if (c.next_k >= K) return -1;
+        c.count = plan_round<kMode>(p, sm, c.next_k, num_tiles, tid);
+        c.next_k += kPlanThreads;
+        c.idx = 0;
+    }
+    return c.idx++;
+}
 
 __device__ __forceinline__ void issue_state(const Params &p, const Work &w, StepSmem &sm) {
     const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
@@ -186,6 +252,7 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, Step
         bulk_load(sm.state + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, &sm.bar);
 }
 
+// Raw inputs and gate parameters of an item into shared memory (cp.async).
 template <Mode kMode>
 __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSmem &raw, int warp,
                                           int lane) {
@@ -194,18 +261,21 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSme
         const int u = c / 3;
         const int part = c - 3 * u;
         const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
-        uint2 *dst = part == 0 ? raw.k[u] : (part == 1 ? raw.v[u] : raw.g[u]);
-        cp_async8(dst + lane, src + lane);
+        uint32_t *dst = part == 0 ? raw.k[u] : (part == 1 ? raw.v[u] : raw.g[u]);
+        cp_async8(dst + 2 * lane, src + lane);
     }
-    if (warp == kWarps - 1 && lane < w.p)
-        cp_async8(&raw.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
+    if (warp == kWarps - 1) {
+        if (lane < w.p) cp_async8(&raw.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
+        if (lane == 31) cp_async4(&raw.a_log, p.A_log + w.head);
+    }
+    if (warp == kWarps - 2) cp_async16(&raw.bias[4 * lane], p.g_bias + w.head * kD + 4 * lane);
     if constexpr (kMode == Mode::kVerify) {
         for (int c = warp; c < 4 * w.T; c += kWarps) {
             const int t = c >> 2;
             const int part = c & 3;
             const size_t tok = (size_t)(w.bos + t);
             const __nv_bfloat16 *src;
-            uint2 *dst;
+            uint32_t *dst;
             if (part == 0) {
                 src = p.k + tok * p.stride_k;
                 dst = raw.k[w.p + t];
@@ -219,18 +289,80 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSme
                 src = p.q + tok * p.stride_q;
                 dst = raw.q[t];
             }
-            cp_async8(dst + lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
+            cp_async8(dst + 2 * lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
         }
     }
     cp_async_commit();
 }
 
+// Per-token vectors of an item, all 8 warps: token u is prepared by the 64
+// threads of quarter (u & 3) in pass (u >> 2), two channels per thread, so
+// every token is computed the same way however many tokens the item has.
+// The verify also writes the new tokens' raw records.
+template <Mode kMode, bool kBounded>
+__device__ __forceinline__ void prep_item(StepSmem &sm, const Params &p, const Work &w, int tid) {
+    const int quarter = tid >> 6;
+    const int c2 = tid & 63;              // channels 2*c2, 2*c2 + 1
+    const int half = c2 >> 5;             // which of the quarter's two warps
+    const bool lead = (tid & 31) == 0;
+    const int total = w.p + w.T;
+    const int passes = (total + 3) >> 2;
+    const float a = expf(sm.raw.a_log);
+    const float2 bias = *reinterpret_cast<const float2 *>(&sm.raw.bias[2 * c2]);
+    __nv_bfloat16 *rec = record_base(p, w.r, w.head);
+    for (int pass = 0; pass < passes; ++pass) {
+        const int u = 4 * pass + quarter;
+        const bool active = u < total;
+        const bool is_new = kMode == Mode::kVerify && u >= w.p;
+        const int t = u - w.p;
+        float2 k = make_float2(0.f, 0.f), q = make_float2(0.f, 0.f);
+        if (active) {
+            const uint32_t kb = sm.raw.k[u][c2], vb = sm.raw.v[u][c2], gb = sm.raw.g[u][c2];
+            k = bf16x2_to_float2(kb);
+            const float sk = warp_allsum(__fmaf_rn(k.y, k.y, __fmul_rn(k.x, k.x)));
+            if (lead) sm.red_k[u][half] = sk;
+            const float2 g = bf16x2_to_float2(gb);
+            float2 e;
+            e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
+            e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
+            *reinterpret_cast<float2 *>(&sm.tok.e[u][2 * c2]) = e;
+            *reinterpret_cast<float2 *>(&sm.tok.v[u][2 * c2]) = bf16x2_to_float2(vb);
+            const uint32_t bb = is_new ? sm.raw.beta_new[t] : (sm.raw.tail[u].x & 0xffffu);
+            if (c2 == 0) sm.tok.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+            if (is_new) {
+                const uint32_t qb = sm.raw.q[t][c2];
+                q = bf16x2_to_float2(qb);
+                const float sq = warp_allsum(__fmaf_rn(q.y, q.y, __fmul_rn(q.x, q.x)));
+                if (lead) sm.red_q[t][half] = sq;
+                __nv_bfloat16 *dst = rec + (size_t)t * kRecStride;
+                reinterpret_cast<uint32_t *>(dst)[c2] = kb;
+                reinterpret_cast<uint32_t *>(dst + kRecV)[c2] = vb;
+                reinterpret_cast<uint32_t *>(dst + kRecG)[c2] = gb;
+                if (c2 == 0) reinterpret_cast<uint16_t *>(dst)[kRecBeta] = (uint16_t)bb;
+            }
+        }
+        __syncthreads();  // both halves of the norms are in
+        if (active) {
+            const float ik = inv_l2(__fadd_rn(sm.red_k[u][0], sm.red_k[u][1]));
+            *reinterpret_cast<float2 *>(&sm.tok.kh[u][2 * c2]) =
+                make_float2(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik));
+            if (is_new) {
+                const float iq = inv_l2(__fadd_rn(sm.red_q[t][0], sm.red_q[t][1]));
+                *reinterpret_cast<float2 *>(&sm.tok.qh[t][2 * c2]) =
+                    make_float2(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
+                                __fmul_rn(__fmul_rn(q.y, iq), p.scale));
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ kernel --
 //
 // Persistent: gridDim.x CTAs (two per SM) walk the tiles b*H + head with a
-// stride of gridDim.x.  While a CTA computes one item from registers, the
-// next item's checkpoint streams into shared memory through the TMA unit and
-// its raw inputs through cp.async, so memory and arithmetic overlap.
+// stride of gridDim.x, planned in rounds into a shared-memory work list.
+// While a CTA computes one item from registers, the next item's checkpoint
+// streams into shared memory through the TMA unit and its raw inputs and
+// gate parameters through cp.async, so memory and arithmetic overlap.
 
 template <Mode kMode, bool kBounded>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int num_tiles) {
@@ -242,7 +374,6 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
     L.w = tid >> 5;
     L.g = L.lane >> 3;
     L.j = L.lane & 7;
-    const int stride = gridDim.x;
 
     if (tid == 0) {
         mbar_init(&sm.bar, 1);
@@ -250,8 +381,10 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
     }
     __syncthreads();
 
-    Work cur = next_work<kMode>(p, blockIdx.x, stride, num_tiles, L.w, L.lane);
-    if (cur.tile < 0) return;
+    Cursor cursor{0, 0, 0};
+    const int first = next_item<kMode>(p, sm, cursor, num_tiles, tid);
+    if (first < 0) return;
+    Work cur = list_item(sm, first, p.H);
     if (tid == 0) issue_state(p, cur, sm);
     fetch_raw<kMode>(p, cur, sm.raw, L.w, L.lane);
     uint32_t beta_next = 0;
@@ -267,30 +400,11 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
         if (kMode == Mode::kVerify && tid < cur.T) sm.raw.beta_new[tid] = beta_next;
         __syncthreads();
 
-        // per-token vectors of `cur`; the verify also writes its records
-        const float a = expf(p.A_log[cur.head]);
-        const float4 bias =
-            *reinterpret_cast<const float4 *>(p.g_bias + cur.head * kD + 4 * L.lane);
-        __nv_bfloat16 *rec = record_base(p, cur.r, cur.head);
-        for (int u = L.w; u < cur.p + cur.T; u += kWarps) {
-            RawToken rt;
-            rt.k = sm.raw.k[u][L.lane];
-            rt.v = sm.raw.v[u][L.lane];
-            rt.g = sm.raw.g[u][L.lane];
-            rt.beta = u < cur.p ? (sm.raw.tail[u].x & 0xffffu) : sm.raw.beta_new[u - cur.p];
-            prep_token(sm.tok, u, rt, bias, a, kBounded, p.lower_bound, L.lane);
-            if constexpr (kMode == Mode::kVerify) {
-                if (u >= cur.p) {
-                    const int t = u - cur.p;
-                    prep_query(sm.tok, t, sm.raw.q[t][L.lane], p.scale, L.lane);
-                    store_record(rec + (size_t)t * kRecStride, rt, L.lane);
-                }
-            }
-        }
+        prep_item<kMode, kBounded>(sm, p, cur, tid);
 
         // checkpoint of `cur`: staged by the TMA unit
         if (tid == 0) sm.ok = mbar_wait_bounded(&sm.bar, phase, kWaitBudget) ? 1 : 0;
-        __syncthreads();
+        __syncthreads();  // also: token vectors ready, raw inputs consumed
         if (!sm.ok) {
             if (tid == 0) {
                 flag_error(p.err, kErrWaitTimeout);
@@ -302,15 +416,13 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
         phase ^= 1u;
         float4 h[4][4];
         load_tile(h, sm.state, L);
-        __syncthreads();  // staging buffer and raw inputs free
+        __syncthreads();  // staging buffer free
 
         // start the next item's copies before computing this one
-        const Work nxt = next_work<kMode>(p, cur.tile + stride, stride, num_tiles, L.w, L.lane);
-        if (nxt.tile >= 0) {
-            if (tid == 0) {
-                fence_proxy_async_smem();
-                issue_state(p, nxt, sm);
-            }
+        const int nidx = next_item<kMode>(p, sm, cursor, num_tiles, tid);
+        if (nidx >= 0) {
+            const Work nxt = list_item(sm, nidx, p.H);
+            if (tid == 0) issue_state(p, nxt, sm);
             fetch_raw<kMode>(p, nxt, sm.raw, L.w, L.lane);
             if (kMode == Mode::kVerify && tid < nxt.T)
                 beta_next = reinterpret_cast<const uint16_t *>(
@@ -329,8 +441,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
                     store_tile(h, p.traj + (tok * p.H + cur.head) * (size_t)(kD * kD), L);
             }
         }
-        if (nxt.tile < 0) break;
-        cur = nxt;
+        if (nidx < 0) break;
+        cur = list_item(sm, nidx, p.H);
     }
 }
 
