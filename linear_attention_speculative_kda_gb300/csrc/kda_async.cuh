@@ -1,7 +1,6 @@
 // Asynchronous copy helpers (inline PTX, sm_90+ / sm_103a):
 //  - 1-D bulk copies global -> shared through the TMA unit, completing on an
-//    mbarrier transaction count (cp.async.bulk ... mbarrier::complete_tx),
-//    and bulk prefetches of global memory into L2;
+//    mbarrier transaction count (cp.async.bulk ... mbarrier::complete_tx);
 //  - 4-, 8- and 16-byte cp.async (LDGSTS) global -> shared, grouped and
 //    waited on per thread;
 //  - a bounded mbarrier wait: it gives up after a clock budget instead of
@@ -46,13 +45,6 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
             "r"(smem_u32(dst_smem)),
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into
-// L2 through the TMA unit; no completion to wait for.
-__device__ __forceinline__ void bulk_prefetch_l2(const void *src_gmem, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {

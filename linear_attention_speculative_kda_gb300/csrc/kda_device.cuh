@@ -14,7 +14,7 @@
 // token loop reads them with conflict-free broadcast loads.
 //
 // Bit-exactness of commit against verify: the verify, the commit replay, the
-// deferred fold and the flush all run the token pieces below with the same thread
+// deferred fold and the flush all run `token_step` below with the same thread
 // mapping, the same explicit round-to-nearest intrinsics (no contraction left
 // to the compiler) and the same reduction tree, so the state after token n is
 // the same bits whichever kernel computes it.
@@ -205,22 +205,20 @@ __device__ __forceinline__ float reduce_rows(const float (&part)[4], int j) {
 
 __device__ __forceinline__ int reduced_row(int j) { return 2 * ((j >> 2) & 1) + ((j >> 1) & 1); }
 
-// Pieces of one token of the recurrence on the thread's part of the tile:
-//   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T;  o = S q^.
-// Every kernel runs the state-changing pieces (decay_partials, reduce_rows,
-// delta_update) in the same order on the same operands, so the state after a
-// token has the same bits whichever kernel computes it.
-
-__device__ __forceinline__ void load_cols(float4 (&x)[4], const float *vec, const Lane &L) {
+// One token of the recurrence on the thread's part of the tile:
+//   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T
+// and, when kOut, o = S q^ written as bf16 to out_row (128 outputs).
+template <bool kOut>
+__device__ __forceinline__ void token_step(float4 (&h)[4][4], const TokenSmem &sm, int slot,
+                                           int qslot, const Lane &L,
+                                           __nv_bfloat16 *out_row) {
+    float4 kk[4], ee[4];
 #pragma unroll
-    for (int m = 0; m < 4; ++m) x[m] = *reinterpret_cast<const float4 *>(vec + L.col(m));
-}
-
-// Decay along K in place, then the partial sums of u = S k^ of the 4 rows.
-__device__ __forceinline__ void decay_partials(float4 (&h)[4][4], const TokenSmem &sm, int slot,
-                                               const Lane &L, float (&part)[4]) {
-    float4 ee[4];
-    load_cols(ee, sm.e[slot], L);
+    for (int m = 0; m < 4; ++m) {
+        kk[m] = *reinterpret_cast<const float4 *>(&sm.kh[slot][L.col(m)]);
+        ee[m] = *reinterpret_cast<const float4 *>(&sm.e[slot][L.col(m)]);
+    }
+    // decay along K
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -229,15 +227,10 @@ __device__ __forceinline__ void decay_partials(float4 (&h)[4][4], const TokenSme
             const float2 hi = mul2(h[i][m].z, h[i][m].w, ee[m].z, ee[m].w);
             h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
-    float4 kk[4];
-    load_cols(kk, sm.kh[slot], L);
+    // u = S k^ for the 4 rows, reduced over the row group
+    float part[4];
     row_partials(h, kk, part);
-}
-
-// v' = beta (v - u) for the lane's reduced row, shared with the row group,
-// then the rank-one update S <- S + v' k^T.
-__device__ __forceinline__ void delta_update(float4 (&h)[4][4], const TokenSmem &sm, int slot,
-                                             float u, const Lane &L) {
+    const float u = reduce_rows(part, L.j);
     const int R = reduced_row(L.j);
     const float vr = sm.v[slot][L.row(R)];
     const float vp = __fmul_rn(sm.beta[slot], __fsub_rn(vr, u));
@@ -246,8 +239,7 @@ __device__ __forceinline__ void delta_update(float4 (&h)[4][4], const TokenSmem 
     float vpi[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) vpi[i] = __shfl_sync(kFull, vp, base + 2 * i);
-    float4 kk[4];
-    load_cols(kk, sm.kh[slot], L);
+    // rank-one update
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -258,42 +250,15 @@ __device__ __forceinline__ void delta_update(float4 (&h)[4][4], const TokenSmem 
                 fma2(vpi[i], vpi[i], kk[m].z, kk[m].w, make_float2(h[i][m].z, h[i][m].w));
             h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
-}
-
-// One token without output (commit replay, deferred fold, flush).
-__device__ __forceinline__ void token_plain(float4 (&h)[4][4], const TokenSmem &sm, int slot,
-                                            const Lane &L) {
-    float part[4];
-    decay_partials(h, sm, slot, L, part);
-    delta_update(h, sm, slot, reduce_rows(part, L.j), L);
-}
-
-// The new tokens of a verify: slots first .. first + T - 1, outputs to
-// out_row0 + t * out_stride (bf16, 128 values each); traj (tests only) gets
-// the state after every token.  Software-pipelined: the output reduction of
-// token t and the delta reduction of token t + 1 are independent and run
-// side by side.
-__device__ __forceinline__ void run_verify_tokens(float4 (&h)[4][4], const TokenSmem &sm,
-                                                  int first, int T, const Lane &L,
-                                                  __nv_bfloat16 *out_row0, size_t out_stride,
-                                                  float *traj0, size_t traj_stride) {
-    if (T <= 0) return;
-    float part_u[4];
-    decay_partials(h, sm, first, L, part_u);
-    delta_update(h, sm, first, reduce_rows(part_u, L.j), L);
-    for (int t = 0; t < T; ++t) {
-        if (traj0 != nullptr) store_tile(h, traj0 + (size_t)t * traj_stride, L);
-        float part_o[4];
+    if constexpr (kOut) {
         float4 qq[4];
-        load_cols(qq, sm.qh[t], L);
-        row_partials(h, qq, part_o);  // o of token t, from the state after it
-        const bool more = t + 1 < T;
-        if (more) decay_partials(h, sm, first + t + 1, L, part_u);
-        const float o = reduce_rows(part_o, L.j);
-        const float u = more ? reduce_rows(part_u, L.j) : 0.0f;
-        if ((L.j & 1) == 0)
-            out_row0[(size_t)t * out_stride + L.row(reduced_row(L.j))] = __float2bfloat16_rn(o);
-        if (more) delta_update(h, sm, first + t + 1, u, L);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            qq[m] = *reinterpret_cast<const float4 *>(&sm.qh[qslot][L.col(m)]);
+        float opart[4];
+        row_partials(h, qq, opart);
+        const float o = reduce_rows(opart, L.j);
+        if ((L.j & 1) == 0) out_row[L.row(R)] = __float2bfloat16_rn(o);
     }
 }
 

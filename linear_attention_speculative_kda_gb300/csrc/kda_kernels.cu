@@ -158,10 +158,17 @@ struct RawSmem {
 };
 
 struct __align__(16) StepSmem {
+    float state[kD * kD];       // staging of the next item's checkpoint (TMA)
     TokenSmem tok;              // per-token vectors of the current item
     RawSmem raw;                // raw inputs of the current / next item
+    float red_k[2 * kMaxQ][2];  // per-warp halves of |k|^2
+    float red_q[kMaxQ][2];      // per-warp halves of |q|^2
     WorkList list;
+    uint64_t bar;               // completion of the staging copy
+    int ok;
 };
+
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 
 __device__ __forceinline__ int num_candidates(int num_tiles) {
     const int first = (int)blockIdx.x;
@@ -237,12 +244,12 @@ __device__ __forceinline__ int next_item(const Params &p, StepSmem &sm, Cursor &
     return c.idx++;
 }
 
-// Ask the TMA unit to bring an item's checkpoint into L2 (no shared-memory
-// destination); the item's own loads later hit L2.
-__device__ __forceinline__ void prefetch_state(const Params &p, const Work &w) {
+__device__ __forceinline__ void issue_state(const Params &p, const Work &w, StepSmem &sm) {
     const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
+    mbar_arrive_expect_tx(&sm.bar, kD * kD * 4);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) bulk_prefetch_l2(src + c * (kD * kD / 4), kD * kD);
+    for (int c = 0; c < 4; ++c)
+        bulk_load(sm.state + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, &sm.bar);
 }
 
 // Raw inputs and gate parameters of an item into shared memory (cp.async).
@@ -291,54 +298,60 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSme
 // Per-token vectors of an item, all 8 warps: token u is prepared by the 64
 // threads of quarter (u & 3) in pass (u >> 2), two channels per thread, so
 // every token is computed the same way however many tokens the item has.
-// Each of the quarter's two warps sums the full |k|^2 (and |q|^2) itself, in
-// the same order, so no barrier is needed.  The verify also writes the new
-// tokens' raw records.
-__device__ __forceinline__ float token_norm_inv(const uint32_t *row, int lane) {
-    const uint2 w = reinterpret_cast<const uint2 *>(row)[lane];  // channels 4 lane .. +3
-    const float2 a = bf16x2_to_float2(w.x), b = bf16x2_to_float2(w.y);
-    float s = __fmul_rn(a.x, a.x);
-    s = __fmaf_rn(a.y, a.y, s);
-    s = __fmaf_rn(b.x, b.x, s);
-    s = __fmaf_rn(b.y, b.y, s);
-    return inv_l2(warp_allsum(s));
-}
-
+// The verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
 __device__ __forceinline__ void prep_item(StepSmem &sm, const Params &p, const Work &w, int tid) {
     const int quarter = tid >> 6;
     const int c2 = tid & 63;              // channels 2*c2, 2*c2 + 1
-    const int lane = tid & 31;
+    const int half = c2 >> 5;             // which of the quarter's two warps
+    const bool lead = (tid & 31) == 0;
     const int total = w.p + w.T;
+    const int passes = (total + 3) >> 2;
     const float a = expf(sm.raw.a_log);
     const float2 bias = *reinterpret_cast<const float2 *>(&sm.raw.bias[2 * c2]);
     __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int u = quarter; u < total; u += 4) {
+    for (int pass = 0; pass < passes; ++pass) {
+        const int u = 4 * pass + quarter;
+        const bool active = u < total;
         const bool is_new = kMode == Mode::kVerify && u >= w.p;
         const int t = u - w.p;
-        const uint32_t kb = sm.raw.k[u][c2], vb = sm.raw.v[u][c2], gb = sm.raw.g[u][c2];
-        const float ik = token_norm_inv(sm.raw.k[u], lane);
-        const float2 k = bf16x2_to_float2(kb);
-        *reinterpret_cast<float2 *>(&sm.tok.kh[u][2 * c2]) =
-            make_float2(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik));
-        const float2 g = bf16x2_to_float2(gb);
-        float2 e;
-        e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
-        e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
-        *reinterpret_cast<float2 *>(&sm.tok.e[u][2 * c2]) = e;
-        *reinterpret_cast<float2 *>(&sm.tok.v[u][2 * c2]) = bf16x2_to_float2(vb);
-        const uint32_t bb = is_new ? sm.raw.beta_new[t] : (sm.raw.tail[u].x & 0xffffu);
-        if (c2 == 0) sm.tok.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
-        if (is_new) {
-            const float iq = __fmul_rn(token_norm_inv(sm.raw.q[t], lane), p.scale);
-            const float2 q = bf16x2_to_float2(sm.raw.q[t][c2]);
-            *reinterpret_cast<float2 *>(&sm.tok.qh[t][2 * c2]) =
-                make_float2(__fmul_rn(q.x, iq), __fmul_rn(q.y, iq));
-            __nv_bfloat16 *dst = rec + (size_t)t * kRecStride;
-            reinterpret_cast<uint32_t *>(dst)[c2] = kb;
-            reinterpret_cast<uint32_t *>(dst + kRecV)[c2] = vb;
-            reinterpret_cast<uint32_t *>(dst + kRecG)[c2] = gb;
-            if (c2 == 0) reinterpret_cast<uint16_t *>(dst)[kRecBeta] = (uint16_t)bb;
+        float2 k = make_float2(0.f, 0.f), q = make_float2(0.f, 0.f);
+        if (active) {
+            const uint32_t kb = sm.raw.k[u][c2], vb = sm.raw.v[u][c2], gb = sm.raw.g[u][c2];
+            k = bf16x2_to_float2(kb);
+            const float sk = warp_allsum(__fmaf_rn(k.y, k.y, __fmul_rn(k.x, k.x)));
+            if (lead) sm.red_k[u][half] = sk;
+            const float2 g = bf16x2_to_float2(gb);
+            float2 e;
+            e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
+            e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
+            *reinterpret_cast<float2 *>(&sm.tok.e[u][2 * c2]) = e;
+            *reinterpret_cast<float2 *>(&sm.tok.v[u][2 * c2]) = bf16x2_to_float2(vb);
+            const uint32_t bb = is_new ? sm.raw.beta_new[t] : (sm.raw.tail[u].x & 0xffffu);
+            if (c2 == 0) sm.tok.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+            if (is_new) {
+                const uint32_t qb = sm.raw.q[t][c2];
+                q = bf16x2_to_float2(qb);
+                const float sq = warp_allsum(__fmaf_rn(q.y, q.y, __fmul_rn(q.x, q.x)));
+                if (lead) sm.red_q[t][half] = sq;
+                __nv_bfloat16 *dst = rec + (size_t)t * kRecStride;
+                reinterpret_cast<uint32_t *>(dst)[c2] = kb;
+                reinterpret_cast<uint32_t *>(dst + kRecV)[c2] = vb;
+                reinterpret_cast<uint32_t *>(dst + kRecG)[c2] = gb;
+                if (c2 == 0) reinterpret_cast<uint16_t *>(dst)[kRecBeta] = (uint16_t)bb;
+            }
+        }
+        __syncthreads();  // both halves of the norms are in
+        if (active) {
+            const float ik = inv_l2(__fadd_rn(sm.red_k[u][0], sm.red_k[u][1]));
+            *reinterpret_cast<float2 *>(&sm.tok.kh[u][2 * c2]) =
+                make_float2(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik));
+            if (is_new) {
+                const float iq = inv_l2(__fadd_rn(sm.red_q[t][0], sm.red_q[t][1]));
+                *reinterpret_cast<float2 *>(&sm.tok.qh[t][2 * c2]) =
+                    make_float2(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
+                                __fmul_rn(__fmul_rn(q.y, iq), p.scale));
+            }
         }
     }
 }
@@ -347,9 +360,9 @@ __device__ __forceinline__ void prep_item(StepSmem &sm, const Params &p, const W
 //
 // Persistent: gridDim.x CTAs (two per SM) walk the tiles b*H + head with a
 // stride of gridDim.x, planned in rounds into a shared-memory work list.
-// While a CTA works on one item, the TMA unit prefetches the next item's
-// checkpoint into L2 and cp.async brings its raw inputs and gate parameters
-// into shared memory, so memory traffic overlaps the arithmetic.
+// While a CTA computes one item from registers, the next item's checkpoint
+// streams into shared memory through the TMA unit and its raw inputs and
+// gate parameters through cp.async, so memory and arithmetic overlap.
 
 template <Mode kMode, bool kBounded>
 __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int num_tiles) {
@@ -362,16 +375,23 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
     L.g = L.lane >> 3;
     L.j = L.lane & 7;
 
+    if (tid == 0) {
+        mbar_init(&sm.bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
     Cursor cursor{0, 0, 0};
     const int first = next_item<kMode>(p, sm, cursor, num_tiles, tid);
     if (first < 0) return;
     Work cur = list_item(sm, first, p.H);
-    if (tid == 0) prefetch_state(p, cur);
+    if (tid == 0) issue_state(p, cur, sm);
     fetch_raw<kMode>(p, cur, sm.raw, L.w, L.lane);
     uint32_t beta_next = 0;
     if (kMode == Mode::kVerify && tid < cur.T)
         beta_next = reinterpret_cast<const uint16_t *>(
             p.beta)[(size_t)(cur.bos + tid) * p.stride_beta + cur.head];
+    uint32_t phase = 0;
 
     while (true) {
         // raw inputs of `cur` have landed (each thread waits for its own
@@ -380,23 +400,29 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
         if (kMode == Mode::kVerify && tid < cur.T) sm.raw.beta_new[tid] = beta_next;
         __syncthreads();
 
-        // the checkpoint of `cur` (prefetched into L2 one item ago) is loaded
-        // straight into registers; the loads are in flight while the next
-        // item is planned and this item's token vectors are prepared
-        float *tile = p.pool + ((size_t)cur.slot * p.H + cur.head) * (size_t)(kD * kD);
-        float4 h[4][4];
-        load_tile(h, tile, L);
-        const int nidx = next_item<kMode>(p, sm, cursor, num_tiles, tid);
-        Work nxt;
-        if (nidx >= 0) {
-            nxt = list_item(sm, nidx, p.H);
-            if (tid == 0) prefetch_state(p, nxt);
-        }
         prep_item<kMode, kBounded>(sm, p, cur, tid);
-        __syncthreads();  // token vectors ready, raw inputs consumed
 
-        // start the next item's raw copies before computing this one
+        // checkpoint of `cur`: staged by the TMA unit
+        if (tid == 0) sm.ok = mbar_wait_bounded(&sm.bar, phase, kWaitBudget) ? 1 : 0;
+        __syncthreads();  // also: token vectors ready, raw inputs consumed
+        if (!sm.ok) {
+            if (tid == 0) {
+                flag_error(p.err, kErrWaitTimeout);
+                mbar_wait_bounded(&sm.bar, phase, kWaitBudget);
+            }
+            return;
+        }
+        mbar_try_wait(&sm.bar, phase);  // completed phase: acquires the staged bytes
+        phase ^= 1u;
+        float4 h[4][4];
+        load_tile(h, sm.state, L);
+        __syncthreads();  // staging buffer free
+
+        // start the next item's copies before computing this one
+        const int nidx = next_item<kMode>(p, sm, cursor, num_tiles, tid);
         if (nidx >= 0) {
+            const Work nxt = list_item(sm, nidx, p.H);
+            if (tid == 0) issue_state(p, nxt, sm);
             fetch_raw<kMode>(p, nxt, sm.raw, L.w, L.lane);
             if (kMode == Mode::kVerify && tid < nxt.T)
                 beta_next = reinterpret_cast<const uint16_t *>(
@@ -404,16 +430,19 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int n
         }
 
         // replay the folded / accepted records, store the state once
-        for (int u = 0; u < cur.p; ++u) token_plain(h, sm.tok, u, L);
+        float *tile = p.pool + ((size_t)cur.slot * p.H + cur.head) * (size_t)(kD * kD);
+        for (int u = 0; u < cur.p; ++u) token_step<false>(h, sm.tok, u, 0, L, nullptr);
         if (cur.p > 0) store_tile(h, tile, L);
         if constexpr (kMode == Mode::kVerify) {
-            const size_t tok0 = (size_t)cur.bos * p.H + cur.head;
-            run_verify_tokens(h, sm.tok, cur.p, cur.T, L, p.out + tok0 * kD, (size_t)p.H * kD,
-                              p.traj != nullptr ? p.traj + tok0 * (size_t)(kD * kD) : nullptr,
-                              (size_t)p.H * kD * kD);
+            for (int t = 0; t < cur.T; ++t) {
+                const size_t tok = (size_t)(cur.bos + t);
+                token_step<true>(h, sm.tok, cur.p + t, t, L, p.out + (tok * p.H + cur.head) * kD);
+                if (p.traj != nullptr)
+                    store_tile(h, p.traj + (tok * p.H + cur.head) * (size_t)(kD * kD), L);
+            }
         }
         if (nidx < 0) break;
-        cur = nxt;
+        cur = list_item(sm, nidx, p.H);
     }
 }
 
