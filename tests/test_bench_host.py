@@ -1,0 +1,147 @@
+"""Host-side logic of bench.py on CPU: the multi-rank reductions (world size 2
+over gloo), the per-rank seeds of weak scaling, the algorithmic byte count,
+the clock-sample summary and the profile lookup."""
+
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from linear_attention_speculative_kda_gb300 import workloads as W  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mx = bench.max_over_ranks(10.0 + rank, world, torch.device("cpu"))
+        sm = bench.sum_over_ranks(100.0 * (rank + 1), world, torch.device("cpu"))
+        out.put((rank, mx, sm, bench.shard_seed(0, rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_reductions_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=10) for _ in range(2))
+    assert [r[1] for r in res] == [11.0, 11.0]          # max over ranks
+    assert [r[2] for r in res] == [300.0, 300.0]        # sum over ranks
+    assert res[0][3] != res[1][3]                       # each rank its own batch
+
+
+def test_single_rank_reductions_are_identity():
+    assert bench.max_over_ranks(3.5, 1, None) == 3.5
+    assert bench.sum_over_ranks(7.0, 1, None) == 7.0
+
+
+def _bytes_by_loops(wl):
+    """Per-row loop of the algorithmic byte count: the state tile read once per
+    live row, 2052 bytes per verified token, and 131072 + 770 bytes per
+    replayed token for a commit, counted one row at a time."""
+    sp = wl.spec
+    lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
+    slots = wl.state_indices.tolist()
+    state, tok, rec = 65536, 2052, 770
+
+    def n_of(acc, T):
+        return min(max(acc, 0), T, sp.Q)
+
+    if not sp.deferred:
+        acc = wl.steps[0].num_accepted.tolist()
+        v = c = 0
+        for b in range(sp.B):
+            if slots[b] > 0 and lens[b] > 0:
+                v += state + lens[b] * tok
+            n = n_of(acc[b], lens[b])
+            if slots[b] > 0 and n > 0:
+                c += 2 * state + n * rec
+        return [v * sp.H, c * sp.H]
+    a1 = wl.steps[0].num_accepted.tolist()
+    a2 = wl.steps[1].num_accepted.tolist()
+    eg = wl.steps[0].eager.tolist()
+    v1 = c1 = v2 = c2 = 0
+    for b in range(sp.B):
+        live = slots[b] > 0
+        n1, n2 = n_of(a1[b], lens[b]), n_of(a2[b], lens[b])
+        if live and lens[b] > 0:
+            v1 += state + lens[b] * tok
+        if live and n1 > 0 and eg[b]:
+            c1 += 2 * state + n1 * rec
+        pend = n1 if (live and n1 > 0 and not eg[b]) else 0
+        if live and (lens[b] > 0 or pend > 0):
+            v2 += state + lens[b] * tok + (state + pend * rec if pend else 0)
+        if live and n2 > 0:
+            c2 += 2 * state + n2 * rec
+    return [x * sp.H for x in (v1, c1, v2, c2)]
+
+
+@pytest.mark.parametrize("name", ["tiny", "dflash7"])
+def test_plan_bytes_small(name):
+    wl = W.generate(name)
+    assert [b for _, b in bench.plan_bytes(wl)] == _bytes_by_loops(wl)
+
+
+def test_plan_bytes_deferred():
+    wl = W.custom(B=32, H=3, Q=4, lens=[4] * 30 + [0, 2], S=40, R=36, deferred=True, steps=2,
+                  seed=5, slots=[0] * 3 + list(range(4, 33)))
+    names = [n for n, _ in bench.plan_bytes(wl)]
+    assert names == ["verify", "commit_deferred", "verify_fused", "commit"]
+    assert [b for _, b in bench.plan_bytes(wl)] == _bytes_by_loops(wl)
+    assert bench.units_per_step(wl) == 2 * 32 * 3
+
+
+def test_clock_summary_filters_the_timed_window():
+    cs = bench.ClockSampler.__new__(bench.ClockSampler)
+    cs.window = (100.0, 101.0)
+
+    def row(sm, reason="Not Active", cap="Not Active"):
+        return ["2026/01/01 00:00:00.000", str(sm), "2070", "900.0", "0x0", reason,
+                "Not Active", "Not Active", cap]
+
+    cs.samples = [(99.0, row(1000)), (100.2, row(2070)), (100.6, row(2040, cap="Active")),
+                  (103.0, row(500, reason="Active"))]
+    s = cs.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == np.median([2070, 2040])
+    assert s["reasons"] == ["sw_power_cap"]
+    cs.samples = [(90.0, row(1800)), (100.5 + 5.0, row(1900))]
+    s = cs.summary()                        # nothing inside: nearest sample
+    assert s["samples"] == 1 and s["sm_mhz"] == 1900
+
+
+def test_profiled_traffic_requires_current_sources(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    csrc = tmp_path / "linear_attention_speculative_kda_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "a.cu").write_text("kernel v1")
+    h = bench.kernel_source_hash()
+    (tmp_path / "profiles" / "ncu_w.md").write_text(
+        f"source_hash: {h}\ntraffic[verify]: 1234\n")
+    assert bench.profiled_traffic("verify", "w") == 1234.0
+    assert bench.profiled_traffic("commit", "w") is None
+    (csrc / "a.cu").write_text("kernel v2")
+    assert bench.profiled_traffic("verify", "w") is None
