@@ -1,23 +1,23 @@
 // Device building blocks of the KDA verify / commit kernels (sm_103a).
 //
-// One CTA owns one (request row, head) state tile S (128 x 128 fp32, row v,
-// column k) for the whole window, in registers.  256 threads = 8 warps; warp
-// w owns rows 16w .. 16w+15.  Inside a warp, lane = 8*g + j: the thread owns
-// the 4 rows 16w + 4g + i (i = 0..3) and, of each row, the 16 columns
-// 32m + 4j + c (m = 0..3, c = 0..3), held as float4 h[i][m].  A row therefore
-// lives in the 8 lanes that share g, and its dot products (S k^, S q^) are
-// reduced across those 8 lanes with shuffles only: no shared memory and no
-// block barrier inside the token loop.
+// A consumer group of 128 threads (4 warps) owns one (request row, head)
+// state tile S (128 x 128 fp32, row v, column k) in registers for the whole
+// window.  Warp w owns rows 32w .. 32w+31; inside a warp, lane = 8*g + j and
+// the thread owns the 8 rows 32w + 8g + i (i = 0..7) and, of each row, the 16
+// columns 32m + 4j + c (m = 0..3, c = 0..3), held as float4 h[i][m].  A row
+// lives in the 8 lanes that share g, so its dot products (S k^, S q^) are
+// reduced across those 8 lanes with shuffles only.
 //
 // The per-token vectors that do not depend on the state (k^, q^, exp(g),
-// beta, v) are computed once per CTA per token and kept in shared memory; the
-// token loop reads them with conflict-free broadcast loads.
+// beta, v) are prepared by producer warps into shared memory; the token loop
+// reads them with conflict-free broadcast loads.
 //
 // Bit-exactness of commit against verify: the verify, the commit replay, the
-// deferred fold and the flush all run `token_step` below with the same thread
-// mapping, the same explicit round-to-nearest intrinsics (no contraction left
-// to the compiler) and the same reduction tree, so the state after token n is
-// the same bits whichever kernel computes it.
+// deferred fold and the flush all run the token pieces below with the same
+// thread mapping, the same explicit round-to-nearest intrinsics (no
+// contraction left to the compiler), the same reduction tree and the same
+// token preparation, so the state after a token has the same bits whichever
+// kernel computes it.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -26,8 +26,6 @@
 namespace kda {
 
 constexpr int kD = 128;             // head dim, K = V
-constexpr int kThreads = 256;       // threads per CTA
-constexpr int kWarps = kThreads / 32;
 constexpr int kMaxQ = 8;            // window limit
 constexpr int kRecStride = 392;     // bf16 elements per token record
 constexpr int kRecV = 128;          // offset of v inside a token record
@@ -63,16 +61,6 @@ struct Params {
     int *err;
 };
 
-// Per-token vectors of one window, in shared memory.  Slots [0, p) hold the
-// folded (recorded) tokens, [p, p + T) the new ones; q^ only for new tokens.
-struct TokenSmem {
-    float kh[2 * kMaxQ][kD];
-    float e[2 * kMaxQ][kD];
-    float v[2 * kMaxQ][kD];
-    float qh[kMaxQ][kD];
-    float beta[2 * kMaxQ];
-};
-
 // ---------------------------------------------------------------- helpers --
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
@@ -81,6 +69,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
     return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ float4 bf16x4_to_float4(uint2 u) {
+    const float2 a = bf16x2_to_float2(u.x), b = bf16x2_to_float2(u.y);
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // Butterfly sum over the 32 lanes: every lane ends with the same bits
@@ -114,30 +107,6 @@ __device__ __forceinline__ float sigmoidf_rn(float x) {
     return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
 }
 
-// ------------------------------------------------------------ state tile --
-
-struct Lane {
-    int w, g, j, lane;
-    __device__ __forceinline__ int row(int i) const { return 16 * w + 4 * g + i; }
-    __device__ __forceinline__ int col(int m) const { return 32 * m + 4 * j; }
-};
-
-__device__ __forceinline__ void load_tile(float4 (&h)[4][4], const float *tile, const Lane &L) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            h[i][m] = *reinterpret_cast<const float4 *>(tile + L.row(i) * kD + L.col(m));
-}
-
-__device__ __forceinline__ void store_tile(const float4 (&h)[4][4], float *tile, const Lane &L) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            *reinterpret_cast<float4 *>(tile + L.row(i) * kD + L.col(m)) = h[i][m];
-}
-
 // Packed pairs of fp32 operations (Blackwell's f32x2 forms): each lane does
 // two independent round-to-nearest multiplies or fused multiply-adds per
 // instruction, bit-identical to two scalar __fmul_rn / __fmaf_rn.
@@ -167,103 +136,166 @@ __device__ __forceinline__ float2 fma2(float ax, float ay, float bx, float by, f
     return unpack2(d);
 }
 
-// Row dot products of the thread's 4 rows with a vector x (its 16 columns),
-// in a fixed order: two interleaved partial sums per row (the even and the
-// odd columns of each float4, one packed pair), then their sum.
-__device__ __forceinline__ void row_partials(const float4 (&h)[4][4], const float4 (&x)[4],
-                                             float (&part)[4]) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 a = mul2(h[i][0].x, h[i][0].y, x[0].x, x[0].y);
-        a = fma2(h[i][0].z, h[i][0].w, x[0].z, x[0].w, a);
-#pragma unroll
-        for (int m = 1; m < 4; ++m) {
-            a = fma2(h[i][m].x, h[i][m].y, x[m].x, x[m].y, a);
-            a = fma2(h[i][m].z, h[i][m].w, x[m].z, x[m].w, a);
-        }
-        part[i] = __fadd_rn(a.x, a.y);
-    }
-}
-
-// Sum the 4 row partials over the 8 lanes of the row group (lane bits 0..2)
-// by a transpose-reduce: after it, lane j holds the full sum of row
-// R(j) = 2*bit2(j) + bit1(j); lanes j and j^1 hold identical bits.
-__device__ __forceinline__ float reduce_rows(const float (&part)[4], int j) {
-    const bool hi = (j & 4) != 0;
-    const float send0 = hi ? part[0] : part[2];
-    const float send1 = hi ? part[1] : part[3];
-    const float keep0 = hi ? part[2] : part[0];
-    const float keep1 = hi ? part[3] : part[1];
-    const float t0 = __fadd_rn(keep0, __shfl_xor_sync(kFull, send0, 4));
-    const float t1 = __fadd_rn(keep1, __shfl_xor_sync(kFull, send1, 4));
-    const bool mid = (j & 2) != 0;
-    const float send = mid ? t0 : t1;
-    const float keep = mid ? t1 : t0;
-    const float u = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 2));
-    return __fadd_rn(u, __shfl_xor_sync(kFull, u, 1));
-}
-
-__device__ __forceinline__ int reduced_row(int j) { return 2 * ((j >> 2) & 1) + ((j >> 1) & 1); }
-
-// One token of the recurrence on the thread's part of the tile:
-//   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T
-// and, when kOut, o = S q^ written as bf16 to out_row (128 outputs).
-template <bool kOut>
-__device__ __forceinline__ void token_step(float4 (&h)[4][4], const TokenSmem &sm, int slot,
-                                           int qslot, const Lane &L,
-                                           __nv_bfloat16 *out_row) {
-    float4 kk[4], ee[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        kk[m] = *reinterpret_cast<const float4 *>(&sm.kh[slot][L.col(m)]);
-        ee[m] = *reinterpret_cast<const float4 *>(&sm.e[slot][L.col(m)]);
-    }
-    // decay along K
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float2 lo = mul2(h[i][m].x, h[i][m].y, ee[m].x, ee[m].y);
-            const float2 hi = mul2(h[i][m].z, h[i][m].w, ee[m].z, ee[m].w);
-            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        }
-    // u = S k^ for the 4 rows, reduced over the row group
-    float part[4];
-    row_partials(h, kk, part);
-    const float u = reduce_rows(part, L.j);
-    const int R = reduced_row(L.j);
-    const float vr = sm.v[slot][L.row(R)];
-    const float vp = __fmul_rn(sm.beta[slot], __fsub_rn(vr, u));
-    // every lane of the group gets v' of its 4 rows (lanes 2i hold row i)
-    const int base = L.lane & ~7;
-    float vpi[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) vpi[i] = __shfl_sync(kFull, vp, base + 2 * i);
-    // rank-one update
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float2 lo =
-                fma2(vpi[i], vpi[i], kk[m].x, kk[m].y, make_float2(h[i][m].x, h[i][m].y));
-            const float2 hi =
-                fma2(vpi[i], vpi[i], kk[m].z, kk[m].w, make_float2(h[i][m].z, h[i][m].w));
-            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        }
-    if constexpr (kOut) {
-        float4 qq[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-            qq[m] = *reinterpret_cast<const float4 *>(&sm.qh[qslot][L.col(m)]);
-        float opart[4];
-        row_partials(h, qq, opart);
-        const float o = reduce_rows(opart, L.j);
-        if ((L.j & 1) == 0) out_row[L.row(R)] = __float2bfloat16_rn(o);
-    }
-}
-
 __device__ __forceinline__ void flag_error(int *err, int bits) {
     if (err != nullptr) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------- token vectors --
+//
+// One buffer of per-token vectors (fp32): slots [0, p) are folded (recorded)
+// tokens, [p, p + T) the new ones; q^ only for new tokens.
+struct TokView {
+    float *kh, *e, *v, *qh, *beta;
+    __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q) {
+        kh = reinterpret_cast<float *>(base);
+        e = kh + slots * kD;
+        v = e + slots * kD;
+        qh = v + slots * kD;
+        beta = qh + Q * kD;
+    }
+};
+
+__host__ __device__ inline int tok_buffer_bytes(int slots, int Q) {
+    return (3 * slots + Q) * kD * 4 + ((slots * 4 + 15) / 16) * 16;
+}
+
+// ------------------------------------------------------------ state tile --
+
+struct Lane {
+    int w, g, j, lane;
+    __device__ __forceinline__ int row(int i) const { return 32 * w + 8 * g + i; }
+    __device__ __forceinline__ int col(int m) const { return 32 * m + 4 * j; }
+};
+
+using Tile = float4[8][4];
+
+__device__ __forceinline__ void load_tile(Tile &h, const float *tile, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            h[i][m] = *reinterpret_cast<const float4 *>(tile + L.row(i) * kD + L.col(m));
+}
+
+__device__ __forceinline__ void store_tile(const Tile &h, float *tile, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4 *>(tile + L.row(i) * kD + L.col(m)) = h[i][m];
+}
+
+__device__ __forceinline__ float4 ld_cols(const float *vec, const Lane &L, int m) {
+    return *reinterpret_cast<const float4 *>(vec + L.col(m));
+}
+
+// Row dot products of the thread's 8 rows with a vector x (its 16 columns),
+// in a fixed order: two interleaved partial sums per row (the even and the
+// odd columns of each float4, one packed pair), then their sum.
+__device__ __forceinline__ void row_partials(const Tile &h, const float *x, const Lane &L,
+                                             float (&part)[8]) {
+    float2 acc[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 xx = ld_cols(x, L, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (m == 0)
+                acc[i] = mul2(h[i][0].x, h[i][0].y, xx.x, xx.y);
+            else
+                acc[i] = fma2(h[i][m].x, h[i][m].y, xx.x, xx.y, acc[i]);
+            acc[i] = fma2(h[i][m].z, h[i][m].w, xx.z, xx.w, acc[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[i] = __fadd_rn(acc[i].x, acc[i].y);
+}
+
+// Sum the 8 row partials over the 8 lanes of the row group (lane bits 0..2)
+// by a transpose-reduce: after it, lane j holds the full sum of row j.
+__device__ __forceinline__ float reduce_rows(const float (&part)[8], int j) {
+    const bool hi = (j & 4) != 0;
+    float t[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float send = hi ? part[q] : part[q + 4];
+        const float keep = hi ? part[q + 4] : part[q];
+        t[q] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 4));
+    }
+    const bool mid = (j & 2) != 0;
+    float t2[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float send = mid ? t[q] : t[q + 2];
+        const float keep = mid ? t[q + 2] : t[q];
+        t2[q] = __fadd_rn(keep, __shfl_xor_sync(kFull, send, 2));
+    }
+    const bool lo = (j & 1) != 0;
+    const float send = lo ? t2[0] : t2[1];
+    const float keep = lo ? t2[1] : t2[0];
+    return __fadd_rn(keep, __shfl_xor_sync(kFull, send, 1));
+}
+
+// Pieces of one token of the recurrence on the thread's part of the tile:
+//   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T;  o = S q^.
+
+// Decay along K in place, then the partial sums of u = S k^ of the 8 rows.
+__device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int slot, const Lane &L,
+                                               float (&part)[8]) {
+    const float *e = tv.e + slot * kD;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 ee = ld_cols(e, L, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 lo = mul2(h[i][m].x, h[i][m].y, ee.x, ee.y);
+            const float2 hi = mul2(h[i][m].z, h[i][m].w, ee.z, ee.w);
+            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+    }
+    row_partials(h, tv.kh + slot * kD, L, part);
+}
+
+// v' = beta (v - u) for the lane's row, shared with the row group, then the
+// rank-one update S <- S + v' k^T.
+__device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slot, float u,
+                                             const Lane &L) {
+    const float vr = tv.v[slot * kD + L.row(L.j)];
+    const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
+    const int base = L.lane & ~7;
+    float vpi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vpi[i] = __shfl_sync(kFull, vp, base + i);
+    const float *kh = tv.kh + slot * kD;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 kk = ld_cols(kh, L, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 lo =
+                fma2(vpi[i], vpi[i], kk.x, kk.y, make_float2(h[i][m].x, h[i][m].y));
+            const float2 hi =
+                fma2(vpi[i], vpi[i], kk.z, kk.w, make_float2(h[i][m].z, h[i][m].w));
+            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+    }
+}
+
+// One token without output (commit replay, deferred fold, flush).
+__device__ __forceinline__ void token_plain(Tile &h, const TokView &tv, int slot, const Lane &L) {
+    float part[8];
+    decay_partials(h, tv, slot, L, part);
+    delta_update(h, tv, slot, reduce_rows(part, L.j), L);
+}
+
+// One token with output o = S q^ (after the update) to out_row (bf16).
+__device__ __forceinline__ void token_out(Tile &h, const TokView &tv, int slot, int qslot,
+                                          const Lane &L, __nv_bfloat16 *out_row) {
+    token_plain(h, tv, slot, L);
+    float part[8];
+    row_partials(h, tv.qh + qslot * kD, L, part);
+    const float o = reduce_rows(part, L.j);
+    out_row[L.row(L.j)] = __float2bfloat16_rn(o);
 }
 
 }  // namespace kda

@@ -65,7 +65,7 @@ __device__ __forceinline__ __nv_bfloat16 *record_base(const Params &p, int r, in
 enum class Mode { kVerify, kCommit, kFlush };
 
 struct Work {
-    int tile;  // -1: no more work for this CTA
+    int tile;  // -1: none
     int head, slot, r, bos, T, p;
 };
 
@@ -125,152 +125,223 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
     return true;
 }
 
-// ---------------------------------------------------------- shared memory --
+// ------------------------------------------------------------------ roles --
+//
+// One CTA per SM, 384 threads in three warpgroups:
+//  - consumers 0 and 1 (128 threads each) each own one tile in registers at
+//    a time and run its tokens;
+//  - the producer (4 warps) plans the CTA's work, asks the TMA unit to stage
+//    each item's checkpoint into its consumer's shared-memory buffer, brings
+//    the raw inputs in with cp.async and prepares the per-token vectors
+//    ahead of the consumers (double-buffered when shared memory allows).
+// Items alternate between the two consumers.  Hand-offs use mbarriers; every
+// wait is bounded and gives up (error bit KDA_ERR_WAIT_TIMEOUT, all roles
+// leave) instead of hanging.
 
-constexpr int kPlanThreads = 128;   // candidates planned per round
-constexpr int kListCap = kPlanThreads;
-
-// The CTA's work list: candidate k of this CTA is tile blockIdx.x + k *
-// gridDim.x.  A planning round plans kPlanThreads candidates at once, one per
-// thread, and compacts the ones with work, in order, into the list.
-struct WorkList {
-    int tile[kListCap];
-    int slot[kListCap];
-    int r[kListCap];
-    int bos[kListCap];
-    int tp[kListCap];   // T | p << 8
-    int warp_count[kPlanThreads / 32];
-    int count;
-};
-
-// Raw bf16 inputs and gate parameters of one work item, brought in by
-// cp.async: token slots [0, p) are the folded record tokens, [p, p + T) the
-// new tokens.  Stored as channel pairs (one 32-bit word = 2 bf16).
-struct RawSmem {
-    uint32_t k[2 * kMaxQ][kD / 2];
-    uint32_t v[2 * kMaxQ][kD / 2];
-    uint32_t g[2 * kMaxQ][kD / 2];
-    uint32_t q[kMaxQ][kD / 2];
-    uint2 tail[kMaxQ];          // record tails: beta_raw bits in the low half
-    float bias[kD];             // g_bias of the item's head
-    float a_log;                // A_log of the item's head
-    uint32_t beta_new[kMaxQ];   // beta_raw bits of the new tokens
-};
-
-struct __align__(16) StepSmem {
-    float state[kD * kD];       // staging of the next item's checkpoint (TMA)
-    TokenSmem tok;              // per-token vectors of the current item
-    RawSmem raw;                // raw inputs of the current / next item
-    float red_k[2 * kMaxQ][2];  // per-warp halves of |k|^2
-    float red_q[kMaxQ][2];      // per-warp halves of |q|^2
-    WorkList list;
-    uint64_t bar;               // completion of the staging copy
-    int ok;
-};
-
+constexpr int kConsumerThreads = 128;
+constexpr int kProducerWarps = 4;
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kBlockThreads = 2 * kConsumerThreads + kProducerThreads;
+constexpr int kProducerBarrier = 1;  // named barrier of the producer warps
+constexpr int kPlanSize = kProducerThreads;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
+constexpr int kConsumerRegs = 208;
+constexpr int kProducerRegs = 88;
+static_assert(2 * kConsumerThreads * kConsumerRegs + kProducerThreads * kProducerRegs <=
+                  kBlockThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+
+template <int N>
+__device__ __forceinline__ void reg_alloc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void reg_dealloc() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+struct ItemInfo {
+    int tile, slot, head, bos, T, p, end, pad;
+};
+
+struct WorkList {
+    int tile[kPlanSize];
+    int slot[kPlanSize];
+    int r[kPlanSize];
+    int bos[kPlanSize];
+    int tp[kPlanSize];   // T | p << 8
+    int warp_count[kProducerWarps];
+    int count;
+    int pad;
+};
+
+// Hand-off barriers and the abort flag.
+struct Sync {
+    uint64_t full_state[2];    // TMA of a consumer's checkpoint landed
+    uint64_t empty_state[2];   // the consumer has copied it into registers
+    uint64_t full_tok[2][2];   // token vectors of an item are ready
+    uint64_t empty_tok[2][2];  // the consumer is done with them
+    ItemInfo info[2][2];
+    int abort;
+    int pad[3];
+};
+
+// Raw bf16 inputs and gate parameters of one item, in channel pairs.
+struct RawView {
+    uint32_t *k, *v, *g, *q;
+    uint2 *tail;                // record tails: beta_raw bits in the low half
+    float *bias;                // g_bias of the item's head (128)
+    float *a_log;
+    uint32_t *beta_new;         // beta_raw bits of the new tokens
+    __device__ __forceinline__ RawView(unsigned char *base, int slots, int Q) {
+        k = reinterpret_cast<uint32_t *>(base);
+        v = k + slots * (kD / 2);
+        g = v + slots * (kD / 2);
+        q = g + slots * (kD / 2);
+        tail = reinterpret_cast<uint2 *>(q + Q * (kD / 2));
+        bias = reinterpret_cast<float *>(tail + ((Q + 1) / 2) * 2);
+        a_log = bias + kD;
+        beta_new = reinterpret_cast<uint32_t *>(a_log + 4);
+    }
+};
+
+__host__ __device__ inline int raw_buffer_bytes(int slots, int Q) {
+    return slots * 3 * (kD * 2) + Q * (kD * 2) + ((Q + 1) / 2) * 16 + kD * 4 + 16 +
+           ((Q * 4 + 15) / 16) * 16;
+}
+
+// Shared-memory layout of a launch (window Q, whether the verify folds).
+struct Layout {
+    int slots, nbuf, tok_bytes, raw_bytes;
+    int off_state, off_tok, off_raw, off_list, off_sync, total;
+};
+
+__host__ __device__ inline Layout make_layout(int Q, bool fold) {
+    Layout l;
+    l.slots = fold ? 2 * Q : Q;
+    l.tok_bytes = tok_buffer_bytes(l.slots, Q);
+    l.raw_bytes = raw_buffer_bytes(l.slots, Q);
+    l.off_state = 0;                                // 2 x 64 KiB staging
+    l.off_tok = 2 * kD * kD * 4;
+    const int fixed = l.off_tok + 2 * l.raw_bytes + (int)sizeof(WorkList) + (int)sizeof(Sync);
+    l.nbuf = fixed + 4 * l.tok_bytes <= kSmemBudget ? 2 : 1;
+    l.off_raw = l.off_tok + 2 * l.nbuf * l.tok_bytes;
+    l.off_list = l.off_raw + 2 * l.raw_bytes;
+    l.off_sync = l.off_list + (int)sizeof(WorkList);
+    l.total = l.off_sync + (int)sizeof(Sync);
+    return l;
+}
+
+// Bounded wait shared by all roles: gives up on timeout or when another
+// role has given up.
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Sync &sy,
+                                           const Params &p) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(&sy.abort)) return false;
+        if (clock64() - t0 > kWaitBudget) {
+            *reinterpret_cast<volatile int *>(&sy.abort) = 1;
+            flag_error(p.err, kErrWaitTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void producer_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kProducerBarrier), "n"(kProducerThreads) : "memory");
+}
 
 __device__ __forceinline__ int num_candidates(int num_tiles) {
     const int first = (int)blockIdx.x;
     return first < num_tiles ? (num_tiles - first + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 }
 
-// One planning round over candidates [k0, k0 + kPlanThreads); all threads
-// take part (it contains barriers).  Returns the number of listed items.
+// One planning round over candidates [k0, k0 + kPlanSize) by the producer
+// threads; compacts the tiles with work, in order, into the list.
 template <Mode kMode>
-__device__ int plan_round(const Params &p, StepSmem &sm, int k0, int num_tiles, int tid) {
+__device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles, int pt) {
     const int K = num_candidates(num_tiles);
     Work w;
     bool has = false;
-    if (tid < kPlanThreads) {
-        const int k = k0 + tid;
-        if (k < K) has = plan_tile<kMode>(p, (int)blockIdx.x + k * (int)gridDim.x, w);
-    }
+    const int k = k0 + pt;
+    if (k < K) has = plan_tile<kMode>(p, (int)blockIdx.x + k * (int)gridDim.x, w);
     const unsigned ballot = __ballot_sync(kFull, has);
-    const int lane = tid & 31, warp = tid >> 5;
-    if (tid < kPlanThreads && lane == 0) sm.list.warp_count[warp] = __popc(ballot);
-    __syncthreads();
+    const int lane = pt & 31, warp = pt >> 5;
+    if (lane == 0) list.warp_count[warp] = __popc(ballot);
+    producer_sync();
     int before = 0, total = 0;
 #pragma unroll
-    for (int i = 0; i < kPlanThreads / 32; ++i) {
-        const int c = sm.list.warp_count[i];
+    for (int i = 0; i < kProducerWarps; ++i) {
+        const int c = list.warp_count[i];
         if (i < warp) before += c;
         total += c;
     }
     if (has) {
         const int pos = before + __popc(ballot & ((1u << lane) - 1u));
-        sm.list.tile[pos] = w.tile;
-        sm.list.slot[pos] = w.slot;
-        sm.list.r[pos] = w.r;
-        sm.list.bos[pos] = w.bos;
-        sm.list.tp[pos] = w.T | (w.p << 8);
+        list.tile[pos] = w.tile;
+        list.slot[pos] = w.slot;
+        list.r[pos] = w.r;
+        list.bos[pos] = w.bos;
+        list.tp[pos] = w.T | (w.p << 8);
     }
-    __syncthreads();
+    producer_sync();
     return total;
 }
 
-__device__ __forceinline__ Work list_item(const StepSmem &sm, int i, int H) {
-    Work w;
-    w.tile = sm.list.tile[i];
-    w.head = w.tile % H;
-    w.slot = sm.list.slot[i];
-    w.r = sm.list.r[i];
-    w.bos = sm.list.bos[i];
-    const int tp = sm.list.tp[i];
-    w.T = tp & 0xff;
-    w.p = tp >> 8;
-    return w;
-}
-
-// Cursor over the CTA's work: the list of the current round and where the
-// next round starts.  Uniform across the CTA.
 struct Cursor {
     int idx, count, next_k;
 };
 
-// Advance to the next listed item (planning a new round when the list is
-// used up).  Returns its list index, or -1 when the CTA has no more work.
-// The item stays readable in the list until the following call.
+// The producer's next work item (planning a new round when needed), or a
+// Work with tile -1 when the CTA has no more.
 template <Mode kMode>
-__device__ __forceinline__ int next_item(const Params &p, StepSmem &sm, Cursor &c, int num_tiles,
-                                         int tid) {
+__device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Cursor &c,
+                                          int num_tiles, int pt) {
     const int K = num_candidates(num_tiles);
+    Work w;
+    w.tile = -1;
     while (c.idx >= c.count) {
-        if (c.next_k >= K) return -1;
-        c.count = plan_round<kMode>(p, sm, c.next_k, num_tiles, tid);
-        c.next_k += kPlanThreads;
+        if (c.next_k >= K) return w;
+        c.count = plan_round<kMode>(p, list, c.next_k, num_tiles, pt);
+        c.next_k += kPlanSize;
         c.idx = 0;
     }
-    return c.idx++;
+    const int i = c.idx++;
+    w.tile = list.tile[i];
+    w.head = w.tile % p.H;
+    w.slot = list.slot[i];
+    w.r = list.r[i];
+    w.bos = list.bos[i];
+    w.T = list.tp[i] & 0xff;
+    w.p = list.tp[i] >> 8;
+    return w;
 }
 
-__device__ __forceinline__ void issue_state(const Params &p, const Work &w, StepSmem &sm) {
-    const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
-    mbar_arrive_expect_tx(&sm.bar, kD * kD * 4);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        bulk_load(sm.state + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, &sm.bar);
-}
-
-// Raw inputs and gate parameters of an item into shared memory (cp.async).
+// Raw inputs and gate parameters of an item into a raw buffer (cp.async by
+// the producer threads).
 template <Mode kMode>
-__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSmem &raw, int warp,
-                                          int lane) {
+__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, int pt) {
+    const int lane = pt & 31, warp = pt >> 5;
     const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int c = warp; c < 3 * w.p; c += kWarps) {
+    for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
         const int u = c / 3;
         const int part = c - 3 * u;
         const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
-        uint32_t *dst = part == 0 ? raw.k[u] : (part == 1 ? raw.v[u] : raw.g[u]);
+        uint32_t *dst = (part == 0 ? rv.k : (part == 1 ? rv.v : rv.g)) + u * (kD / 2);
         cp_async8(dst + 2 * lane, src + lane);
     }
-    if (warp == kWarps - 1) {
-        if (lane < w.p) cp_async8(&raw.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
-        if (lane == 31) cp_async4(&raw.a_log, p.A_log + w.head);
+    if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
+    if (warp == kProducerWarps - 1) {
+        cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
+        if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
     }
-    if (warp == kWarps - 2) cp_async16(&raw.bias[4 * lane], p.g_bias + w.head * kD + 4 * lane);
     if constexpr (kMode == Mode::kVerify) {
-        for (int c = warp; c < 4 * w.T; c += kWarps) {
+        for (int c = warp; c < 4 * w.T; c += kProducerWarps) {
             const int t = c >> 2;
             const int part = c & 3;
             const size_t tok = (size_t)(w.bos + t);
@@ -278,16 +349,16 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSme
             uint32_t *dst;
             if (part == 0) {
                 src = p.k + tok * p.stride_k;
-                dst = raw.k[w.p + t];
+                dst = rv.k + (w.p + t) * (kD / 2);
             } else if (part == 1) {
                 src = p.v + tok * p.stride_v;
-                dst = raw.v[w.p + t];
+                dst = rv.v + (w.p + t) * (kD / 2);
             } else if (part == 2) {
                 src = p.g + tok * p.stride_g;
-                dst = raw.g[w.p + t];
+                dst = rv.g + (w.p + t) * (kD / 2);
             } else {
                 src = p.q + tok * p.stride_q;
-                dst = raw.q[t];
+                dst = rv.q + t * (kD / 2);
             }
             cp_async8(dst + 2 * lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
         }
@@ -295,154 +366,212 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawSme
     cp_async_commit();
 }
 
-// Per-token vectors of an item, all 8 warps: token u is prepared by the 64
-// threads of quarter (u & 3) in pass (u >> 2), two channels per thread, so
-// every token is computed the same way however many tokens the item has.
-// The verify also writes the new tokens' raw records.
+// Per-token vectors of an item: token u is prepared by producer warp
+// (u mod 2), four channels per lane, the norms summed across the warp; every
+// token is computed the same way however many tokens the item has.  The
+// verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
-__device__ __forceinline__ void prep_item(StepSmem &sm, const Params &p, const Work &w, int tid) {
-    const int quarter = tid >> 6;
-    const int c2 = tid & 63;              // channels 2*c2, 2*c2 + 1
-    const int half = c2 >> 5;             // which of the quarter's two warps
-    const bool lead = (tid & 31) == 0;
-    const int total = w.p + w.T;
-    const int passes = (total + 3) >> 2;
-    const float a = expf(sm.raw.a_log);
-    const float2 bias = *reinterpret_cast<const float2 *>(&sm.raw.bias[2 * c2]);
+__device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView rv, TokView tv,
+                                          int pt) {
+    const int lane = pt & 31, warp = pt >> 5;
+    const float a = expf(*rv.a_log);
+    const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
     __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int pass = 0; pass < passes; ++pass) {
-        const int u = 4 * pass + quarter;
-        const bool active = u < total;
+    for (int u = warp; u < w.p + w.T; u += kProducerWarps) {
         const bool is_new = kMode == Mode::kVerify && u >= w.p;
         const int t = u - w.p;
-        float2 k = make_float2(0.f, 0.f), q = make_float2(0.f, 0.f);
-        if (active) {
-            const uint32_t kb = sm.raw.k[u][c2], vb = sm.raw.v[u][c2], gb = sm.raw.g[u][c2];
-            k = bf16x2_to_float2(kb);
-            const float sk = warp_allsum(__fmaf_rn(k.y, k.y, __fmul_rn(k.x, k.x)));
-            if (lead) sm.red_k[u][half] = sk;
-            const float2 g = bf16x2_to_float2(gb);
-            float2 e;
-            e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
-            e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
-            *reinterpret_cast<float2 *>(&sm.tok.e[u][2 * c2]) = e;
-            *reinterpret_cast<float2 *>(&sm.tok.v[u][2 * c2]) = bf16x2_to_float2(vb);
-            const uint32_t bb = is_new ? sm.raw.beta_new[t] : (sm.raw.tail[u].x & 0xffffu);
-            if (c2 == 0) sm.tok.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
-            if (is_new) {
-                const uint32_t qb = sm.raw.q[t][c2];
-                q = bf16x2_to_float2(qb);
-                const float sq = warp_allsum(__fmaf_rn(q.y, q.y, __fmul_rn(q.x, q.x)));
-                if (lead) sm.red_q[t][half] = sq;
-                __nv_bfloat16 *dst = rec + (size_t)t * kRecStride;
-                reinterpret_cast<uint32_t *>(dst)[c2] = kb;
-                reinterpret_cast<uint32_t *>(dst + kRecV)[c2] = vb;
-                reinterpret_cast<uint32_t *>(dst + kRecG)[c2] = gb;
-                if (c2 == 0) reinterpret_cast<uint16_t *>(dst)[kRecBeta] = (uint16_t)bb;
-            }
-        }
-        __syncthreads();  // both halves of the norms are in
-        if (active) {
-            const float ik = inv_l2(__fadd_rn(sm.red_k[u][0], sm.red_k[u][1]));
-            *reinterpret_cast<float2 *>(&sm.tok.kh[u][2 * c2]) =
-                make_float2(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik));
-            if (is_new) {
-                const float iq = inv_l2(__fadd_rn(sm.red_q[t][0], sm.red_q[t][1]));
-                *reinterpret_cast<float2 *>(&sm.tok.qh[t][2 * c2]) =
-                    make_float2(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
-                                __fmul_rn(__fmul_rn(q.y, iq), p.scale));
-            }
+        const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
+        const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
+        const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
+        const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
+        const float4 k = bf16x4_to_float4(kb);
+        float s = __fmul_rn(k.x, k.x);
+        s = __fmaf_rn(k.y, k.y, s);
+        s = __fmaf_rn(k.z, k.z, s);
+        s = __fmaf_rn(k.w, k.w, s);
+        const float ik = inv_l2(warp_allsum(s));
+        *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) =
+            make_float4(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik), __fmul_rn(k.z, ik),
+                        __fmul_rn(k.w, ik));
+        const float4 g = bf16x4_to_float4(gb);
+        float4 e;
+        e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
+        e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
+        e.z = decay_factor(__fadd_rn(g.z, bias.z), a, kBounded, p.lower_bound);
+        e.w = decay_factor(__fadd_rn(g.w, bias.w), a, kBounded, p.lower_bound);
+        *reinterpret_cast<float4 *>(tv.e + u * kD + 4 * lane) = e;
+        *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
+        if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+        if (is_new) {
+            const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
+            float sq = __fmul_rn(q.x, q.x);
+            sq = __fmaf_rn(q.y, q.y, sq);
+            sq = __fmaf_rn(q.z, q.z, sq);
+            sq = __fmaf_rn(q.w, q.w, sq);
+            const float iq = inv_l2(warp_allsum(sq));
+            *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
+                make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.y, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.z, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.w, iq), p.scale));
+            uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
+            dst[lane] = kb;
+            dst[kRecV / 4 + lane] = vb;
+            dst[kRecG / 4 + lane] = gb;
+            if (lane == 0) reinterpret_cast<uint16_t *>(rec + (size_t)t * kRecStride)[kRecBeta] = (uint16_t)bb;
         }
     }
 }
 
-// ------------------------------------------------------------------ kernel --
-//
-// Persistent: gridDim.x CTAs (two per SM) walk the tiles b*H + head with a
-// stride of gridDim.x, planned in rounds into a shared-memory work list.
-// While a CTA computes one item from registers, the next item's checkpoint
-// streams into shared memory through the TMA unit and its raw inputs and
-// gate parameters through cp.async, so memory and arithmetic overlap.
+__device__ __forceinline__ void issue_state(const Params &p, const Work &w, float *dst,
+                                            uint64_t *bar) {
+    const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
+    mbar_arrive_expect_tx(bar, kD * kD * 4);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        bulk_load(dst + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, bar);
+}
 
 template <Mode kMode, bool kBounded>
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(const Params p, int num_tiles) {
-    extern __shared__ __align__(128) unsigned char smem_bytes[];
-    StepSmem &sm = *reinterpret_cast<StepSmem *>(smem_bytes);
-    const int tid = threadIdx.x;
+__device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
+                             int num_tiles, int pt) {
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
+    WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
+    Cursor cursor{0, 0, 0};
+    Work cur = next_work<kMode>(p, list, cursor, num_tiles, pt);
+    int rb = 0;
+    uint32_t beta_next = 0;
+    if (cur.tile >= 0) {
+        fetch_raw<kMode>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q), pt);
+        if (kMode == Mode::kVerify && pt < cur.T)
+            beta_next = reinterpret_cast<const uint16_t *>(
+                p.beta)[(size_t)(cur.bos + pt) * p.stride_beta + cur.head];
+    }
+    int n = 0;
+    bool ok = true;
+    while (cur.tile >= 0) {
+        const int c = n & 1;
+        const int use_c = n >> 1;
+        // checkpoint of `cur` into consumer c's staging buffer
+        if (pt == 0) {
+            if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
+            if (ok)
+                issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
+                            &sy.full_state[c]);
+        }
+        // raw inputs of `cur` have landed; start those of the next item
+        RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
+        cp_async_wait_all();
+        if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new[pt] = beta_next;
+        const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
+        if (nxt.tile >= 0) {
+            fetch_raw<kMode>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
+                                             lay.slots, p.Q), pt);
+            if (kMode == Mode::kVerify && pt < nxt.T)
+                beta_next = reinterpret_cast<const uint16_t *>(
+                    p.beta)[(size_t)(nxt.bos + pt) * p.stride_beta + nxt.head];
+        }
+        // token vectors of `cur` into consumer c's buffer b, once it is free
+        const int b = use_c % lay.nbuf;
+        const int use_b = use_c / lay.nbuf;
+        if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
+        producer_sync();
+        if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
+        TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
+        prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
+        if (pt == 0) {
+            ItemInfo &it = sy.info[c][b];
+            it.tile = cur.tile;
+            it.slot = cur.slot;
+            it.head = cur.head;
+            it.bos = cur.bos;
+            it.T = cur.T;
+            it.p = cur.p;
+            it.end = 0;
+        }
+        producer_sync();  // all token vectors and the item info written
+        if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
+        ++n;
+        rb ^= 1;
+        cur = nxt;
+    }
+    // end markers: the next buffer of each consumer says "no more items"
+    if (pt == 0) {
+        for (int c = 0; c < 2; ++c) {
+            const int use_c = (n + 1 - c) >> 1;
+            const int b = use_c % lay.nbuf;
+            const int use_b = use_c / lay.nbuf;
+            if (use_b > 0 && !wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p)) return;
+            sy.info[c][b].end = 1;
+            mbar_arrive(&sy.full_tok[c][b]);
+        }
+    }
+}
+
+template <Mode kMode>
+__device__ void run_consumer(const Params &p, unsigned char *smem, const Layout &lay, int c,
+                             int ct) {
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     Lane L;
-    L.lane = tid & 31;
-    L.w = tid >> 5;
+    L.lane = ct & 31;
+    L.w = ct >> 5;
     L.g = L.lane >> 3;
     L.j = L.lane & 7;
+    const float *staging = reinterpret_cast<const float *>(smem + lay.off_state) + c * kD * kD;
+    for (int k = 0;; ++k) {
+        const int b = k % lay.nbuf;
+        const int use_b = k / lay.nbuf;
+        if (!wait_phase(&sy.full_tok[c][b], use_b & 1, sy, p)) return;
+        const ItemInfo it = sy.info[c][b];
+        if (it.end) return;
+        if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
+        Tile h;
+        load_tile(h, staging, L);
+        mbar_arrive(&sy.empty_state[c]);
+        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
+        float *tile = p.pool + ((size_t)it.slot * p.H + it.head) * (size_t)(kD * kD);
+        for (int u = 0; u < it.p; ++u) token_plain(h, tv, u, L);
+        if (it.p > 0) store_tile(h, tile, L);
+        if constexpr (kMode == Mode::kVerify) {
+            for (int t = 0; t < it.T; ++t) {
+                const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
+                token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
+                if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
+            }
+        }
+        mbar_arrive(&sy.empty_tok[c][b]);
+    }
+}
 
+template <Mode kMode, bool kBounded>
+__global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
+                                                                  int fold) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const Layout lay = make_layout(p.Q, fold != 0);
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
+    const int tid = threadIdx.x;
     if (tid == 0) {
-        mbar_init(&sm.bar, 1);
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(&sy.full_state[c], 1);
+            mbar_init(&sy.empty_state[c], kConsumerThreads);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&sy.full_tok[c][b], 1);
+                mbar_init(&sy.empty_tok[c][b], kConsumerThreads);
+            }
+        }
+        sy.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
-
-    Cursor cursor{0, 0, 0};
-    const int first = next_item<kMode>(p, sm, cursor, num_tiles, tid);
-    if (first < 0) return;
-    Work cur = list_item(sm, first, p.H);
-    if (tid == 0) issue_state(p, cur, sm);
-    fetch_raw<kMode>(p, cur, sm.raw, L.w, L.lane);
-    uint32_t beta_next = 0;
-    if (kMode == Mode::kVerify && tid < cur.T)
-        beta_next = reinterpret_cast<const uint16_t *>(
-            p.beta)[(size_t)(cur.bos + tid) * p.stride_beta + cur.head];
-    uint32_t phase = 0;
-
-    while (true) {
-        // raw inputs of `cur` have landed (each thread waits for its own
-        // copies; the barrier publishes them and frees the token vectors)
-        cp_async_wait_all();
-        if (kMode == Mode::kVerify && tid < cur.T) sm.raw.beta_new[tid] = beta_next;
-        __syncthreads();
-
-        prep_item<kMode, kBounded>(sm, p, cur, tid);
-
-        // checkpoint of `cur`: staged by the TMA unit
-        if (tid == 0) sm.ok = mbar_wait_bounded(&sm.bar, phase, kWaitBudget) ? 1 : 0;
-        __syncthreads();  // also: token vectors ready, raw inputs consumed
-        if (!sm.ok) {
-            if (tid == 0) {
-                flag_error(p.err, kErrWaitTimeout);
-                mbar_wait_bounded(&sm.bar, phase, kWaitBudget);
-            }
-            return;
-        }
-        mbar_try_wait(&sm.bar, phase);  // completed phase: acquires the staged bytes
-        phase ^= 1u;
-        float4 h[4][4];
-        load_tile(h, sm.state, L);
-        __syncthreads();  // staging buffer free
-
-        // start the next item's copies before computing this one
-        const int nidx = next_item<kMode>(p, sm, cursor, num_tiles, tid);
-        if (nidx >= 0) {
-            const Work nxt = list_item(sm, nidx, p.H);
-            if (tid == 0) issue_state(p, nxt, sm);
-            fetch_raw<kMode>(p, nxt, sm.raw, L.w, L.lane);
-            if (kMode == Mode::kVerify && tid < nxt.T)
-                beta_next = reinterpret_cast<const uint16_t *>(
-                    p.beta)[(size_t)(nxt.bos + tid) * p.stride_beta + nxt.head];
-        }
-
-        // replay the folded / accepted records, store the state once
-        float *tile = p.pool + ((size_t)cur.slot * p.H + cur.head) * (size_t)(kD * kD);
-        for (int u = 0; u < cur.p; ++u) token_step<false>(h, sm.tok, u, 0, L, nullptr);
-        if (cur.p > 0) store_tile(h, tile, L);
-        if constexpr (kMode == Mode::kVerify) {
-            for (int t = 0; t < cur.T; ++t) {
-                const size_t tok = (size_t)(cur.bos + t);
-                token_step<true>(h, sm.tok, cur.p + t, t, L, p.out + (tok * p.H + cur.head) * kD);
-                if (p.traj != nullptr)
-                    store_tile(h, p.traj + (tok * p.H + cur.head) * (size_t)(kD * kD), L);
-            }
-        }
-        if (nidx < 0) break;
-        cur = list_item(sm, nidx, p.H);
+    // Register split: the launch gives every thread kLaunchRegs; the producer
+    // warpgroup hands registers back and the consumers take them, so that
+    // 2 * 128 * kConsumerRegs + 128 * kProducerRegs == 384 * kLaunchRegs.
+    if (tid < 2 * kConsumerThreads) {
+        reg_alloc<kConsumerRegs>();
+        run_consumer<kMode>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
+    } else {
+        reg_dealloc<kProducerRegs>();
+        run_producer<kMode, kBounded>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
     }
 }
 
@@ -519,24 +648,23 @@ int sm_count() {
     return n;
 }
 
-// Launch the persistent step kernel: two CTAs per SM (or one per tile when
-// there are fewer tiles), each with the StepSmem layout in dynamic shared
-// memory.
+// Launch the warp-specialized step kernel: one CTA per SM (or one per tile
+// when there are fewer tiles), the shared-memory layout sized by the window.
 template <kda::Mode M>
-kda_status launch_step(const Params &p, bool bounded, cudaStream_t stream) {
+kda_status launch_step(const Params &p, bool bounded, bool fold, cudaStream_t stream) {
     const long long tiles = (long long)p.B * p.H;
     const int sms = sm_count();
     if (sms <= 0) return KDA_ERR_CUDA;
-    const int grid = (int)(tiles < 2LL * sms ? tiles : 2LL * sms);
-    const size_t smem = sizeof(kda::StepSmem);
-    void (*kern)(const Params, int) =
+    const int grid = (int)(tiles < (long long)sms ? tiles : (long long)sms);
+    const kda::Layout lay = kda::make_layout(p.Q, fold);
+    void (*kern)(const Params, int, int) =
         bounded ? kda::step_kernel<M, true> : kda::step_kernel<M, false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return KDA_ERR_CUDA;
-    kern<<<grid, kda::kThreads, smem, stream>>>(p, (int)tiles);
+    kern<<<grid, kda::kBlockThreads, lay.total, stream>>>(p, (int)tiles, fold ? 1 : 0);
     return finish_launch();
 }
 
@@ -591,7 +719,7 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     p.traj = trajectory_out;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0,
+    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0, pending != nullptr,
                                            static_cast<cudaStream_t>(stream));
 }
 
@@ -624,7 +752,7 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     p.eager = eager;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0,
+    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,
                                            static_cast<cudaStream_t>(stream));
 }
 
@@ -650,7 +778,7 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
     p.pending_in = pending;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0,
+    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0, false,
                                           static_cast<cudaStream_t>(stream));
 }
 
