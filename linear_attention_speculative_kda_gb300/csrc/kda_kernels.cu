@@ -127,28 +127,29 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
 
 // ------------------------------------------------------------------ roles --
 //
-// One CTA per SM, 512 threads in four warpgroups forming two independent
-// pipelines.  Pipeline c (c = 0, 1) is:
-//  - consumer warpgroup c: owns one tile in registers at a time and runs its
-//    tokens;
-//  - producer warpgroup c: plans the pipeline's share of the CTA's tiles,
-//    asks the TMA unit to stage each item's checkpoint into the consumer's
-//    shared-memory buffer, brings the raw inputs in with cp.async and
-//    prepares the per-token vectors ahead of the consumer (double-buffered
-//    when shared memory allows).
-// Hand-offs use mbarriers; every wait is bounded and gives up (error bit
-// KDA_ERR_WAIT_TIMEOUT, every role leaves) instead of hanging.
+// One CTA per SM, 384 threads in three warpgroups:
+//  - consumers 0 and 1 (128 threads each) each own one tile in registers at
+//    a time and run its tokens;
+//  - the producer (4 warps) plans the CTA's work, asks the TMA unit to stage
+//    each item's checkpoint into its consumer's shared-memory buffer, brings
+//    the raw inputs in with cp.async and prepares the per-token vectors
+//    ahead of the consumers (double-buffered when shared memory allows).
+// Items alternate between the two consumers.  Hand-offs use mbarriers; every
+// wait is bounded and gives up (error bit KDA_ERR_WAIT_TIMEOUT, all roles
+// leave) instead of hanging.
 
-constexpr int kGroupThreads = 128;                 // one warpgroup
-constexpr int kPipes = 2;
-constexpr int kBlockThreads = 2 * kPipes * kGroupThreads;
-constexpr int kPlanSize = kGroupThreads;
+constexpr int kConsumerThreads = 128;
+constexpr int kProducerWarps = 4;
+constexpr int kProducerThreads = 32 * kProducerWarps;
+constexpr int kBlockThreads = 2 * kConsumerThreads + kProducerThreads;
+constexpr int kProducerBarrier = 1;  // named barrier of the producer warps
+constexpr int kPlanSize = kProducerThreads;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kSmemBudget = 227 * 1024;
-constexpr int kLaunchRegs = 128;     // 65536 / 512
-constexpr int kConsumerRegs = 200;
-constexpr int kProducerRegs = 56;
-static_assert(kPipes * kGroupThreads * (kConsumerRegs + kProducerRegs) <=
+constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
+constexpr int kConsumerRegs = 208;
+constexpr int kProducerRegs = 88;
+static_assert(2 * kConsumerThreads * kConsumerRegs + kProducerThreads * kProducerRegs <=
                   kBlockThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 
@@ -172,20 +173,18 @@ struct WorkList {
     int r[kPlanSize];
     int bos[kPlanSize];
     int tp[kPlanSize];   // T | p << 8
-    int warp_count[4];
+    int warp_count[kProducerWarps];
+    int count;
+    int pad;
 };
 
-// Per-pipeline hand-off barriers, item info and the CTA's abort flag.
+// Hand-off barriers and the abort flag.
 struct Sync {
-    uint64_t full_state;    // TMA of the consumer's checkpoint landed
-    uint64_t empty_state;   // the consumer has copied it into registers
-    uint64_t full_tok[2];   // token vectors of an item are ready
-    uint64_t empty_tok[2];  // the consumer is done with them
-    ItemInfo info[2];
-};
-
-struct Shared {
-    Sync pipe[kPipes];
+    uint64_t full_state[2];    // TMA of a consumer's checkpoint landed
+    uint64_t empty_state[2];   // the consumer has copied it into registers
+    uint64_t full_tok[2][2];   // token vectors of an item are ready
+    uint64_t empty_tok[2][2];  // the consumer is done with them
+    ItemInfo info[2][2];
     int abort;
     int pad[3];
 };
@@ -214,15 +213,10 @@ __host__ __device__ inline int raw_buffer_bytes(int slots, int Q) {
            ((Q * 4 + 15) / 16) * 16;
 }
 
-// Shared-memory layout of a launch (window Q, whether the verify folds):
-// per pipeline a 64 KiB checkpoint staging buffer, ntok token-vector buffers,
-// nraw raw buffers and a work list; then the barriers.  Double buffers are
-// used when they fit.
+// Shared-memory layout of a launch (window Q, whether the verify folds).
 struct Layout {
-    int slots, ntok, nraw, tok_bytes, raw_bytes;
-    int off_state, off_tok, off_raw, off_list, off_shared, total;
-    __host__ __device__ int tok(int c, int b) const { return off_tok + (c * ntok + b) * tok_bytes; }
-    __host__ __device__ int raw(int c, int b) const { return off_raw + (c * nraw + b) * raw_bytes; }
+    int slots, nbuf, tok_bytes, raw_bytes;
+    int off_state, off_tok, off_raw, off_list, off_sync, total;
 };
 
 __host__ __device__ inline Layout make_layout(int Q, bool fold) {
@@ -230,76 +224,62 @@ __host__ __device__ inline Layout make_layout(int Q, bool fold) {
     l.slots = fold ? 2 * Q : Q;
     l.tok_bytes = tok_buffer_bytes(l.slots, Q);
     l.raw_bytes = raw_buffer_bytes(l.slots, Q);
-    const int fixed = kPipes * kD * kD * 4 + kPipes * (int)sizeof(WorkList) + (int)sizeof(Shared);
-    const int options[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
-    int pick = 3;
-    for (int i = 0; i < 4; ++i) {
-        if (fixed + kPipes * (options[i][0] * l.tok_bytes + options[i][1] * l.raw_bytes) <=
-            kSmemBudget) {
-            pick = i;
-            break;
-        }
-    }
-    l.ntok = options[pick][0];
-    l.nraw = options[pick][1];
-    l.off_state = 0;
-    l.off_tok = kPipes * kD * kD * 4;
-    l.off_raw = l.off_tok + kPipes * l.ntok * l.tok_bytes;
-    l.off_list = l.off_raw + kPipes * l.nraw * l.raw_bytes;
-    l.off_shared = l.off_list + kPipes * (int)sizeof(WorkList);
-    l.total = l.off_shared + (int)sizeof(Shared);
+    l.off_state = 0;                                // 2 x 64 KiB staging
+    l.off_tok = 2 * kD * kD * 4;
+    const int fixed = l.off_tok + 2 * l.raw_bytes + (int)sizeof(WorkList) + (int)sizeof(Sync);
+    l.nbuf = fixed + 4 * l.tok_bytes <= kSmemBudget ? 2 : 1;
+    l.off_raw = l.off_tok + 2 * l.nbuf * l.tok_bytes;
+    l.off_list = l.off_raw + 2 * l.raw_bytes;
+    l.off_sync = l.off_list + (int)sizeof(WorkList);
+    l.total = l.off_sync + (int)sizeof(Sync);
     return l;
 }
 
 // Bounded wait shared by all roles: gives up on timeout or when another
 // role has given up.
-__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Shared &sh,
+__device__ __forceinline__ bool wait_phase(uint64_t *bar, uint32_t parity, Sync &sy,
                                            const Params &p) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*reinterpret_cast<volatile int *>(&sh.abort)) return false;
+        if (*reinterpret_cast<volatile int *>(&sy.abort)) return false;
         if (clock64() - t0 > kWaitBudget) {
-            *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+            *reinterpret_cast<volatile int *>(&sy.abort) = 1;
             flag_error(p.err, kErrWaitTimeout);
             return false;
         }
     }
 }
 
-// Named barrier of one producer warpgroup (ids 1, 2; 0 is __syncthreads).
-__device__ __forceinline__ void producer_sync(int c) {
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + c), "n"(kGroupThreads) : "memory");
+__device__ __forceinline__ void producer_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(kProducerBarrier), "n"(kProducerThreads) : "memory");
 }
 
-// Candidate k of pipeline c is tile blockIdx.x + (kPipes * k + c) * gridDim.x.
-__device__ __forceinline__ int num_candidates(int num_tiles, int c) {
-    const int first = (int)blockIdx.x + c * (int)gridDim.x;
-    const int step = kPipes * (int)gridDim.x;
-    return first < num_tiles ? (num_tiles - first + step - 1) / step : 0;
+__device__ __forceinline__ int num_candidates(int num_tiles) {
+    const int first = (int)blockIdx.x;
+    return first < num_tiles ? (num_tiles - first + (int)gridDim.x - 1) / (int)gridDim.x : 0;
 }
 
 // One planning round over candidates [k0, k0 + kPlanSize) by the producer
 // threads; compacts the tiles with work, in order, into the list.
 template <Mode kMode>
-__device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles, int c, int pt) {
-    const int K = num_candidates(num_tiles, c);
+__device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles, int pt) {
+    const int K = num_candidates(num_tiles);
     Work w;
     bool has = false;
     const int k = k0 + pt;
-    if (k < K)
-        has = plan_tile<kMode>(p, (int)blockIdx.x + (kPipes * k + c) * (int)gridDim.x, w);
+    if (k < K) has = plan_tile<kMode>(p, (int)blockIdx.x + k * (int)gridDim.x, w);
     const unsigned ballot = __ballot_sync(kFull, has);
     const int lane = pt & 31, warp = pt >> 5;
     if (lane == 0) list.warp_count[warp] = __popc(ballot);
-    producer_sync(c);
+    producer_sync();
     int before = 0, total = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int n = list.warp_count[i];
-        if (i < warp) before += n;
-        total += n;
+    for (int i = 0; i < kProducerWarps; ++i) {
+        const int c = list.warp_count[i];
+        if (i < warp) before += c;
+        total += c;
     }
     if (has) {
         const int pos = before + __popc(ballot & ((1u << lane) - 1u));
@@ -309,7 +289,7 @@ __device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles
         list.bos[pos] = w.bos;
         list.tp[pos] = w.T | (w.p << 8);
     }
-    producer_sync(c);
+    producer_sync();
     return total;
 }
 
@@ -317,21 +297,21 @@ struct Cursor {
     int idx, count, next_k;
 };
 
-// The pipeline's next work item (planning a new round when needed), or a
-// Work with tile -1 when there is no more.
+// The producer's next work item (planning a new round when needed), or a
+// Work with tile -1 when the CTA has no more.
 template <Mode kMode>
-__device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Cursor &cu,
-                                          int num_tiles, int c, int pt) {
-    const int K = num_candidates(num_tiles, c);
+__device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Cursor &c,
+                                          int num_tiles, int pt) {
+    const int K = num_candidates(num_tiles);
     Work w;
     w.tile = -1;
-    while (cu.idx >= cu.count) {
-        if (cu.next_k >= K) return w;
-        cu.count = plan_round<kMode>(p, list, cu.next_k, num_tiles, c, pt);
-        cu.next_k += kPlanSize;
-        cu.idx = 0;
+    while (c.idx >= c.count) {
+        if (c.next_k >= K) return w;
+        c.count = plan_round<kMode>(p, list, c.next_k, num_tiles, pt);
+        c.next_k += kPlanSize;
+        c.idx = 0;
     }
-    const int i = cu.idx++;
+    const int i = c.idx++;
     w.tile = list.tile[i];
     w.head = w.tile % p.H;
     w.slot = list.slot[i];
@@ -343,13 +323,12 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
 }
 
 // Raw inputs and gate parameters of an item into a raw buffer (cp.async by
-// the producer threads), plus the new tokens' beta_raw into a register.
+// the producer threads).
 template <Mode kMode>
-__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, int pt,
-                                          uint32_t &beta_reg) {
+__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, int pt) {
     const int lane = pt & 31, warp = pt >> 5;
     const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int c = warp; c < 3 * w.p; c += 4) {
+    for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
         const int u = c / 3;
         const int part = c - 3 * u;
         const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
@@ -357,12 +336,12 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
         cp_async8(dst + 2 * lane, src + lane);
     }
     if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
-    if (warp == 3) {
+    if (warp == kProducerWarps - 1) {
         cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
         if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
     }
     if constexpr (kMode == Mode::kVerify) {
-        for (int c = warp; c < 4 * w.T; c += 4) {
+        for (int c = warp; c < 4 * w.T; c += kProducerWarps) {
             const int t = c >> 2;
             const int part = c & 3;
             const size_t tok = (size_t)(w.bos + t);
@@ -383,15 +362,12 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
             }
             cp_async8(dst + 2 * lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
         }
-        if (pt < w.T)
-            beta_reg = reinterpret_cast<const uint16_t *>(
-                p.beta)[(size_t)(w.bos + pt) * p.stride_beta + w.head];
     }
     cp_async_commit();
 }
 
 // Per-token vectors of an item: token u is prepared by producer warp
-// (u mod 4), four channels per lane, the norms summed across the warp; every
+// (u mod 2), four channels per lane, the norms summed across the warp; every
 // token is computed the same way however many tokens the item has.  The
 // verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
@@ -399,8 +375,9 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
                                           int pt) {
     const int lane = pt & 31, warp = pt >> 5;
     const float a = expf(*rv.a_log);
+    const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
     __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int u = warp; u < w.p + w.T; u += 4) {
+    for (int u = warp; u < w.p + w.T; u += kProducerWarps) {
         const bool is_new = kMode == Mode::kVerify && u >= w.p;
         const int t = u - w.p;
         const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
@@ -416,15 +393,13 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
         *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) =
             make_float4(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik), __fmul_rn(k.z, ik),
                         __fmul_rn(k.w, ik));
-        // the gate, one channel at a time (keeps the producer's registers low)
-        const uint32_t gw[2] = {gb.x, gb.y};
-        float *e_out = tv.e + u * kD + 4 * lane;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-            const uint32_t bits = ch & 1 ? (gw[ch >> 1] & 0xffff0000u) : (gw[ch >> 1] << 16);
-            e_out[ch] = decay_factor(__fadd_rn(__uint_as_float(bits), rv.bias[4 * lane + ch]), a,
-                                     kBounded, p.lower_bound);
-        }
+        const float4 g = bf16x4_to_float4(gb);
+        float4 e;
+        e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
+        e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
+        e.z = decay_factor(__fadd_rn(g.z, bias.z), a, kBounded, p.lower_bound);
+        e.w = decay_factor(__fadd_rn(g.w, bias.w), a, kBounded, p.lower_bound);
+        *reinterpret_cast<float4 *>(tv.e + u * kD + 4 * lane) = e;
         *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
         if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
         if (is_new) {
@@ -459,43 +434,53 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
 
 template <Mode kMode, bool kBounded>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
-                             int num_tiles, int c, int pt) {
-    Shared &sh = *reinterpret_cast<Shared *>(smem + lay.off_shared);
-    Sync &sy = sh.pipe[c];
-    WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list + c * (int)sizeof(WorkList));
-    float *staging = reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD;
+                             int num_tiles, int pt) {
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
+    WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
     Cursor cursor{0, 0, 0};
-    Work cur = next_work<kMode>(p, list, cursor, num_tiles, c, pt);
+    Work cur = next_work<kMode>(p, list, cursor, num_tiles, pt);
     int rb = 0;
     uint32_t beta_next = 0;
-    if (cur.tile >= 0) fetch_raw<kMode>(p, cur, RawView(smem + lay.raw(c, 0), lay.slots, p.Q), pt, beta_next);
+    if (cur.tile >= 0) {
+        fetch_raw<kMode>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q), pt);
+        if (kMode == Mode::kVerify && pt < cur.T)
+            beta_next = reinterpret_cast<const uint16_t *>(
+                p.beta)[(size_t)(cur.bos + pt) * p.stride_beta + cur.head];
+    }
     int n = 0;
     bool ok = true;
     while (cur.tile >= 0) {
-        // checkpoint of `cur` into the consumer's staging buffer
+        const int c = n & 1;
+        const int use_c = n >> 1;
+        // checkpoint of `cur` into consumer c's staging buffer
         if (pt == 0) {
-            if (n > 0) ok = wait_phase(&sy.empty_state, (n - 1) & 1, sh, p);
-            if (ok) issue_state(p, cur, staging, &sy.full_state);
+            if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
+            if (ok)
+                issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
+                            &sy.full_state[c]);
         }
-        // raw inputs of `cur` have landed; plan the next item and, with a
-        // second raw buffer, start its copies now
-        RawView rv(smem + lay.raw(c, rb), lay.slots, p.Q);
+        // raw inputs of `cur` have landed; start those of the next item
+        RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
         cp_async_wait_all();
         if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new[pt] = beta_next;
-        const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, c, pt);  // has barriers
-        if (lay.nraw == 2 && nxt.tile >= 0)
-            fetch_raw<kMode>(p, nxt, RawView(smem + lay.raw(c, rb ^ 1), lay.slots, p.Q), pt,
-                             beta_next);
-        // token vectors of `cur` into buffer b, once the consumer freed it
-        const int b = n % lay.ntok;
-        const int use_b = n / lay.ntok;
-        if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[b], (use_b - 1) & 1, sh, p);
-        producer_sync(c);
-        if (*reinterpret_cast<volatile int *>(&sh.abort)) return;
-        const TokView tv(smem + lay.tok(c, b), lay.slots, p.Q);
+        const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
+        if (nxt.tile >= 0) {
+            fetch_raw<kMode>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
+                                             lay.slots, p.Q), pt);
+            if (kMode == Mode::kVerify && pt < nxt.T)
+                beta_next = reinterpret_cast<const uint16_t *>(
+                    p.beta)[(size_t)(nxt.bos + pt) * p.stride_beta + nxt.head];
+        }
+        // token vectors of `cur` into consumer c's buffer b, once it is free
+        const int b = use_c % lay.nbuf;
+        const int use_b = use_c / lay.nbuf;
+        if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
+        producer_sync();
+        if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
+        TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
         if (pt == 0) {
-            ItemInfo &it = sy.info[b];
+            ItemInfo &it = sy.info[c][b];
             it.tile = cur.tile;
             it.slot = cur.slot;
             it.head = cur.head;
@@ -504,29 +489,29 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             it.p = cur.p;
             it.end = 0;
         }
-        producer_sync(c);  // token vectors and item info written, raw buffer read
-        if (pt == 0) mbar_arrive(&sy.full_tok[b]);
-        if (lay.nraw == 1 && nxt.tile >= 0)
-            fetch_raw<kMode>(p, nxt, RawView(smem + lay.raw(c, 0), lay.slots, p.Q), pt, beta_next);
+        producer_sync();  // all token vectors and the item info written
+        if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
         ++n;
-        if (lay.nraw == 2) rb ^= 1;
+        rb ^= 1;
         cur = nxt;
     }
-    // end marker: the consumer's next buffer says "no more items"
+    // end markers: the next buffer of each consumer says "no more items"
     if (pt == 0) {
-        const int b = n % lay.ntok;
-        const int use_b = n / lay.ntok;
-        if (use_b > 0 && !wait_phase(&sy.empty_tok[b], (use_b - 1) & 1, sh, p)) return;
-        sy.info[b].end = 1;
-        mbar_arrive(&sy.full_tok[b]);
+        for (int c = 0; c < 2; ++c) {
+            const int use_c = (n + 1 - c) >> 1;
+            const int b = use_c % lay.nbuf;
+            const int use_b = use_c / lay.nbuf;
+            if (use_b > 0 && !wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p)) return;
+            sy.info[c][b].end = 1;
+            mbar_arrive(&sy.full_tok[c][b]);
+        }
     }
 }
 
 template <Mode kMode>
 __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout &lay, int c,
                              int ct) {
-    Shared &sh = *reinterpret_cast<Shared *>(smem + lay.off_shared);
-    Sync &sy = sh.pipe[c];
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     Lane L;
     L.lane = ct & 31;
     L.w = ct >> 5;
@@ -534,16 +519,16 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     L.j = L.lane & 7;
     const float *staging = reinterpret_cast<const float *>(smem + lay.off_state) + c * kD * kD;
     for (int k = 0;; ++k) {
-        const int b = k % lay.ntok;
-        const int use_b = k / lay.ntok;
-        if (!wait_phase(&sy.full_tok[b], use_b & 1, sh, p)) return;
-        const ItemInfo it = sy.info[b];
+        const int b = k % lay.nbuf;
+        const int use_b = k / lay.nbuf;
+        if (!wait_phase(&sy.full_tok[c][b], use_b & 1, sy, p)) return;
+        const ItemInfo it = sy.info[c][b];
         if (it.end) return;
-        if (!wait_phase(&sy.full_state, k & 1, sh, p)) return;
+        if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
         Tile h;
         load_tile(h, staging, L);
-        mbar_arrive(&sy.empty_state);
-        const TokView tv(smem + lay.tok(c, b), lay.slots, p.Q);
+        mbar_arrive(&sy.empty_state[c]);
+        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         float *tile = p.pool + ((size_t)it.slot * p.H + it.head) * (size_t)(kD * kD);
         for (int u = 0; u < it.p; ++u) token_plain(h, tv, u, L);
         if (it.p > 0) store_tile(h, tile, L);
@@ -554,7 +539,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
                 if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
             }
         }
-        mbar_arrive(&sy.empty_tok[b]);
+        mbar_arrive(&sy.empty_tok[c][b]);
     }
 }
 
@@ -563,33 +548,30 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
                                                                   int fold) {
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout lay = make_layout(p.Q, fold != 0);
-    Shared &sh = *reinterpret_cast<Shared *>(smem + lay.off_shared);
+    Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     const int tid = threadIdx.x;
     if (tid == 0) {
-        for (int c = 0; c < kPipes; ++c) {
-            Sync &sy = sh.pipe[c];
-            mbar_init(&sy.full_state, 1);
-            mbar_init(&sy.empty_state, kGroupThreads);
+        for (int c = 0; c < 2; ++c) {
+            mbar_init(&sy.full_state[c], 1);
+            mbar_init(&sy.empty_state[c], kConsumerThreads);
             for (int b = 0; b < 2; ++b) {
-                mbar_init(&sy.full_tok[b], 1);
-                mbar_init(&sy.empty_tok[b], kGroupThreads);
+                mbar_init(&sy.full_tok[c][b], 1);
+                mbar_init(&sy.empty_tok[c][b], kConsumerThreads);
             }
         }
-        sh.abort = 0;
+        sy.abort = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    // Register split: every thread is launched with kLaunchRegs; the producer
-    // warpgroups hand registers back and the consumer warpgroups take them
-    // (kPipes * 128 * (kConsumerRegs + kProducerRegs) == 512 * kLaunchRegs).
-    const int group = tid / kGroupThreads;   // 0, 1: consumers; 2, 3: producers
-    if (group < kPipes) {
+    // Register split: the launch gives every thread kLaunchRegs; the producer
+    // warpgroup hands registers back and the consumers take them, so that
+    // 2 * 128 * kConsumerRegs + 128 * kProducerRegs == 384 * kLaunchRegs.
+    if (tid < 2 * kConsumerThreads) {
         reg_alloc<kConsumerRegs>();
-        run_consumer<kMode>(p, smem, lay, group, tid % kGroupThreads);
+        run_consumer<kMode>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
     } else {
         reg_dealloc<kProducerRegs>();
-        run_producer<kMode, kBounded>(p, smem, lay, num_tiles, group - kPipes,
-                                      tid % kGroupThreads);
+        run_producer<kMode, kBounded>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
     }
 }
 
