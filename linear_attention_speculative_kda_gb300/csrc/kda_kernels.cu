@@ -184,36 +184,33 @@ struct Sync {
     uint64_t empty_state[2];   // the consumer has copied it into registers
     uint64_t full_tok[2][2];   // token vectors of an item are ready
     uint64_t empty_tok[2][2];  // the consumer is done with them
-    uint64_t raw_full[2];      // bulk copies of a raw buffer landed
     ItemInfo info[2][2];
     int abort;
     int pad[3];
 };
 
-// Raw bf16 inputs of one item.  Token slot u holds a 784-byte record image
-// [k | v | g_raw | tail]: folded tokens are copied whole from the records,
-// new tokens get k, v and g_raw from the activations (tail unused).  Then
-// q of the new tokens, the head's g_bias, and the new tokens' beta_raw bits.
-constexpr int kSlotBytes = kRecStride * 2;   // 784
-
+// Raw bf16 inputs and gate parameters of one item, in channel pairs.
 struct RawView {
-    unsigned char *base;
-    int slots, Q;
-    __device__ __forceinline__ RawView(unsigned char *b, int s, int q) : base(b), slots(s), Q(q) {}
-    __device__ __forceinline__ unsigned char *slot(int u) const { return base + u * kSlotBytes; }
-    __device__ __forceinline__ unsigned char *qrow(int t) const {
-        return base + slots * kSlotBytes + t * (kD * 2);
-    }
-    __device__ __forceinline__ float *bias() const {
-        return reinterpret_cast<float *>(base + slots * kSlotBytes + Q * (kD * 2));
-    }
-    __device__ __forceinline__ uint32_t *beta_new() const {
-        return reinterpret_cast<uint32_t *>(base + slots * kSlotBytes + Q * (kD * 2) + kD * 4);
+    uint32_t *k, *v, *g, *q;
+    uint2 *tail;                // record tails: beta_raw bits in the low half
+    float *bias;                // g_bias of the item's head (128)
+    float *a_log;
+    uint32_t *beta_new;         // beta_raw bits of the new tokens
+    __device__ __forceinline__ RawView(unsigned char *base, int slots, int Q) {
+        k = reinterpret_cast<uint32_t *>(base);
+        v = k + slots * (kD / 2);
+        g = v + slots * (kD / 2);
+        q = g + slots * (kD / 2);
+        tail = reinterpret_cast<uint2 *>(q + Q * (kD / 2));
+        bias = reinterpret_cast<float *>(tail + ((Q + 1) / 2) * 2);
+        a_log = bias + kD;
+        beta_new = reinterpret_cast<uint32_t *>(a_log + 4);
     }
 };
 
 __host__ __device__ inline int raw_buffer_bytes(int slots, int Q) {
-    return slots * kSlotBytes + Q * (kD * 2) + kD * 4 + ((Q * 4 + 15) / 16) * 16;
+    return slots * 3 * (kD * 2) + Q * (kD * 2) + ((Q + 1) / 2) * 16 + kD * 4 + 16 +
+           ((Q * 4 + 15) / 16) * 16;
 }
 
 // Shared-memory layout of a launch (window Q, whether the verify folds).
@@ -325,96 +322,68 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
     return w;
 }
 
-// Raw inputs of an item into a raw buffer, and the head's A_log and the new
-// tokens' beta_raw into registers.  kBulk: one producer thread issues TMA
-// bulk copies (whole record tokens, 256-byte activation rows, the g_bias
-// row) that complete on `bar`; otherwise every producer thread issues 8-byte
-// cp.async copies (activations that are only 8-byte aligned).
-template <Mode kMode, bool kBulk>
-__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, uint64_t *bar,
-                                          int pt, float &a_log, uint32_t &beta_reg) {
+// Raw inputs and gate parameters of an item into a raw buffer (cp.async by
+// the producer threads).
+template <Mode kMode>
+__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, int pt) {
     const int lane = pt & 31, warp = pt >> 5;
     const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    const size_t col = (size_t)w.head * kD;
-    if constexpr (kBulk) {
-        if (pt == 0) {
-            const uint32_t bytes =
-                w.p * kSlotBytes + (kMode == Mode::kVerify ? w.T * 4 * (kD * 2) : 0) + kD * 4;
-            mbar_arrive_expect_tx(bar, bytes);
-            for (int u = 0; u < w.p; ++u)
-                bulk_load(rv.slot(u), rec + (size_t)u * kRecStride, kSlotBytes, bar);
-            if constexpr (kMode == Mode::kVerify) {
-                for (int t = 0; t < w.T; ++t) {
-                    const size_t tok = (size_t)(w.bos + t);
-                    unsigned char *dst = rv.slot(w.p + t);
-                    bulk_load(dst, p.k + tok * p.stride_k + col, kD * 2, bar);
-                    bulk_load(dst + kD * 2, p.v + tok * p.stride_v + col, kD * 2, bar);
-                    bulk_load(dst + kD * 4, p.g + tok * p.stride_g + col, kD * 2, bar);
-                    bulk_load(rv.qrow(t), p.q + tok * p.stride_q + col, kD * 2, bar);
-                }
-            }
-            bulk_load(rv.bias(), p.g_bias + col, kD * 4, bar);
-        }
-    } else {
-        for (int c = warp; c < 4 * w.p; c += kProducerWarps) {   // 4 parts: k, v, g, tail
-            const int u = c >> 2;
-            const int part = c & 3;
-            const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
-            uint2 *dst = reinterpret_cast<uint2 *>(rv.slot(u) + part * (kD * 2));
-            if (part < 3 || lane < 2) cp_async8(dst + lane, src + lane);
-        }
-        if constexpr (kMode == Mode::kVerify) {
-            for (int c = warp; c < 4 * w.T; c += kProducerWarps) {
-                const int t = c >> 2;
-                const int part = c & 3;
-                const size_t tok = (size_t)(w.bos + t);
-                const __nv_bfloat16 *src;
-                unsigned char *dst;
-                if (part == 0) {
-                    src = p.k + tok * p.stride_k;
-                    dst = rv.slot(w.p + t);
-                } else if (part == 1) {
-                    src = p.v + tok * p.stride_v;
-                    dst = rv.slot(w.p + t) + kD * 2;
-                } else if (part == 2) {
-                    src = p.g + tok * p.stride_g;
-                    dst = rv.slot(w.p + t) + kD * 4;
-                } else {
-                    src = p.q + tok * p.stride_q;
-                    dst = rv.qrow(t);
-                }
-                cp_async8(reinterpret_cast<uint2 *>(dst) + lane,
-                          reinterpret_cast<const uint2 *>(src + col) + lane);
-            }
-        }
-        if (warp == kProducerWarps - 1) cp_async16(rv.bias() + 4 * lane, p.g_bias + col + 4 * lane);
-        cp_async_commit();
+    for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
+        const int u = c / 3;
+        const int part = c - 3 * u;
+        const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
+        uint32_t *dst = (part == 0 ? rv.k : (part == 1 ? rv.v : rv.g)) + u * (kD / 2);
+        cp_async8(dst + 2 * lane, src + lane);
     }
-    a_log = p.A_log[w.head];
-    if (kMode == Mode::kVerify && pt < w.T)
-        beta_reg = reinterpret_cast<const uint16_t *>(p.beta)[(size_t)(w.bos + pt) * p.stride_beta + w.head];
+    if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
+    if (warp == kProducerWarps - 1) {
+        cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
+        if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
+    }
+    if constexpr (kMode == Mode::kVerify) {
+        for (int c = warp; c < 4 * w.T; c += kProducerWarps) {
+            const int t = c >> 2;
+            const int part = c & 3;
+            const size_t tok = (size_t)(w.bos + t);
+            const __nv_bfloat16 *src;
+            uint32_t *dst;
+            if (part == 0) {
+                src = p.k + tok * p.stride_k;
+                dst = rv.k + (w.p + t) * (kD / 2);
+            } else if (part == 1) {
+                src = p.v + tok * p.stride_v;
+                dst = rv.v + (w.p + t) * (kD / 2);
+            } else if (part == 2) {
+                src = p.g + tok * p.stride_g;
+                dst = rv.g + (w.p + t) * (kD / 2);
+            } else {
+                src = p.q + tok * p.stride_q;
+                dst = rv.q + t * (kD / 2);
+            }
+            cp_async8(dst + 2 * lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
+        }
+    }
+    cp_async_commit();
 }
 
 // Per-token vectors of an item: token u is prepared by producer warp
-// (u mod 4), four channels per lane, the norms summed across the warp; every
+// (u mod 2), four channels per lane, the norms summed across the warp; every
 // token is computed the same way however many tokens the item has.  The
 // verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
 __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView rv, TokView tv,
-                                          float a_log, int pt) {
+                                          int pt) {
     const int lane = pt & 31, warp = pt >> 5;
-    const float a = expf(a_log);
-    const float4 bias = *reinterpret_cast<const float4 *>(rv.bias() + 4 * lane);
+    const float a = expf(*rv.a_log);
+    const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
     __nv_bfloat16 *rec = record_base(p, w.r, w.head);
     for (int u = warp; u < w.p + w.T; u += kProducerWarps) {
         const bool is_new = kMode == Mode::kVerify && u >= w.p;
         const int t = u - w.p;
-        const uint2 *sl = reinterpret_cast<const uint2 *>(rv.slot(u));
-        const uint2 kb = sl[lane];
-        const uint2 vb = sl[kRecV / 4 + lane];
-        const uint2 gb = sl[kRecG / 4 + lane];
-        const uint32_t bb = is_new ? rv.beta_new()[t]
-                                   : (uint32_t) reinterpret_cast<const uint16_t *>(sl)[kRecBeta];
+        const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
+        const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
+        const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
+        const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
         const float4 k = bf16x4_to_float4(kb);
         float s = __fmul_rn(k.x, k.x);
         s = __fmaf_rn(k.y, k.y, s);
@@ -434,7 +403,7 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
         *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
         if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
         if (is_new) {
-            const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.qrow(t))[lane]);
+            const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
             float sq = __fmul_rn(q.x, q.x);
             sq = __fmaf_rn(q.y, q.y, sq);
             sq = __fmaf_rn(q.z, q.z, sq);
@@ -463,7 +432,7 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
         bulk_load(dst + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, bar);
 }
 
-template <Mode kMode, bool kBounded, bool kBulk>
+template <Mode kMode, bool kBounded>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
                              int num_tiles, int pt) {
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
@@ -472,10 +441,12 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     Work cur = next_work<kMode>(p, list, cursor, num_tiles, pt);
     int rb = 0;
     uint32_t beta_next = 0;
-    float alog_next = 0.0f;
-    if (cur.tile >= 0)
-        fetch_raw<kMode, kBulk>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q),
-                                &sy.raw_full[0], pt, alog_next, beta_next);
+    if (cur.tile >= 0) {
+        fetch_raw<kMode>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q), pt);
+        if (kMode == Mode::kVerify && pt < cur.T)
+            beta_next = reinterpret_cast<const uint16_t *>(
+                p.beta)[(size_t)(cur.bos + pt) * p.stride_beta + cur.head];
+    }
     int n = 0;
     bool ok = true;
     while (cur.tile >= 0) {
@@ -488,24 +459,17 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
                 issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
                             &sy.full_state[c]);
         }
-        // raw inputs of `cur` have landed (bulk: the barrier; cp.async: each
-        // thread's own copies, published by the barrier below)
-        const RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
-        if constexpr (kBulk) {
-            if (pt == 0 && ok) ok = wait_phase(&sy.raw_full[rb], (n >> 1) & 1, sy, p);
-        } else {
-            cp_async_wait_all();
-        }
-        const float alog_cur = alog_next;
-        if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new()[pt] = beta_next;
-        // plan the next item and start its copies into the other raw buffer
-        // (its previous contents were consumed before the last barrier)
+        // raw inputs of `cur` have landed; start those of the next item
+        RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
+        cp_async_wait_all();
+        if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new[pt] = beta_next;
         const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
         if (nxt.tile >= 0) {
-            if (kBulk && pt == 0) fence_proxy_async_smem();
-            fetch_raw<kMode, kBulk>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
-                                                    lay.slots, p.Q),
-                                    &sy.raw_full[rb ^ 1], pt, alog_next, beta_next);
+            fetch_raw<kMode>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
+                                             lay.slots, p.Q), pt);
+            if (kMode == Mode::kVerify && pt < nxt.T)
+                beta_next = reinterpret_cast<const uint16_t *>(
+                    p.beta)[(size_t)(nxt.bos + pt) * p.stride_beta + nxt.head];
         }
         // token vectors of `cur` into consumer c's buffer b, once it is free
         const int b = use_c % lay.nbuf;
@@ -513,9 +477,8 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
         producer_sync();
         if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
-        if constexpr (kBulk) mbar_try_wait(&sy.raw_full[rb], (n >> 1) & 1);  // completed: acquire
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
-        prep_item<kMode, kBounded>(p, cur, rv, tv, alog_cur, pt);
+        prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
         if (pt == 0) {
             ItemInfo &it = sy.info[c][b];
             it.tile = cur.tile;
@@ -526,7 +489,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             it.p = cur.p;
             it.end = 0;
         }
-        producer_sync();  // all token vectors and the item info written, raw buffer read
+        producer_sync();  // all token vectors and the item info written
         if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
         ++n;
         rb ^= 1;
@@ -580,7 +543,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-template <Mode kMode, bool kBounded, bool kBulk>
+template <Mode kMode, bool kBounded>
 __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
                                                                   int fold) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -595,7 +558,6 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
                 mbar_init(&sy.full_tok[c][b], 1);
                 mbar_init(&sy.empty_tok[c][b], kConsumerThreads);
             }
-            mbar_init(&sy.raw_full[c], 1);
         }
         sy.abort = 0;
         fence_mbar_init();
@@ -609,7 +571,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
         run_consumer<kMode>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
     } else {
         reg_dealloc<kProducerRegs>();
-        run_producer<kMode, kBounded, kBulk>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
+        run_producer<kMode, kBounded>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
     }
 }
 
@@ -689,17 +651,14 @@ int sm_count() {
 // Launch the warp-specialized step kernel: one CTA per SM (or one per tile
 // when there are fewer tiles), the shared-memory layout sized by the window.
 template <kda::Mode M>
-kda_status launch_step(const Params &p, bool bounded, bool fold, bool bulk, cudaStream_t stream) {
+kda_status launch_step(const Params &p, bool bounded, bool fold, cudaStream_t stream) {
     const long long tiles = (long long)p.B * p.H;
     const int sms = sm_count();
     if (sms <= 0) return KDA_ERR_CUDA;
     const int grid = (int)(tiles < (long long)sms ? tiles : (long long)sms);
     const kda::Layout lay = kda::make_layout(p.Q, fold);
-    void (*kern)(const Params, int, int);
-    if (bulk)
-        kern = bounded ? kda::step_kernel<M, true, true> : kda::step_kernel<M, false, true>;
-    else
-        kern = bounded ? kda::step_kernel<M, true, false> : kda::step_kernel<M, false, false>;
+    void (*kern)(const Params, int, int) =
+        bounded ? kda::step_kernel<M, true> : kda::step_kernel<M, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -760,12 +719,7 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     p.traj = trajectory_out;
     p.err = error_word;
 
-    // Raw activation rows go by TMA bulk copy when every row starts on a
-    // 16-byte boundary, else by 8-byte cp.async.
-    const bool bulk = aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(g_raw, 16) &&
-                      cfg->stride_q_t % 8 == 0 && cfg->stride_k_t % 8 == 0 &&
-                      cfg->stride_v_t % 8 == 0 && cfg->stride_g_t % 8 == 0;
-    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0, pending != nullptr, bulk,
+    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0, pending != nullptr,
                                            static_cast<cudaStream_t>(stream));
 }
 
@@ -798,7 +752,7 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     p.eager = eager;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false, true,
+    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,
                                            static_cast<cudaStream_t>(stream));
 }
 
@@ -824,7 +778,7 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
     p.pending_in = pending;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0, false, true,
+    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0, false,
                                           static_cast<cudaStream_t>(stream));
 }
 

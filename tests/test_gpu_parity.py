@@ -276,35 +276,3 @@ def test_all_rows_idle_and_more_ctas_than_work():
     assert int(g.err.item()) == 0
     assert torch.equal(g.pool, g.pool0)
     assert (f64(g.out) == -9.0).all()
-
-
-def test_eight_byte_aligned_activations_match_sixteen():
-    """Activation rows that start on 8-byte (not 16-byte) boundaries take the
-    cp.async path instead of the bulk-copy path; results must be the same
-    bits."""
-    wl = W.custom(B=9, H=3, Q=8, lens=[8, 3, 0, 8, 5, 1, 8, 7, 2], S=12, seed=23)
-    ref = GpuRun(wl, with_traj=True)
-    ref.verify()
-    ref.commit()
-    g = GpuRun(wl, with_traj=True)
-    st = g.steps[0]
-    T, H, D = st["qkv"].shape[0], wl.spec.H, wl.spec.D
-    # token stride 3*H*D + 4 elements and a base 4 elements into the buffer
-    buf = torch.zeros((T, 3 * H * D + 4), dtype=torch.bfloat16, device="cuda")
-    flat = torch.zeros(buf.numel() + 4, dtype=torch.bfloat16, device="cuda")
-    view = flat[4:].view(T, 3 * H * D + 4)
-    view[:, : 3 * H * D] = st["qkv"].reshape(T, -1)
-    q = view[:, 0 * H * D:1 * H * D].view(T, H, D)
-    k = view[:, 1 * H * D:2 * H * D].view(T, H, D)
-    v = view[:, 2 * H * D:3 * H * D].view(T, H, D)
-    assert q.stride(0) % 8 == 4 and q.data_ptr() % 16 == 8
-    api.kda_verify(q, k, v, st["g_raw"], st["beta_buf"][:, :H], g.A_log, g.g_bias, g.pool, g.cu,
-                   g.slots, g.records, g.out, trajectory_out=g.traj, error_word=g.err, **g.kw())
-    g.commit()
-    torch.cuda.synchronize()
-    assert int(g.err.item()) == 0 and int(ref.err.item()) == 0
-    assert torch.equal(g.out, ref.out)
-    assert torch.equal(g.traj, ref.traj)
-    assert torch.equal(g.pool, ref.pool)
-    assert torch.equal(g.records, ref.records)
-    del buf
