@@ -147,8 +147,8 @@ constexpr int kPlanSize = kProducerThreads;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
-constexpr int kConsumerRegs = 200;
-constexpr int kProducerRegs = 104;
+constexpr int kConsumerRegs = 208;
+constexpr int kProducerRegs = 88;
 static_assert(2 * kConsumerThreads * kConsumerRegs + kProducerThreads * kProducerRegs <=
                   kBlockThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
@@ -215,37 +215,21 @@ __host__ __device__ inline int raw_buffer_bytes(int slots, int Q) {
 
 // Shared-memory layout of a launch (window Q, whether the verify folds).
 struct Layout {
-    int slots, nbuf, nset, tok_bytes, raw_bytes;
+    int slots, nbuf, tok_bytes, raw_bytes;
     int off_state, off_tok, off_raw, off_list, off_sync, total;
-    // raw buffer of item i (0, 1) of a pair in raw set `set`
-    __host__ __device__ int raw(int set, int i) const { return off_raw + (2 * set + i) * raw_bytes; }
-    __host__ __device__ int tok(int c, int b) const { return off_tok + (c * nbuf + b) * tok_bytes; }
 };
 
-// The producer works on pairs of items (one per consumer).  Per consumer a
-// 64 KiB staging buffer and nbuf token-vector buffers; nset sets of two raw
-// buffers.  Double buffers are used when they fit.
 __host__ __device__ inline Layout make_layout(int Q, bool fold) {
     Layout l;
     l.slots = fold ? 2 * Q : Q;
     l.tok_bytes = tok_buffer_bytes(l.slots, Q);
     l.raw_bytes = raw_buffer_bytes(l.slots, Q);
-    const int fixed = 2 * kD * kD * 4 + (int)sizeof(WorkList) + (int)sizeof(Sync);
-    const int options[4][2] = {{2, 2}, {2, 1}, {1, 2}, {1, 1}};
-    int pick = 3;
-    for (int i = 0; i < 4; ++i) {
-        if (fixed + 2 * options[i][0] * l.tok_bytes + 2 * options[i][1] * l.raw_bytes <=
-            kSmemBudget) {
-            pick = i;
-            break;
-        }
-    }
-    l.nbuf = options[pick][0];
-    l.nset = options[pick][1];
     l.off_state = 0;                                // 2 x 64 KiB staging
     l.off_tok = 2 * kD * kD * 4;
+    const int fixed = l.off_tok + 2 * l.raw_bytes + (int)sizeof(WorkList) + (int)sizeof(Sync);
+    l.nbuf = fixed + 4 * l.tok_bytes <= kSmemBudget ? 2 : 1;
     l.off_raw = l.off_tok + 2 * l.nbuf * l.tok_bytes;
-    l.off_list = l.off_raw + 2 * l.nset * l.raw_bytes;
+    l.off_list = l.off_raw + 2 * l.raw_bytes;
     l.off_sync = l.off_list + (int)sizeof(WorkList);
     l.total = l.off_sync + (int)sizeof(Sync);
     return l;
@@ -382,82 +366,59 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
     cp_async_commit();
 }
 
-// Per-token vectors: token u of item w, four channels per lane of one
-// producer warp, the norms summed across the warp; every token is computed
-// the same way whichever warp prepares it and however many tokens the item
-// has.  The verify also writes the new tokens' raw records.
+// Per-token vectors of an item: token u is prepared by producer warp
+// (u mod 2), four channels per lane, the norms summed across the warp; every
+// token is computed the same way however many tokens the item has.  The
+// verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
-__device__ __forceinline__ void prep_token(const Params &p, const Work &w, const RawView &rv,
-                                           const TokView &tv, int u, float a, float4 bias,
-                                           int lane) {
-    const bool is_new = kMode == Mode::kVerify && u >= w.p;
-    const int t = u - w.p;
-    const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
-    const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
-    const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
-    const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
-    const float4 k = bf16x4_to_float4(kb);
-    float s = __fmul_rn(k.x, k.x);
-    s = __fmaf_rn(k.y, k.y, s);
-    s = __fmaf_rn(k.z, k.z, s);
-    s = __fmaf_rn(k.w, k.w, s);
-    const float ik = inv_l2(warp_allsum(s));
-    *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) =
-        make_float4(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik), __fmul_rn(k.z, ik), __fmul_rn(k.w, ik));
-    const float4 g = bf16x4_to_float4(gb);
-    float4 e;
-    e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
-    e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
-    e.z = decay_factor(__fadd_rn(g.z, bias.z), a, kBounded, p.lower_bound);
-    e.w = decay_factor(__fadd_rn(g.w, bias.w), a, kBounded, p.lower_bound);
-    *reinterpret_cast<float4 *>(tv.e + u * kD + 4 * lane) = e;
-    *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
-    if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
-    if (is_new) {
-        const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
-        float sq = __fmul_rn(q.x, q.x);
-        sq = __fmaf_rn(q.y, q.y, sq);
-        sq = __fmaf_rn(q.z, q.z, sq);
-        sq = __fmaf_rn(q.w, q.w, sq);
-        const float iq = inv_l2(warp_allsum(sq));
-        *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
-            make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale), __fmul_rn(__fmul_rn(q.y, iq), p.scale),
-                        __fmul_rn(__fmul_rn(q.z, iq), p.scale), __fmul_rn(__fmul_rn(q.w, iq), p.scale));
-        __nv_bfloat16 *rec = record_base(p, w.r, w.head) + (size_t)t * kRecStride;
-        uint2 *dst = reinterpret_cast<uint2 *>(rec);
-        dst[lane] = kb;
-        dst[kRecV / 4 + lane] = vb;
-        dst[kRecG / 4 + lane] = gb;
-        if (lane == 0) reinterpret_cast<uint16_t *>(rec)[kRecBeta] = (uint16_t)bb;
-    }
-}
-
-// Token vectors of a pair of items (item 1 may be absent): the tokens of both
-// are spread over the four producer warps, two at a time per warp so their
-// latency chains overlap.
-template <Mode kMode, bool kBounded>
-__device__ __forceinline__ void prep_pair(const Params &p, const Work &w0, const RawView &rv0,
-                                          const TokView &tv0, const Work &w1, const RawView &rv1,
-                                          const TokView &tv1, int pt) {
+__device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView rv, TokView tv,
+                                          int pt) {
     const int lane = pt & 31, warp = pt >> 5;
-    const int n0 = w0.p + w0.T;
-    const int total = n0 + (w1.tile >= 0 ? w1.p + w1.T : 0);
-    const float a0 = expf(*rv0.a_log);
-    const float4 b0 = *reinterpret_cast<const float4 *>(rv0.bias + 4 * lane);
-    float a1 = 0.0f;
-    float4 b1 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (w1.tile >= 0) {
-        a1 = expf(*rv1.a_log);
-        b1 = *reinterpret_cast<const float4 *>(rv1.bias + 4 * lane);
-    }
-    for (int x = warp; x < total; x += 2 * kProducerWarps) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int idx = x + h * kProducerWarps;
-            if (idx < n0)
-                prep_token<kMode, kBounded>(p, w0, rv0, tv0, idx, a0, b0, lane);
-            else if (idx < total)
-                prep_token<kMode, kBounded>(p, w1, rv1, tv1, idx - n0, a1, b1, lane);
+    const float a = expf(*rv.a_log);
+    const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
+    __nv_bfloat16 *rec = record_base(p, w.r, w.head);
+    for (int u = warp; u < w.p + w.T; u += kProducerWarps) {
+        const bool is_new = kMode == Mode::kVerify && u >= w.p;
+        const int t = u - w.p;
+        const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
+        const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
+        const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
+        const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
+        const float4 k = bf16x4_to_float4(kb);
+        float s = __fmul_rn(k.x, k.x);
+        s = __fmaf_rn(k.y, k.y, s);
+        s = __fmaf_rn(k.z, k.z, s);
+        s = __fmaf_rn(k.w, k.w, s);
+        const float ik = inv_l2(warp_allsum(s));
+        *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) =
+            make_float4(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik), __fmul_rn(k.z, ik),
+                        __fmul_rn(k.w, ik));
+        const float4 g = bf16x4_to_float4(gb);
+        float4 e;
+        e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
+        e.y = decay_factor(__fadd_rn(g.y, bias.y), a, kBounded, p.lower_bound);
+        e.z = decay_factor(__fadd_rn(g.z, bias.z), a, kBounded, p.lower_bound);
+        e.w = decay_factor(__fadd_rn(g.w, bias.w), a, kBounded, p.lower_bound);
+        *reinterpret_cast<float4 *>(tv.e + u * kD + 4 * lane) = e;
+        *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
+        if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+        if (is_new) {
+            const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
+            float sq = __fmul_rn(q.x, q.x);
+            sq = __fmaf_rn(q.y, q.y, sq);
+            sq = __fmaf_rn(q.z, q.z, sq);
+            sq = __fmaf_rn(q.w, q.w, sq);
+            const float iq = inv_l2(warp_allsum(sq));
+            *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
+                make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.y, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.z, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.w, iq), p.scale));
+            uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
+            dst[lane] = kb;
+            dst[kRecV / 4 + lane] = vb;
+            dst[kRecG / 4 + lane] = gb;
+            if (lane == 0) reinterpret_cast<uint16_t *>(rec + (size_t)t * kRecStride)[kRecBeta] = (uint16_t)bb;
         }
     }
 }
@@ -471,124 +432,75 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
         bulk_load(dst + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, bar);
 }
 
-__device__ __forceinline__ uint32_t load_beta(const Params &p, const Work &w, int pt) {
-    return reinterpret_cast<const uint16_t *>(p.beta)[(size_t)(w.bos + pt) * p.stride_beta + w.head];
-}
-
-__device__ __forceinline__ void write_info(ItemInfo &it, const Work &w) {
-    it.tile = w.tile;
-    it.slot = w.slot;
-    it.head = w.head;
-    it.bos = w.bos;
-    it.T = w.T;
-    it.p = w.p;
-    it.end = 0;
-}
-
-// The producer walks its items in pairs: item 2j goes to consumer 0 and item
-// 2j + 1 to consumer 1.
 template <Mode kMode, bool kBounded>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
                              int num_tiles, int pt) {
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
-    constexpr bool kVerify = kMode == Mode::kVerify;
     Cursor cursor{0, 0, 0};
-    Work w0 = next_work<kMode>(p, list, cursor, num_tiles, pt);
-    Work w1;
-    w1.tile = -1;
-    if (w0.tile >= 0) w1 = next_work<kMode>(p, list, cursor, num_tiles, pt);
-    uint32_t beta0 = 0, beta1 = 0;
-    if (w0.tile >= 0) {
-        fetch_raw<kMode>(p, w0, RawView(smem + lay.raw(0, 0), lay.slots, p.Q), pt);
-        if (kVerify && pt < w0.T) beta0 = load_beta(p, w0, pt);
+    Work cur = next_work<kMode>(p, list, cursor, num_tiles, pt);
+    int rb = 0;
+    uint32_t beta_next = 0;
+    if (cur.tile >= 0) {
+        fetch_raw<kMode>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q), pt);
+        if (kMode == Mode::kVerify && pt < cur.T)
+            beta_next = reinterpret_cast<const uint16_t *>(
+                p.beta)[(size_t)(cur.bos + pt) * p.stride_beta + cur.head];
     }
-    if (w1.tile >= 0) {
-        fetch_raw<kMode>(p, w1, RawView(smem + lay.raw(0, 1), lay.slots, p.Q), pt);
-        if (kVerify && pt < w1.T) beta1 = load_beta(p, w1, pt);
-    }
-    int set = 0;
-    int j = 0;           // pairs handed out
-    int got1 = 0;        // items handed to consumer 1
+    int n = 0;
     bool ok = true;
-    float *staging = reinterpret_cast<float *>(smem + lay.off_state);
-    while (w0.tile >= 0) {
-        // checkpoints of the pair into the consumers' staging buffers
+    while (cur.tile >= 0) {
+        const int c = n & 1;
+        const int use_c = n >> 1;
+        // checkpoint of `cur` into consumer c's staging buffer
         if (pt == 0) {
-            if (j > 0) ok = wait_phase(&sy.empty_state[0], (j - 1) & 1, sy, p);
-            if (ok) issue_state(p, w0, staging, &sy.full_state[0]);
-            if (w1.tile >= 0 && ok) {
-                if (got1 > 0) ok = wait_phase(&sy.empty_state[1], (got1 - 1) & 1, sy, p);
-                if (ok) issue_state(p, w1, staging + kD * kD, &sy.full_state[1]);
-            }
+            if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
+            if (ok)
+                issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
+                            &sy.full_state[c]);
         }
-        // raw inputs of the pair have landed (each thread's own copies,
-        // published by the barrier below)
-        const RawView rv0(smem + lay.raw(set, 0), lay.slots, p.Q);
-        const RawView rv1(smem + lay.raw(set, 1), lay.slots, p.Q);
+        // raw inputs of `cur` have landed; start those of the next item
+        RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
         cp_async_wait_all();
-        if (kVerify && pt < w0.T) rv0.beta_new[pt] = beta0;
-        if (kVerify && w1.tile >= 0 && pt < w1.T) rv1.beta_new[pt] = beta1;
-        // plan the next pair; with a second raw set, start its copies now
-        Work n0 = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
-        Work n1;
-        n1.tile = -1;
-        if (n0.tile >= 0) n1 = next_work<kMode>(p, list, cursor, num_tiles, pt);
-        if (lay.nset == 2) {
-            if (n0.tile >= 0) {
-                fetch_raw<kMode>(p, n0, RawView(smem + lay.raw(set ^ 1, 0), lay.slots, p.Q), pt);
-                if (kVerify && pt < n0.T) beta0 = load_beta(p, n0, pt);
-            }
-            if (n1.tile >= 0) {
-                fetch_raw<kMode>(p, n1, RawView(smem + lay.raw(set ^ 1, 1), lay.slots, p.Q), pt);
-                if (kVerify && pt < n1.T) beta1 = load_beta(p, n1, pt);
-            }
+        if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new[pt] = beta_next;
+        const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
+        if (nxt.tile >= 0) {
+            fetch_raw<kMode>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
+                                             lay.slots, p.Q), pt);
+            if (kMode == Mode::kVerify && pt < nxt.T)
+                beta_next = reinterpret_cast<const uint16_t *>(
+                    p.beta)[(size_t)(nxt.bos + pt) * p.stride_beta + nxt.head];
         }
-        // token-vector buffers of the pair, once the consumers freed them
-        const int b0 = j % lay.nbuf, use0 = j / lay.nbuf;
-        const int b1 = got1 % lay.nbuf, use1 = got1 / lay.nbuf;
-        if (pt == 0) {
-            if (use0 > 0 && ok) ok = wait_phase(&sy.empty_tok[0][b0], (use0 - 1) & 1, sy, p);
-            if (w1.tile >= 0 && use1 > 0 && ok)
-                ok = wait_phase(&sy.empty_tok[1][b1], (use1 - 1) & 1, sy, p);
-        }
+        // token vectors of `cur` into consumer c's buffer b, once it is free
+        const int b = use_c % lay.nbuf;
+        const int use_b = use_c / lay.nbuf;
+        if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
         producer_sync();
         if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
-        const TokView tv0(smem + lay.tok(0, b0), lay.slots, p.Q);
-        const TokView tv1(smem + lay.tok(1, b1), lay.slots, p.Q);
-        prep_pair<kMode, kBounded>(p, w0, rv0, tv0, w1, rv1, tv1, pt);
+        TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
+        prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
         if (pt == 0) {
-            write_info(sy.info[0][b0], w0);
-            if (w1.tile >= 0) write_info(sy.info[1][b1], w1);
+            ItemInfo &it = sy.info[c][b];
+            it.tile = cur.tile;
+            it.slot = cur.slot;
+            it.head = cur.head;
+            it.bos = cur.bos;
+            it.T = cur.T;
+            it.p = cur.p;
+            it.end = 0;
         }
-        producer_sync();  // token vectors and item info written, raw set read
-        if (pt == 0) {
-            mbar_arrive(&sy.full_tok[0][b0]);
-            if (w1.tile >= 0) mbar_arrive(&sy.full_tok[1][b1]);
-        }
-        if (lay.nset == 1) {
-            if (n0.tile >= 0) {
-                fetch_raw<kMode>(p, n0, RawView(smem + lay.raw(0, 0), lay.slots, p.Q), pt);
-                if (kVerify && pt < n0.T) beta0 = load_beta(p, n0, pt);
-            }
-            if (n1.tile >= 0) {
-                fetch_raw<kMode>(p, n1, RawView(smem + lay.raw(0, 1), lay.slots, p.Q), pt);
-                if (kVerify && pt < n1.T) beta1 = load_beta(p, n1, pt);
-            }
-        } else {
-            set ^= 1;
-        }
-        ++j;
-        if (w1.tile >= 0) ++got1;
-        w0 = n0;
-        w1 = n1;
+        producer_sync();  // all token vectors and the item info written
+        if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
+        ++n;
+        rb ^= 1;
+        cur = nxt;
     }
-    // end markers: each consumer's next buffer says "no more items"
+    // end markers: the next buffer of each consumer says "no more items"
     if (pt == 0) {
-        const int given[2] = {j, got1};
         for (int c = 0; c < 2; ++c) {
-            const int b = given[c] % lay.nbuf;
-            const int use_b = given[c] / lay.nbuf;
+            const int use_c = (n + 1 - c) >> 1;
+            const int b = use_c % lay.nbuf;
+            const int use_b = use_c / lay.nbuf;
             if (use_b > 0 && !wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p)) return;
             sy.info[c][b].end = 1;
             mbar_arrive(&sy.full_tok[c][b]);
@@ -616,7 +528,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         Tile h;
         load_tile(h, staging, L);
         mbar_arrive(&sy.empty_state[c]);
-        const TokView tv(smem + lay.tok(c, b), lay.slots, p.Q);
+        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         float *tile = p.pool + ((size_t)it.slot * p.H + it.head) * (size_t)(kD * kD);
         for (int u = 0; u < it.p; ++u) token_plain(h, tv, u, L);
         if (it.p > 0) store_tile(h, tile, L);
