@@ -143,8 +143,7 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 // ------------------------------------------------------- token vectors --
 //
 // One buffer of per-token vectors (fp32): slots [0, p) are folded (recorded)
-// tokens, [p, p + T) the new ones.  kh holds k and qh holds q as given (the
-// consumers normalise them); q only for new tokens.
+// tokens, [p, p + T) the new ones; q^ only for new tokens.
 struct TokView {
     float *kh, *e, *v, *qh, *beta;
     __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q) {
@@ -192,20 +191,13 @@ __device__ __forceinline__ float4 ld_cols(const float *vec, const Lane &L, int m
 
 // Row dot products of the thread's 8 rows with a vector x (its 16 columns),
 // in a fixed order: two interleaved partial sums per row (the even and the
-// odd columns of each float4, one packed pair), then their sum.  Also the
-// sum of squares of the thread's 16 entries of x, in a fixed order.
+// odd columns of each float4, one packed pair), then their sum.
 __device__ __forceinline__ void row_partials(const Tile &h, const float *x, const Lane &L,
-                                             float (&part)[8], float &sumsq) {
+                                             float (&part)[8]) {
     float2 acc[8];
-    float2 sq = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const float4 xx = ld_cols(x, L, m);
-        if (m == 0)
-            sq = mul2(xx.x, xx.y, xx.x, xx.y);
-        else
-            sq = fma2(xx.x, xx.y, xx.x, xx.y, sq);
-        sq = fma2(xx.z, xx.w, xx.z, xx.w, sq);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (m == 0)
@@ -217,15 +209,6 @@ __device__ __forceinline__ void row_partials(const Tile &h, const float *x, cons
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) part[i] = __fadd_rn(acc[i].x, acc[i].y);
-    sumsq = __fadd_rn(sq.x, sq.y);
-}
-
-// Sum over the 8 lanes of a row group (lane bits 0..2); every lane of the
-// group ends with the same bits.
-__device__ __forceinline__ float group_sum(float x) {
-    x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 1));
-    x = __fadd_rn(x, __shfl_xor_sync(kFull, x, 2));
-    return __fadd_rn(x, __shfl_xor_sync(kFull, x, 4));
 }
 
 // Sum the 8 row partials over the 8 lanes of the row group (lane bits 0..2)
@@ -255,15 +238,10 @@ __device__ __forceinline__ float reduce_rows(const float (&part)[8], int j) {
 
 // Pieces of one token of the recurrence on the thread's part of the tile:
 //   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T;  o = S q^.
-// The token vectors hold k and q as they come (not normalised): with
-// ik = 1 / |k| (eps inside the root), S k^ = ik (S k) and v' k^T =
-// (ik v') k^T, so the norms cost one sum of squares per lane, a reduction
-// over the row group and a handful of multiplies per row.
 
-// Decay along K in place, then the partial sums of S k of the 8 rows and
-// 1 / sqrt(|k|^2 + 1e-6).
+// Decay along K in place, then the partial sums of u = S k^ of the 8 rows.
 __device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int slot, const Lane &L,
-                                               float (&part)[8], float &ik) {
+                                               float (&part)[8]) {
     const float *e = tv.e + slot * kD;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
@@ -275,17 +253,15 @@ __device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int s
             h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     }
-    float ss;
-    row_partials(h, tv.kh + slot * kD, L, part, ss);
-    ik = inv_l2(group_sum(ss));
+    row_partials(h, tv.kh + slot * kD, L, part);
 }
 
-// v' = beta (v - u) for the lane's row, times ik, shared with the row group,
-// then the rank-one update S <- S + (ik v') k^T.
+// v' = beta (v - u) for the lane's row, shared with the row group, then the
+// rank-one update S <- S + v' k^T.
 __device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slot, float u,
-                                             float ik, const Lane &L) {
+                                             const Lane &L) {
     const float vr = tv.v[slot * kD + L.row(L.j)];
-    const float vp = __fmul_rn(__fmul_rn(tv.beta[slot], __fsub_rn(vr, u)), ik);
+    const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
     const int base = L.lane & ~7;
     float vpi[8];
 #pragma unroll
@@ -307,20 +283,18 @@ __device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slo
 
 // One token without output (commit replay, deferred fold, flush).
 __device__ __forceinline__ void token_plain(Tile &h, const TokView &tv, int slot, const Lane &L) {
-    float part[8], ik;
-    decay_partials(h, tv, slot, L, part, ik);
-    delta_update(h, tv, slot, __fmul_rn(reduce_rows(part, L.j), ik), ik, L);
+    float part[8];
+    decay_partials(h, tv, slot, L, part);
+    delta_update(h, tv, slot, reduce_rows(part, L.j), L);
 }
 
-// One token with output o = S q^ (after the update), q^ = q / |q| * scale,
-// written to out_row (bf16).
+// One token with output o = S q^ (after the update) to out_row (bf16).
 __device__ __forceinline__ void token_out(Tile &h, const TokView &tv, int slot, int qslot,
-                                          float scale, const Lane &L, __nv_bfloat16 *out_row) {
+                                          const Lane &L, __nv_bfloat16 *out_row) {
     token_plain(h, tv, slot, L);
-    float part[8], ss;
-    row_partials(h, tv.qh + qslot * kD, L, part, ss);
-    const float iq = __fmul_rn(inv_l2(group_sum(ss)), scale);
-    const float o = __fmul_rn(reduce_rows(part, L.j), iq);
+    float part[8];
+    row_partials(h, tv.qh + qslot * kD, L, part);
+    const float o = reduce_rows(part, L.j);
     out_row[L.row(L.j)] = __float2bfloat16_rn(o);
 }
 

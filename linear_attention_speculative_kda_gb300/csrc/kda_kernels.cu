@@ -147,8 +147,8 @@ constexpr int kPlanSize = kProducerThreads;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
-constexpr int kConsumerRegs = 216;
-constexpr int kProducerRegs = 72;
+constexpr int kConsumerRegs = 208;
+constexpr int kProducerRegs = 88;
 static_assert(2 * kConsumerThreads * kConsumerRegs + kProducerThreads * kProducerRegs <=
                   kBlockThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
@@ -384,7 +384,15 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
         const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
         const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
         const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
-        *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) = bf16x4_to_float4(kb);
+        const float4 k = bf16x4_to_float4(kb);
+        float s = __fmul_rn(k.x, k.x);
+        s = __fmaf_rn(k.y, k.y, s);
+        s = __fmaf_rn(k.z, k.z, s);
+        s = __fmaf_rn(k.w, k.w, s);
+        const float ik = inv_l2(warp_allsum(s));
+        *reinterpret_cast<float4 *>(tv.kh + u * kD + 4 * lane) =
+            make_float4(__fmul_rn(k.x, ik), __fmul_rn(k.y, ik), __fmul_rn(k.z, ik),
+                        __fmul_rn(k.w, ik));
         const float4 g = bf16x4_to_float4(gb);
         float4 e;
         e.x = decay_factor(__fadd_rn(g.x, bias.x), a, kBounded, p.lower_bound);
@@ -395,8 +403,17 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
         *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
         if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
         if (is_new) {
+            const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
+            float sq = __fmul_rn(q.x, q.x);
+            sq = __fmaf_rn(q.y, q.y, sq);
+            sq = __fmaf_rn(q.z, q.z, sq);
+            sq = __fmaf_rn(q.w, q.w, sq);
+            const float iq = inv_l2(warp_allsum(sq));
             *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
-                bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
+                make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.y, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.z, iq), p.scale),
+                            __fmul_rn(__fmul_rn(q.w, iq), p.scale));
             uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
             dst[lane] = kb;
             dst[kRecV / 4 + lane] = vb;
@@ -518,7 +535,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         if constexpr (kMode == Mode::kVerify) {
             for (int t = 0; t < it.T; ++t) {
                 const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
-                token_out(h, tv, it.p + t, t, p.scale, L, p.out + tok * kD);
+                token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
                 if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
             }
         }
