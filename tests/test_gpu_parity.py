@@ -276,3 +276,93 @@ def test_all_rows_idle_and_more_ctas_than_work():
     assert int(g.err.item()) == 0
     assert torch.equal(g.pool, g.pool0)
     assert (f64(g.out) == -9.0).all()
+
+
+def test_strided_activations_eight_byte_aligned():
+    """Activation rows whose token stride is a multiple of 4 elements but not of
+    8, starting 8 bytes past a 16-byte boundary, give the same bits as the
+    packed layout."""
+    wl = W.custom(B=9, H=3, Q=8, lens=[8, 3, 0, 8, 5, 1, 8, 7, 2], S=12, seed=23)
+    ref = GpuRun(wl, with_traj=True)
+    ref.verify()
+    ref.commit()
+    g = GpuRun(wl, with_traj=True)
+    st = g.steps[0]
+    T, H, D = st["qkv"].shape[0], wl.spec.H, wl.spec.D
+    width = 3 * H * D + 4
+    flat = torch.zeros(T * width + 4, dtype=torch.bfloat16, device="cuda")
+    view = flat[4:].view(T, width)
+    view[:, : 3 * H * D] = st["qkv"].reshape(T, -1)
+    q = view[:, 0 * H * D:1 * H * D].view(T, H, D)
+    k = view[:, 1 * H * D:2 * H * D].view(T, H, D)
+    v = view[:, 2 * H * D:3 * H * D].view(T, H, D)
+    assert q.stride(0) % 8 == 4 and q.data_ptr() % 16 == 8
+    api.kda_verify(q, k, v, st["g_raw"], st["beta_buf"][:, :H], g.A_log, g.g_bias, g.pool, g.cu,
+                   g.slots, g.records, g.out, trajectory_out=g.traj, error_word=g.err, **g.kw())
+    g.commit()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0 and int(ref.err.item()) == 0
+    assert torch.equal(g.out, ref.out)
+    assert torch.equal(g.traj, ref.traj)
+    assert torch.equal(g.pool, ref.pool)
+    assert torch.equal(g.records, ref.records)
+
+
+def test_deferred_window8_bounded_with_folds():
+    """Window 8 with the bounded gate and pending folds (token-vector buffers
+    sized for 16 tokens): two deferred steps equal two eager steps bit for
+    bit and match the oracle."""
+    wl = W.custom(B=24, H=2, Q=8, lens=[8, 7, 1, 8, 3, 8, 8, 5, 0, 8, 2, 8] * 2, S=30, R=28,
+                  deferred=True, steps=2, seed=29, bounded=True, lower_bound=-5.0,
+                  eager_prob=0.2)
+    ge = GpuRun(wl)
+    ge.verify(0)
+    ge.commit(0)
+    ge.verify(1)
+    ge.commit(1)
+    gd = GpuRun(wl)
+    gd.verify(0, pending=True)
+    gd.commit(0, deferred=True)
+    gd.verify(1, pending=True)
+    gd.commit(1, deferred=True, eager=torch.ones_like(wl.steps[1].eager).cuda())
+    torch.cuda.synchronize()
+    assert int(ge.err.item()) == 0 and int(gd.err.item()) == 0
+    assert torch.equal(ge.out, gd.out)
+    assert torch.equal(ge.pool, gd.pool)
+    layer = oracle_layer(wl)
+    cache = oracle_cache(wl)
+    s1, s2 = oracle_step(wl, 0), oracle_step(wl, 1)
+    O.verify(layer, cache, s1, pending=True)
+    O.commit(layer, cache, s1, wl.steps[0].num_accepted.numpy(), deferred=True,
+             eager=wl.steps[0].eager.numpy())
+    r2 = O.verify(layer, cache, s2, pending=True)
+    O.commit(layer, cache, s2, wl.steps[1].num_accepted.numpy())
+    assert_out_close(gd.out, r2.out)
+    pool = gd.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
+
+
+def test_record_slot_minus_one_rows():
+    """Rows without a record slot (-1) verify normally into the scratch row,
+    are never committed, and leave pending alone."""
+    wl = W.custom(B=6, H=2, Q=4, lens=[4, 4, 4, 4, 4, 4], S=10, R=6, deferred=True, seed=31,
+                  record_rows=[0, -1, 2, -1, 4, 5])
+    g = GpuRun(wl)
+    g.pending.fill_(0)
+    g.verify(pending=True)
+    g.commit(deferred=True, eager=torch.ones(6, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    res = O.verify(layer, cache, step, pending=True)
+    O.commit(layer, cache, step, wl.steps[0].num_accepted.numpy(), deferred=True,
+             eager=np.ones(6, np.uint8))
+    assert_out_close(g.out, res.out)
+    slots = wl.state_indices.numpy()
+    for b in (1, 3):
+        assert torch.equal(g.pool[int(slots[b])], g.pool0[int(slots[b])])
+    pool = g.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
