@@ -277,16 +277,22 @@ class Engine:
         self.pending = torch.zeros(sp.record_slots, dtype=torch.int32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
         self.all_eager = torch.ones(sp.B, dtype=torch.uint8, device=d)
-        T = wl.total_tokens
-        self.steps = []
-        for st in wl.steps:
-            self.steps.append(dict(
+        self.steps = self.new_input_set()
+        self.kw = dict(window=sp.Q, record_slots=sp.record_slots,
+                       lower_bound=sp.lower_bound if sp.bounded else None)
+
+    def new_input_set(self):
+        """Device copies of every decode step's inputs, plus output buffers."""
+        sp, d = self.wl.spec, self.dev
+        T = self.wl.total_tokens
+        steps = []
+        for st in self.wl.steps:
+            steps.append(dict(
                 qkv=st.qkv.to(d), beta_buf=st.beta_buf.to(d), g_raw=st.g_raw.to(d),
                 num_accepted=st.num_accepted.to(d),
                 eager=None if st.eager is None else st.eager.to(d),
                 out=torch.empty((T, sp.H, sp.D), dtype=torch.bfloat16, device=d)))
-        self.kw = dict(window=sp.Q, record_slots=sp.record_slots,
-                       lower_bound=sp.lower_bound if sp.bounded else None)
+        return steps
 
     def _verify(self, s, pending):
         H = self.wl.spec.H
@@ -302,20 +308,21 @@ class Engine:
                             pending=self.pending if deferred else None,
                             eager=eager if deferred else None, error_word=self.err, **self.kw)
 
-    def launches(self):
-        """The step as a list of (name, callable)."""
+    def launches(self, steps=None):
+        """The step as a list of (name, callable), on input set `steps`."""
+        steps = self.steps if steps is None else steps
         if not self.wl.spec.deferred:
-            s = self.steps[0]
+            s = steps[0]
             return [("verify", lambda: self._verify(s, False)),
                     ("commit", lambda: self._commit(s, False, None))]
-        s1, s2 = self.steps
+        s1, s2 = steps
         return [("verify", lambda: self._verify(s1, True)),
                 ("commit_deferred", lambda: self._commit(s1, True, s1["eager"])),
                 ("verify_fused", lambda: self._verify(s2, True)),
                 ("commit", lambda: self._commit(s2, True, self.all_eager))]
 
-    def run_step(self, events=None):
-        for i, (_, fn) in enumerate(self.launches()):
+    def run_step(self, events=None, steps=None):
+        for i, (_, fn) in enumerate(self.launches(steps)):
             if events is not None:
                 events[i][0].record()
             fn()
@@ -324,31 +331,58 @@ class Engine:
 
 
 class HostIO:
-    """Pinned host copies of each step's inputs and outputs, for the
-    end-to-end measure through the public API."""
+    """End-to-end steps through the public API with host buffers: every step
+    copies its inputs from pinned host memory to the device, runs the
+    launches, and copies its outputs back to pinned host memory.  Two device
+    input sets and three streams (copy-in, compute, copy-out) let step i+1's
+    inputs travel while step i computes, as a serving loop would."""
+
+    KEYS = ("qkv", "beta_buf", "g_raw", "num_accepted", "eager")
 
     def __init__(self, eng: Engine):
         self.eng = eng
+        self.sets = [eng.steps, eng.new_input_set()]
         self.h_in = []
-        self.h_out = []
         for st in eng.steps:
-            ins = {k: st[k].cpu().pin_memory() for k in ("qkv", "beta_buf", "g_raw",
-                                                          "num_accepted")}
-            if st["eager"] is not None:
-                ins["eager"] = st["eager"].cpu().pin_memory()
-            self.h_in.append(ins)
-            self.h_out.append(torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory())
+            self.h_in.append({k: st[k].cpu().pin_memory() for k in self.KEYS
+                              if st[k] is not None})
+        self.h_out = [[torch.empty(st["out"].shape, dtype=st["out"].dtype).pin_memory()
+                       for st in eng.steps] for _ in range(2)]
         self.h2d = sum(t.numel() * t.element_size() for ins in self.h_in for t in ins.values())
-        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out[0])
+        self.copy_in = torch.cuda.Stream(eng.dev)
+        self.copy_out = torch.cuda.Stream(eng.dev)
+        self.freed = [None, None]
 
-    def run_step(self):
-        eng = self.eng
-        for st, ins in zip(eng.steps, self.h_in):
-            for k, t in ins.items():
-                st[k].copy_(t, non_blocking=True)
-        eng.run_step()
-        for st, out in zip(eng.steps, self.h_out):
-            out.copy_(st["out"], non_blocking=True)
+    def run(self, k_steps: int):
+        comp = torch.cuda.current_stream(self.eng.dev)
+        go = torch.cuda.Event()
+        go.record(comp)
+        self.copy_in.wait_event(go)
+        for i in range(k_steps):
+            s = i & 1
+            dev = self.sets[s]
+            with torch.cuda.stream(self.copy_in):
+                if self.freed[s] is not None:
+                    self.copy_in.wait_event(self.freed[s])
+                for st, ins in zip(dev, self.h_in):
+                    for k, t in ins.items():
+                        st[k].copy_(t, non_blocking=True)
+                arrived = torch.cuda.Event()
+                arrived.record(self.copy_in)
+            comp.wait_event(arrived)
+            self.eng.run_step(steps=dev)
+            done = torch.cuda.Event()
+            done.record(comp)
+            with torch.cuda.stream(self.copy_out):
+                self.copy_out.wait_event(done)
+                for st, out in zip(dev, self.h_out[s]):
+                    out.copy_(st["out"], non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(self.copy_out)
+                self.freed[s] = freed
+        comp.wait_stream(self.copy_in)
+        comp.wait_stream(self.copy_out)
 
 
 # -------------------------------------------------------------- CPU side --
@@ -494,15 +528,13 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     hio = HostIO(eng)
-    for _ in range(2):
-        hio.run_step()
+    hio.run(4)
     torch.cuda.synchronize()
     e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     e_start.record(stream)
-    for _ in range(args.steps):
-        hio.run_step()
+    hio.run(args.steps)
     e_stop.record(stream)
     torch.cuda.synchronize()
     e_ms = max_over_ranks(e_start.elapsed_time(e_stop), world, device)
