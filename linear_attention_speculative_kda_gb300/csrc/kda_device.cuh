@@ -89,17 +89,33 @@ __device__ __forceinline__ float inv_l2(float sum) {
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(sum, 1e-6f)));
 }
 
+// softplus(x) = log(1 + e^x), taken as x itself for x > 20, evaluated as
+// max(x, 0) + log1p(z) with z = e^{-|x|} in (0, 1] (an identity) and
+// log1p(z) = z * P(z): P is a degree-9 least-squares fit of log1p(z) / z on
+// [0, 1] (coefficients from softplus_poly.py), within 2 ulp of log1p in
+// fp32.  A fixed chain of fused multiply-adds: no branch, no logarithm.
+__device__ __forceinline__ float softplus(float x) {
+    constexpr float c[10] = {0x1p+0f,        -0x1.ffffcp-2f,  0x1.554c9cp-2f, -0x1.ff11c2p-3f,
+                             0x1.930202p-3f, -0x1.399642p-3f, 0x1.b2c2a2p-4f, -0x1.d3784ep-5f,
+                             0x1.4628bp-6f,  -0x1.aad1eep-9f};
+    const float z = expf(-fabsf(x));
+    float r = c[9];
+#pragma unroll
+    for (int i = 8; i >= 0; --i) r = __fmaf_rn(r, z, c[i]);
+    const float l = __fmul_rn(z, r);
+    const float sp = x > 0.0f ? __fadd_rn(x, l) : l;
+    return x > 20.0f ? x : sp;
+}
+
 // exp(g) for one channel, x = g_raw + g_bias, a = exp(A_log[h]).
 // Bounded gate: g = lb * sigmoid(a x) = lb / (1 + exp(-a x)).
-// Softplus gate: g = -a * softplus(x), softplus(x) = x for x > 20.
+// Softplus gate: g = -a * softplus(x).
 __device__ __forceinline__ float decay_factor(float x, float a, bool bounded, float lb) {
     float g;
-    if (bounded) {
+    if (bounded)
         g = __fdiv_rn(lb, __fadd_rn(1.0f, expf(-__fmul_rn(a, x))));
-    } else {
-        float sp = x > 20.0f ? x : log1pf(expf(x));
-        g = -__fmul_rn(a, sp);
-    }
+    else
+        g = -__fmul_rn(a, softplus(x));
     return expf(g);
 }
 

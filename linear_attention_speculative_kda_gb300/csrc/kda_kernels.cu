@@ -367,7 +367,7 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
 }
 
 // Per-token vectors of an item: token u is prepared by producer warp
-// (u mod 2), four channels per lane, the norms summed across the warp; every
+// (u mod 4), four channels per lane, the norms summed across the warp; every
 // token is computed the same way however many tokens the item has.  The
 // verify also writes the new tokens' raw records.
 template <Mode kMode, bool kBounded>
