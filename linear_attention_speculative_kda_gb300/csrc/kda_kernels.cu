@@ -427,9 +427,7 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
                                             uint64_t *bar) {
     const float *src = p.pool + ((size_t)w.slot * p.H + w.head) * (size_t)(kD * kD);
     mbar_arrive_expect_tx(bar, kD * kD * 4);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-        bulk_load(dst + c * (kD * kD / 4), src + c * (kD * kD / 4), kD * kD, bar);
+    bulk_load(dst, src, kD * kD * 4, bar);
 }
 
 template <Mode kMode, bool kBounded>
