@@ -26,6 +26,11 @@ the pages define around it, each function citing the passage it follows:
   only store n as the pending replay of their record slot.
 * ``flush`` -- ``KDADeferredCommitContext.flush``: fold pending replays into
   the checkpoints in place, leaving ``pending`` as it is.
+* ``conv_compact`` -- ``_compact_conv_state_kernel`` of recoverssm.py in its
+  non-align form: after the verify a row's conv state holds
+  ``[history[1:], x_0 .. x_{Q-1}]``; once n tokens are accepted the window
+  that starts at column n - 1 is moved to column 0, so that the next step
+  reads it as if one token had been accepted.
 
 Readings where the pages are silent (the same list is kept with the design
 notes): a row with T > Q, a state index >= the pool size, a record slot
@@ -374,6 +379,51 @@ def flush(layer: Layer, cache: Cache, step: Step, *, rows=None, heads=None,
         return None
 
     return [x for x in _map_rows(run, list(rows), threads) if x is not None]
+
+
+def conv_history(width: int, window: int) -> int:
+    """Columns of conv history a row keeps: the conv state is
+    ``history + Q - 1`` wide (the commit context derives the history length
+    as the width minus the window plus one)."""
+    return int(width) - int(window) + 1
+
+
+def conv_compact(conv, cu_seqlens, state_indices, num_accepted, window: int):
+    """Conv-state compaction of a commit (``_compact_conv_state_kernel``,
+    non-align mode: the final state is the source state).
+
+    ``conv`` is the logical conv-state pool ``[slots, conv_dim, width]`` (any
+    dtype: the values are moved, not computed).  For every row b with
+    T = cu_seqlens[b+1] - cu_seqlens[b], slot s = state_indices[b] and
+    n = min(max(num_accepted[b], 0), T, Q): if s > 0 and n > 0, the columns
+    [n - 1, n - 1 + history) of every channel of slot s are copied to columns
+    [0, history), reading all of them before writing any (the kernel loads
+    the whole block, then stores it).  Other rows and the columns from
+    ``history`` on are left alone.  Rows with T outside [0, Q] or s beyond
+    the pool are invalid: skipped and reported.
+
+    Returns (new pool, list of RowIssue)."""
+    out = np.array(conv, copy=True)
+    S, _, width = out.shape
+    hist = conv_history(width, window)
+    if hist < 1:
+        raise ValueError("conv state narrower than its window")
+    issues = []
+    for b in range(len(state_indices)):
+        T = _row_len(cu_seqlens, b)
+        slot = int(state_indices[b])
+        if T < 0 or T > window:
+            issues.append(RowIssue(b, "length"))
+            continue
+        if slot >= S:
+            issues.append(RowIssue(b, "slot"))
+            continue
+        n = commit_len(num_accepted[b], T, window)
+        if slot <= 0 or n <= 0:
+            continue
+        src = np.array(out[slot, :, n - 1:n - 1 + hist], copy=True)
+        out[slot, :, 0:hist] = src
+    return out, issues
 
 
 def default_threads() -> int:
