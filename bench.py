@@ -461,6 +461,60 @@ def workload_config(wl: W.Workload, world: int):
                 wl.pool.numel() * 4 / 1e9)}
 
 
+def conv_compact_bytes(wl: W.Workload, conv_dim: int, hist: int, elem_bytes: int, acc) -> int:
+    """Algorithmic bytes of one conv compaction: every committed row (slot > 0,
+    n > 0) reads its window of conv_dim x history elements and writes it
+    back at column 0."""
+    lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
+    slots = wl.state_indices.tolist()
+    rows = sum(1 for b in range(wl.spec.B)
+               if slots[b] > 0 and min(max(int(acc[b]), 0), lens[b], wl.spec.Q) > 0)
+    return 2 * rows * conv_dim * hist * elem_bytes
+
+
+def measure_conv_compact(wl: W.Workload, device, iters: int, warmup: int, peak: float,
+                         layout: str = "dim_first"):
+    """The conv-state compaction of the workload's commit (bf16 pool
+    [S, 3*H*D, history + Q - 1], channel-major or column-major), timed alone
+    with CUDA events.  Three pool copies in rotation keep each launch's pool
+    out of L2."""
+    from linear_attention_speculative_kda_gb300 import api
+    S, C, width = W.conv_shape(wl.spec)
+
+    def on_device(t):  # keep the storage order of the host pool
+        return t.to(device) if layout == "dim_first" else \
+            t.transpose(1, 2).contiguous().to(device).transpose(1, 2)
+
+    pools = [on_device(W.conv_state(S, C, width, seed=i, layout=layout)) for i in range(3)]
+    i32 = dict(dtype=torch.int32, device=device)
+    cu = wl.cu_seqlens.to(**i32)
+    slots = wl.state_indices.to(**i32)
+    acc = wl.steps[0].num_accepted.to(**i32)
+    err = torch.zeros(1, **i32)
+
+    def launch(k):
+        api.kda_conv_compact(pools[k % 3], cu, slots, acc, window=wl.spec.Q, error_word=err)
+
+    for k in range(warmup):
+        launch(k)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for k in range(iters):
+        launch(k)
+    stop.record()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the conv compaction")
+    us = start.elapsed_time(stop) * 1e3 / iters
+    b = conv_compact_bytes(wl, C, width - wl.spec.Q + 1, 2, wl.steps[0].num_accepted.tolist())
+    del pools
+    return {"shape": [S, C, width], "dtype": "bf16",
+            "layout": "channel-major" if layout == "dim_first" else "column-major",
+            "launches": iters, "avg_us": us, "bytes_per_launch": b,
+            "gbs": b / (us / 1e6) / 1e9, "frac": b / (us / 1e6) / 1e9 / peak}
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     device = torch.device("cuda", local)
@@ -543,6 +597,10 @@ def run_ours(args):
     e2e = {"value": units_all / (e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": hio.h2d,
            "d2h_bytes_per_step": hio.d2h, "ms_per_step": e_ms / args.steps}
 
+    # the commit's conv-state compaction, a separate launch, timed on its own
+    conv = {lay: measure_conv_compact(wl, device, max(20, args.steps // 4), args.warmup, peak,
+                                      layout=lay) for lay in ("dim_first", "col_first")}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_budget)
@@ -553,7 +611,8 @@ def run_ours(args):
             "data": "synthetic (seeded)", "config": workload_config(wl, world),
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
-            "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu}
+            "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
+            "extras": {"conv_compact": conv}}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:

@@ -186,6 +186,51 @@ kda_status kda_flush(const kda_config *cfg,
                      const int32_t *pending,
                      int32_t *error_word, void *stream);
 
+/*
+ * kda_conv_compact -- conv-state compaction of a commit ([GLM]
+ * `_compact_conv_state_kernel` in its non-align form, launched by
+ * `Glm5NextRecoverSSMCommitContext.commit` beside the state replay).
+ *
+ * The short causal conv in front of q, k and v keeps, per state slot, a
+ * window of `width` columns per channel; after the verify it holds
+ * [history[1:], x_0 .. x_{Q-1}] with history = width - Q + 1 columns.  For
+ * each row b with T = cu_seqlens[b+1] - cu_seqlens[b], slot s =
+ * state_indices[b] and n = min(max(num_accepted[b], 0), T, Q) (the commit's
+ * count): if s > 0 and n > 0, every channel's columns [n-1, n-1+history) of
+ * slot s move to columns [0, history), all read before any is written, so the
+ * next step reads its history at column 0.  Columns from `history` on and all
+ * other slots are left alone.  Deferred rows are compacted too: only the
+ * recurrent replay is deferred, and the next step's conv needs the window now.
+ * Rows with T outside [0, Q] or s >= num_slots are skipped and flagged in
+ * *error_word (KDA_ROW_BAD_LENGTH, KDA_ROW_BAD_SLOT).
+ *
+ * conv_state: the caller's pool, element (slot, channel, column) at
+ * slot*stride_slot + channel*stride_dim + column*stride_col elements of
+ * elem_bytes each (2: bf16/fp16, 4: fp32; values are moved as bits).  Both
+ * the channel-major ("dim first") and the column-major layouts are strides
+ * of this form.  The strides must map distinct (channel, column) pairs of a
+ * slot to distinct elements.  A separate launch from kda_commit: it runs
+ * over every committed row, deferred or not, and is a plain copy.
+ */
+#define KDA_MAX_CONV_HISTORY 16
+
+typedef struct kda_conv_config {
+    int32_t num_slots;        /* S: slots of the conv-state pool (slot 0 = null) */
+    int32_t conv_dim;         /* channels >= 1 */
+    int32_t width;            /* columns per channel: history + window - 1 */
+    int32_t window;           /* Q = 1 + num_spec, 1..8 */
+    int32_t elem_bytes;       /* 2 or 4 */
+    int32_t reserved;         /* 0 */
+    int64_t stride_slot;      /* element strides, each >= 1 */
+    int64_t stride_dim;
+    int64_t stride_col;
+} kda_conv_config;
+
+kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
+                            const int32_t *cu_seqlens, const int32_t *state_indices,
+                            int32_t B, const int32_t *num_accepted,
+                            int32_t *error_word, void *stream);
+
 /* Name of a status code (static string). */
 const char *kda_status_string(kda_status status);
 

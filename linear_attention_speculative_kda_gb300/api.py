@@ -38,6 +38,7 @@ EXPORTED = (
     "kda_verify",
     "kda_commit",
     "kda_flush",
+    "kda_conv_compact",
     "kda_status_string",
     "kda_abi_version",
 )
@@ -69,6 +70,22 @@ class KdaConfig(ctypes.Structure):
     ]
 
 
+class KdaConvConfig(ctypes.Structure):
+    _fields_ = [
+        ("num_slots", ctypes.c_int32),
+        ("conv_dim", ctypes.c_int32),
+        ("width", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("elem_bytes", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("stride_slot", ctypes.c_int64),
+        ("stride_dim", ctypes.c_int64),
+        ("stride_col", ctypes.c_int64),
+    ]
+
+
+MAX_CONV_HISTORY = 16
+
 _lib_handle = None
 
 
@@ -96,6 +113,8 @@ def load_library():
     lib.kda_commit.argtypes = [cfgp] + [vp] * 5 + [i32] + [vp] * 7
     lib.kda_flush.restype = ctypes.c_int
     lib.kda_flush.argtypes = [cfgp] + [vp] * 4 + [i32] + [vp] * 5
+    lib.kda_conv_compact.restype = ctypes.c_int
+    lib.kda_conv_compact.argtypes = [ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] + [vp] * 3
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_abi_version.restype = i32
@@ -288,3 +307,45 @@ def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, win
                        _ptr(state_indices), B, _ptr(record_rows), _ptr(records), _ptr(pending),
                        _ptr(error_word), _stream_ptr(dev))
     _check("kda_flush", st)
+
+
+def make_conv_config(conv_state: torch.Tensor, window: int) -> KdaConvConfig:
+    """``kda_conv_config`` of a conv-state pool viewed as [S, conv_dim, width]
+    (any strides: a channel-major pool or a transposed view of a
+    column-major one)."""
+    if conv_state.dim() != 3:
+        raise ValueError("conv_state must be viewed as [S, conv_dim, width]")
+    cc = KdaConvConfig()
+    cc.num_slots, cc.conv_dim, cc.width = (int(x) for x in conv_state.shape)
+    cc.window = window
+    cc.elem_bytes = conv_state.element_size()
+    cc.reserved = 0
+    cc.stride_slot, cc.stride_dim, cc.stride_col = (int(x) for x in conv_state.stride())
+    return cc
+
+
+def kda_conv_compact(conv_state, cu_seqlens, state_indices, num_accepted, *, window: int,
+                     error_word=None) -> None:
+    """``kda_conv_compact``: move each committed row's conv window (starting
+    at column n - 1) to column 0, in place.  conv_state: [S, conv_dim, width]
+    view of 2- or 4-byte elements."""
+    dev = conv_state.device
+    i32 = torch.int32
+    if conv_state.element_size() not in (2, 4):
+        raise TypeError("conv_state elements must be 2 or 4 bytes")
+    _req(cu_seqlens, i32, "cu_seqlens", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _req(num_accepted, i32, "num_accepted", dev)
+    _opt(error_word, i32, "error_word", dev)
+    for t in (cu_seqlens, state_indices, num_accepted):
+        if not t.is_contiguous():
+            raise ValueError("metadata tensors must be contiguous")
+    B = state_indices.shape[0]
+    if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < B:
+        raise ValueError("metadata sizes do not match the batch")
+    cc = make_conv_config(conv_state, window)
+    lib = load_library()
+    st = lib.kda_conv_compact(ctypes.byref(cc), _ptr(conv_state), _ptr(cu_seqlens),
+                              _ptr(state_indices), B, _ptr(num_accepted), _ptr(error_word),
+                              _stream_ptr(dev))
+    _check("kda_conv_compact", st)

@@ -790,6 +790,6 @@ const char *kda_status_string(kda_status status) {
     return "KDA_ERR_UNKNOWN";
 }
 
-int32_t kda_abi_version(void) { return 1; }
+int32_t kda_abi_version(void) { return 2; }
 
 }  // extern "C"

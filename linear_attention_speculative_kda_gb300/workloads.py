@@ -223,3 +223,30 @@ def custom(B: int, H: int, Q: int, lens, *, S: int | None = None, R: int = 0,
     for _ in range(steps):
         wl.steps.append(_step_inputs(spec, lens_pos, gen))
     return wl
+
+
+# ------------------------------------------------------------ conv state --
+
+CONV_KERNEL = 4   # short causal conv width (history 3), the usual KDA setting
+
+
+def conv_shape(spec: Spec, kernel: int = CONV_KERNEL) -> tuple[int, int, int]:
+    """[S, conv_dim, width] of the conv-state pool of a workload: one conv
+    channel per q, k and v channel of every head (conv_dim = 3 * H * D) and
+    kernel - 1 history columns plus Q - 1 draft columns."""
+    return spec.S, 3 * spec.H * spec.D, kernel - 1 + spec.Q - 1
+
+
+def conv_state(S: int, conv_dim: int, width: int, *, dtype=torch.bfloat16, seed: int = 0,
+               layout: str = "dim_first") -> torch.Tensor:
+    """A seeded conv-state pool viewed as [S, conv_dim, width] (CPU).
+    ``dim_first``: stored channel-major, [S][conv_dim][width];
+    ``col_first``: stored column-major, [S][width][conv_dim], viewed
+    transposed.  Values are N(0, 1) cast to ``dtype`` (only their bits
+    matter: the compaction moves them)."""
+    gen = torch.Generator().manual_seed(seed)
+    if layout == "dim_first":
+        return torch.randn((S, conv_dim, width), generator=gen).to(dtype)
+    if layout == "col_first":
+        return torch.randn((S, width, conv_dim), generator=gen).to(dtype).transpose(1, 2)
+    raise ValueError(layout)

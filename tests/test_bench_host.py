@@ -145,3 +145,10 @@ def test_profiled_traffic_requires_current_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("commit", "w") is None
     (csrc / "a.cu").write_text("kernel v2")
     assert bench.profiled_traffic("verify", "w") is None
+
+
+def test_conv_compact_bytes_counts_committed_rows():
+    wl = W.custom(B=6, H=2, Q=4, lens=[4, 0, 3, 4, 2, 4], S=10, seed=8,
+                  slots=[1, 2, 3, 0, 5, 6])
+    acc = [2, 3, 0, 4, 9, -1]  # committed: rows 0 (n 2) and 4 (n clamped to 2)
+    assert bench.conv_compact_bytes(wl, 768, 3, 2, acc) == 2 * 2 * 768 * 3 * 2

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(api.EXPORTED)
     for name in names:
         assert hasattr(lib, name), name
-    assert lib.kda_abi_version() == 1
+    assert lib.kda_abi_version() == 2
     assert lib.kda_status_string(api.KDA_ERR_CUDA) == b"KDA_ERR_CUDA"
 
 
@@ -105,3 +105,33 @@ def test_commit_and_flush_host_checks(lib):
                          None) == api.KDA_ERR_INVALID_ARG
     assert lib.kda_flush(c, FAKE, FAKE, FAKE, FAKE, 0, None, FAKE, FAKE, None,
                          None) == api.KDA_OK
+
+
+def _conv(lib, B=3, cc=None, conv=FAKE, cu=FAKE, slots=FAKE, acc=FAKE, err=None, **kw):
+    if cc is None:
+        base = dict(num_slots=8, conv_dim=384, width=6, window=4, elem_bytes=2, reserved=0,
+                    stride_slot=384 * 6, stride_dim=6, stride_col=1)
+        base.update(kw)
+        cc = api.KdaConvConfig(**base)
+    ccp = None if cc is False else ctypes.byref(cc)
+    return lib.kda_conv_compact(ccp, conv, cu, slots, B, acc, err, None)
+
+
+def test_conv_compact_host_checks(lib):
+    assert _conv(lib, cc=False) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, elem_bytes=8) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, width=3) == api.KDA_ERR_INVALID_ARG            # narrower than the window
+    assert _conv(lib, width=20) == api.KDA_ERR_UNSUPPORTED           # history 17 > 16
+    assert _conv(lib, window=9, width=12) == api.KDA_ERR_UNSUPPORTED
+    assert _conv(lib, window=0) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, conv_dim=0) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, stride_col=0) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, reserved=1) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, B=-1) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, conv=None) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, acc=None) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, conv=FAKE + 1) == api.KDA_ERR_INVALID_ARG      # not element-aligned
+    assert _conv(lib, elem_bytes=4, conv=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, cu=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+    # B == 0: nothing to do, and no pointer is looked at
+    assert _conv(lib, B=0, conv=None, cu=None, slots=None, acc=None) == api.KDA_OK
