@@ -26,6 +26,12 @@ the pages define around it, each function citing the passage it follows:
   only store n as the pending replay of their record slot.
 * ``flush`` -- ``KDADeferredCommitContext.flush``: fold pending replays into
   the checkpoints in place, leaving ``pending`` as it is.
+* ``commit_align`` / ``conv_compact_align`` -- the align mode of the same
+  commit (``_prepare_commit_plan_kernel`` with a block table,
+  ``_replay_indices_kernel``): the state after the n-th accepted token goes
+  to the block that holds that token, and, when the step crosses a block
+  boundary before its last token, the state at the boundary goes to the
+  block that ends there; the conv windows follow the same two blocks.
 * ``conv_compact`` -- ``_compact_conv_state_kernel`` of recoverssm.py in its
   non-align form: after the verify a row's conv state holds
   ``[history[1:], x_0 .. x_{Q-1}]``; once n tokens are accepted the window
@@ -423,6 +429,142 @@ def conv_compact(conv, cu_seqlens, state_indices, num_accepted, window: int):
             continue
         src = np.array(out[slot, :, n - 1:n - 1 + hist], copy=True)
         out[slot, :, 0:hist] = src
+    return out, issues
+
+
+# ---------------------------------------------------------------------------
+# Align mode (paged mamba blocks)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class AlignPlan:
+    n: int                   # commit count
+    final: int               # block slot of the state after token n - 1
+    boundary: int            # block slot of the state at the crossed boundary, or 0
+    boundary_len: int        # tokens up to that boundary (0 when none)
+
+
+def align_plan(n: int, num_computed: int, block_row, block_size: int):
+    """``_prepare_commit_plan_kernel``, align branch, for a row whose commit
+    count is n > 0: token t of the step sits at position num_computed + t.
+    The final state belongs to the block of the last committed token,
+    column (num_computed + n - 1) // block_size (the table's last column if
+    it runs past the table).  The first block boundary after num_computed
+    (the next multiple of block_size above it) is crossed when the step
+    reaches it; the state after those boundary_len tokens belongs to the
+    block that ends there.  Returns None when that block lies past the
+    table."""
+    width = len(block_row)
+    final_col = min(max(num_computed + n - 1, 0) // block_size, width - 1)
+    next_boundary = (num_computed // block_size + 1) * block_size
+    boundary, boundary_len = 0, next_boundary - num_computed
+    if num_computed + n >= next_boundary:
+        col = next_boundary // block_size - 1
+        if col >= width:
+            return None
+        boundary = int(block_row[col])
+    return AlignPlan(n, int(block_row[final_col]), boundary, boundary_len)
+
+
+def _align_row(layer, cache_slots, T, slot, num_accepted, num_computed, block_row, block_size):
+    """Plan of one row, or (None, reason) / (None, None) when it commits nothing."""
+    n = commit_len(num_accepted, T, layer.window)
+    if slot <= 0 or n <= 0:
+        return None, None
+    plan = align_plan(n, int(num_computed), block_row, block_size)
+    if plan is None:
+        return None, "block"
+    if plan.final >= cache_slots or plan.boundary >= cache_slots:
+        return None, "slot"
+    if plan.final <= 0:
+        return None, None
+    return plan, None
+
+
+def commit_align(layer: Layer, cache: Cache, step: Step, num_accepted, block_table,
+                 num_computed, block_size: int, *, request_indices=None, rows=None,
+                 heads=None, threads: int = 1) -> list:
+    """Align-mode commit (recoverssm.py commit context with a block table;
+    ``_replay_indices_kernel``): each valid row replays its first n records
+    from the checkpoint of ``state_indices[b]`` and writes the state after
+    token n - 1 to its final block and, if the boundary comes before the last
+    token (boundary_len < n), the state after boundary_len tokens to the
+    boundary block.  The source slot itself is not written unless it is one
+    of those blocks.  ``num_accepted``, ``num_computed`` and the block-table
+    rows are indexed by request (``request_indices[b]``, or b).  Returns the
+    list of invalid rows."""
+    B = len(step.state_indices)
+    H = layer.num_heads
+    rows = range(B) if rows is None else rows
+    heads = range(H) if heads is None else heads
+
+    def run(b):
+        T = _row_len(step.cu_seqlens, b)
+        slot = int(step.state_indices[b])
+        r = _record_slot(step.record_rows, b)
+        bad = _row_checks(layer, cache, T, slot, r)
+        if bad:
+            return RowIssue(b, bad)
+        req = b if request_indices is None else int(request_indices[b])
+        plan, bad = _align_row(layer, cache.num_slots, T, slot, num_accepted[req],
+                               num_computed[req], block_table[req], block_size)
+        if bad:
+            return RowIssue(b, bad)
+        if plan is None or r < 0:
+            return None
+        for h in heads:
+            # both replays start from the checkpoint as it was before the commit
+            mid = None
+            if plan.boundary > 0 and plan.boundary_len < plan.n:
+                mid = _replay_records(layer, cache, slot, h, r, plan.boundary_len)
+            end = _replay_records(layer, cache, slot, h, r, plan.n)
+            if mid is not None:
+                cache.set_state(plan.boundary, h, mid)
+            cache.set_state(plan.final, h, end)
+        return None
+
+    return [x for x in _map_rows(run, list(rows), threads) if x is not None]
+
+
+def conv_compact_align(conv, cu_seqlens, state_indices, num_accepted, window: int,
+                       block_table, num_computed, block_size: int, *, request_indices=None):
+    """Align-mode conv compaction (``_compact_conv_state_kernel`` with
+    ALIGN_MODE): the window at column n - 1 of the source slot goes to
+    columns [0, history) of the final block, and the window at column
+    boundary_len - 1 to the boundary block when there is one; both are read
+    before either is written.  Returns (new pool, list of RowIssue)."""
+    out = np.array(conv, copy=True)
+    S, _, width = out.shape
+    hist = conv_history(width, window)
+    if hist < 1:
+        raise ValueError("conv state narrower than its window")
+    layer = Layer(0, 0, window, None, None, False, 0.0, 1.0)
+    issues = []
+    for b in range(len(state_indices)):
+        T = _row_len(cu_seqlens, b)
+        slot = int(state_indices[b])
+        if T < 0 or T > window:
+            issues.append(RowIssue(b, "length"))
+            continue
+        if slot >= S:
+            issues.append(RowIssue(b, "slot"))
+            continue
+        req = b if request_indices is None else int(request_indices[b])
+        plan, bad = _align_row(layer, S, T, slot, num_accepted[req], num_computed[req],
+                               block_table[req], block_size)
+        if bad:
+            issues.append(RowIssue(b, bad))
+            continue
+        if plan is None:
+            continue
+        fin = np.array(out[slot, :, plan.n - 1:plan.n - 1 + hist], copy=True)
+        bnd = None
+        if plan.boundary > 0:
+            bnd = np.array(out[slot, :, plan.boundary_len - 1:plan.boundary_len - 1 + hist],
+                           copy=True)
+        if bnd is not None:
+            out[plan.boundary, :, 0:hist] = bnd
+        out[plan.final, :, 0:hist] = fin
     return out, issues
 
 

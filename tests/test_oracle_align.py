@@ -1,0 +1,173 @@
+"""Pins of the oracle's align-mode commit (CPU).
+
+Align mode keeps the recurrent and conv states in paged blocks of
+``block_size`` tokens: the state after the last committed token belongs to
+the block that holds that token, and a step that completes a block leaves
+that block the state at its end.  The pins check the plan by walking the
+token positions against explicit block ranges (no division formula), the
+replayed states against the oracle verify's own trajectory, the reduction to
+the plain commit when every block is the source slot, and the conv windows
+against the accepted input sequence.
+"""
+
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+from linear_attention_speculative_kda_gb300 import workloads as W  # noqa: E402
+from oracle import kda_oracle as O  # noqa: E402
+from tests.helpers import oracle_cache, oracle_layer, oracle_step  # noqa: E402
+
+
+def _walk(n, num_computed, block_size, width):
+    """Final column and (boundary column, boundary_len) by walking positions."""
+    blocks = [range(j * block_size, (j + 1) * block_size) for j in range(width + 4)]
+    last = num_computed + n - 1
+    final_col = next(j for j, blk in enumerate(blocks) if last in blk)
+    final_col = min(final_col, width - 1)
+    boundary = None
+    for t in range(n):
+        done = num_computed + t + 1          # tokens in the sequence after token t
+        for j, blk in enumerate(blocks):
+            if done == blk[-1] + 1 and blk[-1] >= num_computed:
+                boundary = (j, t + 1)
+                break
+        if boundary:
+            break
+    return final_col, boundary
+
+
+@pytest.mark.parametrize("block_size", [4, 5, 8, 16])
+def test_plan_matches_walk_over_positions(block_size):
+    width = 6
+    row = [100 + j for j in range(width)]
+    for num_computed in range(0, block_size * width - 1):
+        for n in range(1, min(block_size, 8) + 1):
+            plan = O.align_plan(n, num_computed, row, block_size)
+            final_col, boundary = _walk(n, num_computed, block_size, width)
+            if boundary is not None and boundary[0] >= width:
+                assert plan is None
+                continue
+            assert plan.final == row[final_col]
+            if boundary is None:
+                assert plan.boundary == 0
+            else:
+                assert (plan.boundary, plan.boundary_len) == (row[boundary[0]], boundary[1])
+
+
+def _align_case(seed=21, Q=4, bs=4):
+    wl = W.custom(B=8, H=2, Q=Q, lens=[4, 4, 3, 4, 2, 4, 4, 1], S=60, seed=seed,
+                  slots=[1, 2, 3, 0, 4, 5, 6, 7])
+    rng = np.random.default_rng(seed)
+    width = 6
+    # distinct block slots 10.. per row
+    table = np.arange(10, 10 + 8 * width).reshape(8, width)
+    num_computed = rng.integers(0, bs * (width - 1), size=8)
+    return wl, table, num_computed, bs
+
+
+def test_states_are_the_verify_trajectory_at_final_and_boundary():
+    wl, table, nc, bs = _align_case()
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    ref = O.verify(layer, oracle_cache(wl), step, want_traj=True)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)                       # writes the records
+    acc = wl.steps[0].num_accepted.numpy()
+    issues = O.commit_align(layer, cache, step, acc, table, nc, bs)
+    assert issues == []
+    cu = wl.cu_seqlens.numpy()
+    written = set()
+    for b in range(8):
+        slot = int(wl.state_indices[b])
+        n = O.commit_len(acc[b], cu[b + 1] - cu[b], wl.spec.Q)
+        if slot <= 0 or n <= 0:
+            continue
+        plan = O.align_plan(n, int(nc[b]), table[b], bs)
+        for h in range(wl.spec.H):
+            assert np.array_equal(cache.state(plan.final, h), ref.traj[(cu[b] + n - 1, h)])
+            written.add((plan.final, h))
+            if plan.boundary > 0 and plan.boundary_len < n:
+                assert np.array_equal(cache.state(plan.boundary, h),
+                                      ref.traj[(cu[b] + plan.boundary_len - 1, h)])
+                written.add((plan.boundary, h))
+    assert set(cache.written) == written               # nothing else, not the sources
+
+
+def test_blocks_all_at_source_is_the_plain_commit():
+    wl, _, nc, bs = _align_case(seed=22)
+    table = np.repeat(wl.state_indices.numpy()[:, None], 6, axis=1)
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    acc = wl.steps[0].num_accepted.numpy()
+    a, p = oracle_cache(wl), oracle_cache(wl)
+    O.verify(layer, a, step)
+    O.verify(layer, p, step)
+    assert O.commit_align(layer, a, step, acc, table, nc, bs) == []
+    assert O.commit(layer, p, step, acc) == []
+    assert set(a.written) == set(p.written)
+    for key in p.written:
+        assert np.array_equal(a.written[key], p.written[key])
+
+
+def test_conv_windows_follow_the_accepted_sequence():
+    rng = np.random.default_rng(30)
+    Q, hist, bs, width_bt = 4, 3, 4, 5
+    B, S, C = 6, 60, 3
+    slots = np.arange(1, B + 1)
+    table = np.arange(20, 20 + B * width_bt).reshape(B, width_bt)
+    nc = rng.integers(0, bs * (width_bt - 1), size=B)
+    acc = rng.integers(1, Q + 1, size=B)
+    cu = np.arange(0, Q * (B + 1), Q)
+    pool = rng.integers(-10**6, 10**6, size=(S, C, hist + Q - 1)).astype(np.int64)
+    seqs = {}
+    for s in slots:
+        hst = rng.integers(0, 10**6, size=(C, hist))
+        x = rng.integers(0, 10**6, size=(C, Q))
+        pool[s] = np.concatenate([hst[:, 1:], x], axis=1)
+        seqs[int(s)] = (hst, x)
+    out, issues = O.conv_compact_align(pool, cu, slots, acc, Q, table, nc, bs)
+    assert issues == []
+    for b, s in enumerate(slots):
+        hst, x = seqs[int(s)]
+        n = int(acc[b])
+        plan = O.align_plan(n, int(nc[b]), table[b], bs)
+        for c in range(C):
+            seq = list(hst[c]) + list(x[c])
+            assert list(out[plan.final, c, :hist]) == seq[:hist + n][-hist:]
+            if plan.boundary > 0 and plan.boundary != plan.final:
+                assert list(out[plan.boundary, c, :hist]) == seq[:hist + plan.boundary_len][-hist:]
+        # the source slot keeps its post-verify layout (it is neither block)
+        assert np.array_equal(out[s], pool[s])
+
+
+def test_conv_align_with_blocks_at_source_is_the_plain_compaction():
+    rng = np.random.default_rng(31)
+    Q, B, S = 4, 7, 12
+    pool = rng.normal(size=(S, 5, 6))
+    slots = np.array([1, 2, 0, 4, 5, 6, 7])
+    cu = np.concatenate([[0], np.cumsum(rng.integers(0, Q + 1, size=B))])
+    acc = rng.integers(-1, Q + 2, size=B)
+    table = np.repeat(slots[:, None], 4, axis=1)
+    nc = rng.integers(0, 12, size=B)
+    a, ia = O.conv_compact_align(pool, cu, slots, acc, Q, table, nc, 4)
+    p, ip = O.conv_compact(pool, cu, slots, acc, Q)
+    assert ia == ip == []
+    assert np.array_equal(a, p)
+
+
+def test_invalid_blocks_are_reported():
+    wl, table, nc, bs = _align_case(seed=23)
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)
+    acc = np.full(8, 2)
+    table = table.copy()
+    table[0, :] = 999                          # final block beyond the pool
+    nc = nc.copy()
+    nc[1] = bs * 6 + bs - 1                    # boundary block beyond the table
+    issues = O.commit_align(layer, cache, step, acc, table, nc, bs)
+    assert [(i.row, i.reason) for i in issues][:2] == [(0, "slot"), (1, "block")]
