@@ -76,6 +76,9 @@ typedef enum kda_status {
  * into shared memory and returned early; its remaining rows were not
  * processed.  Not expected in normal operation. */
 #define KDA_ERR_WAIT_TIMEOUT 16
+/* align mode: request index outside the block table, negative num_computed,
+ * or a boundary block past the table's last column */
+#define KDA_ROW_BAD_BLOCK 32
 
 #define KDA_HEAD_DIM 128
 #define KDA_MAX_WINDOW 8
@@ -230,6 +233,68 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
                             const int32_t *cu_seqlens, const int32_t *state_indices,
                             int32_t B, const int32_t *num_accepted,
                             int32_t *error_word, void *stream);
+
+/*
+ * Align mode ([GLM] `_prepare_commit_plan_kernel` with a block table,
+ * `_replay_indices_kernel`, and the ALIGN_MODE branch of
+ * `_compact_conv_state_kernel`): states live in paged blocks of block_size
+ * tokens.  For a committing row with n accepted tokens, request q =
+ * request_indices[b] (or b) and c = num_computed[q] tokens before this step:
+ *   final block    = block_table[q][min((c + n - 1) / block_size, width - 1)];
+ *   boundary       = (c / block_size + 1) * block_size, the first block
+ *                    boundary after c; if c + n >= boundary the step reaches
+ *                    it: boundary_len = boundary - c tokens and
+ *                    boundary block = block_table[q][boundary / block_size - 1].
+ * The state after n tokens (and the conv window at column n - 1) goes to the
+ * final block; the state after boundary_len tokens (the conv window at column
+ * boundary_len - 1) goes to the boundary block, for the recurrent state only
+ * when boundary_len < n (otherwise the final block is that block).  Both are
+ * computed from the row's source slot state_indices[b] as it was before the
+ * call; the source is not written unless it is one of the blocks.  A row
+ * whose final block is <= 0 commits nothing.  num_accepted is indexed by
+ * request in align mode.  Rows must not write a block another row reads.
+ */
+typedef struct kda_align {
+    const int32_t *block_table;      /* [num_requests][>= width], row stride below */
+    int64_t block_table_stride;      /* elements between rows, >= width */
+    int32_t block_table_width;       /* columns >= 1 */
+    int32_t block_size;              /* tokens per block, >= window */
+    int32_t num_requests;            /* rows of block_table, num_computed, num_accepted */
+    int32_t reserved;                /* 0 */
+    const int32_t *num_computed;     /* [num_requests] */
+    const int32_t *request_indices;  /* [B], or NULL: request b is row b */
+} kda_align;
+
+/*
+ * kda_commit_align -- the eager commit in align mode: as kda_commit with
+ * pending == NULL, but the replayed states go to the final and boundary
+ * blocks above.  Rows with a request index outside [0, num_requests), a
+ * negative num_computed or a boundary block past the table are skipped and
+ * flagged KDA_ROW_BAD_BLOCK; a block >= num_slots flags KDA_ROW_BAD_SLOT.
+ * num_accepted: int32 [num_requests].
+ */
+kda_status kda_commit_align(const kda_config *cfg,
+                            const float *A_log, const float *g_bias,
+                            float *state_pool,
+                            const int32_t *cu_seqlens, const int32_t *state_indices,
+                            int32_t B,
+                            const int32_t *num_accepted,
+                            const int32_t *record_rows, const void *records,
+                            const kda_align *align,
+                            int32_t *error_word, void *stream);
+
+/*
+ * kda_conv_compact_align -- kda_conv_compact in align mode: the window at
+ * column n - 1 of the source slot goes to columns [0, history) of the final
+ * block, and the window at column boundary_len - 1 to the boundary block when
+ * the step reaches one; both windows are read before either is written.
+ * num_accepted: int32 [num_requests].
+ */
+kda_status kda_conv_compact_align(const kda_conv_config *cc, void *conv_state,
+                                  const int32_t *cu_seqlens, const int32_t *state_indices,
+                                  int32_t B, const int32_t *num_accepted,
+                                  const kda_align *align,
+                                  int32_t *error_word, void *stream);
 
 /* Name of a status code (static string). */
 const char *kda_status_string(kda_status status);

@@ -32,6 +32,7 @@ ROW_BAD_SLOT = 2
 ROW_BAD_RECORD = 4
 ROW_BAD_PENDING = 8
 ERR_WAIT_TIMEOUT = 16
+ROW_BAD_BLOCK = 32
 
 EXPORTED = (
     "kda_records_bytes",
@@ -39,6 +40,8 @@ EXPORTED = (
     "kda_commit",
     "kda_flush",
     "kda_conv_compact",
+    "kda_commit_align",
+    "kda_conv_compact_align",
     "kda_status_string",
     "kda_abi_version",
 )
@@ -86,6 +89,19 @@ class KdaConvConfig(ctypes.Structure):
 
 MAX_CONV_HISTORY = 16
 
+
+class KdaAlign(ctypes.Structure):
+    _fields_ = [
+        ("block_table", ctypes.c_void_p),
+        ("block_table_stride", ctypes.c_int64),
+        ("block_table_width", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_requests", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+        ("num_computed", ctypes.c_void_p),
+        ("request_indices", ctypes.c_void_p),
+    ]
+
 _lib_handle = None
 
 
@@ -115,6 +131,12 @@ def load_library():
     lib.kda_flush.argtypes = [cfgp] + [vp] * 4 + [i32] + [vp] * 5
     lib.kda_conv_compact.restype = ctypes.c_int
     lib.kda_conv_compact.argtypes = [ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] + [vp] * 3
+    alp = ctypes.POINTER(KdaAlign)
+    lib.kda_commit_align.restype = ctypes.c_int
+    lib.kda_commit_align.argtypes = [cfgp] + [vp] * 5 + [i32] + [vp] * 3 + [alp, vp, vp]
+    lib.kda_conv_compact_align.restype = ctypes.c_int
+    lib.kda_conv_compact_align.argtypes = ([ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] +
+                                           [vp, alp, vp, vp])
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_abi_version.restype = i32
@@ -349,3 +371,92 @@ def kda_conv_compact(conv_state, cu_seqlens, state_indices, num_accepted, *, win
                               _ptr(state_indices), B, _ptr(num_accepted), _ptr(error_word),
                               _stream_ptr(dev))
     _check("kda_conv_compact", st)
+
+
+def make_align(block_table, num_computed, block_size: int, request_indices=None) -> KdaAlign:
+    """``kda_align`` of an int32 block table [num_requests, width] (row stride
+    free, columns contiguous) and int32 num_computed [num_requests]."""
+    if block_table.dim() != 2 or block_table.stride(1) != 1:
+        raise ValueError("block_table must be [num_requests, width] with contiguous columns")
+    al = KdaAlign()
+    al.block_table = block_table.data_ptr()
+    al.block_table_stride = block_table.stride(0)
+    al.block_table_width = block_table.shape[1]
+    al.block_size = block_size
+    al.num_requests = block_table.shape[0]
+    al.reserved = 0
+    al.num_computed = num_computed.data_ptr()
+    al.request_indices = None if request_indices is None else request_indices.data_ptr()
+    return al
+
+
+def _check_align(block_table, num_computed, request_indices, dev):
+    i32 = torch.int32
+    _req(block_table, i32, "block_table", dev)
+    _req(num_computed, i32, "num_computed", dev)
+    _opt(request_indices, i32, "request_indices", dev)
+    if num_computed.shape[0] < block_table.shape[0] or not num_computed.is_contiguous():
+        raise ValueError("num_computed must be contiguous with one entry per request")
+    if request_indices is not None and not request_indices.is_contiguous():
+        raise ValueError("request_indices must be contiguous")
+
+
+def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepted, records,
+                     block_table, num_computed, *, block_size: int, window: int,
+                     record_slots: int, lower_bound=None, record_rows=None,
+                     request_indices=None, error_word=None) -> None:
+    """``kda_commit_align``: the eager commit writing the final and boundary
+    blocks of a paged state cache.  num_accepted, num_computed and the block
+    table rows are per request."""
+    dev = state_pool.device
+    f32, i32 = torch.float32, torch.int32
+    for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
+        _req(t, f32, name, dev)
+    _req(records, torch.bfloat16, "records", dev)
+    _req(cu_seqlens, i32, "cu_seqlens", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _req(num_accepted, i32, "num_accepted", dev)
+    _opt(record_rows, i32, "record_rows", dev)
+    _opt(error_word, i32, "error_word", dev)
+    _check_align(block_table, num_computed, request_indices, dev)
+    if state_pool.dim() != 4 or not state_pool.is_contiguous():
+        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    B = state_indices.shape[0]
+    if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < block_table.shape[0]:
+        raise ValueError("metadata sizes do not match the batch")
+    S, H = state_pool.shape[0], state_pool.shape[1]
+    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
+                      head_dim=state_pool.shape[-1])
+    al = make_align(block_table, num_computed, block_size, request_indices)
+    lib = load_library()
+    st = lib.kda_commit_align(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
+                              _ptr(cu_seqlens), _ptr(state_indices), B, _ptr(num_accepted),
+                              _ptr(record_rows), _ptr(records), ctypes.byref(al),
+                              _ptr(error_word), _stream_ptr(dev))
+    _check("kda_commit_align", st)
+
+
+def kda_conv_compact_align(conv_state, cu_seqlens, state_indices, num_accepted, block_table,
+                           num_computed, *, block_size: int, window: int,
+                           request_indices=None, error_word=None) -> None:
+    """``kda_conv_compact_align``: the conv windows of each committed row go
+    to its final and boundary blocks."""
+    dev = conv_state.device
+    i32 = torch.int32
+    if conv_state.element_size() not in (2, 4):
+        raise TypeError("conv_state elements must be 2 or 4 bytes")
+    _req(cu_seqlens, i32, "cu_seqlens", dev)
+    _req(state_indices, i32, "state_indices", dev)
+    _req(num_accepted, i32, "num_accepted", dev)
+    _opt(error_word, i32, "error_word", dev)
+    _check_align(block_table, num_computed, request_indices, dev)
+    B = state_indices.shape[0]
+    if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < block_table.shape[0]:
+        raise ValueError("metadata sizes do not match the batch")
+    cc = make_conv_config(conv_state, window)
+    al = make_align(block_table, num_computed, block_size, request_indices)
+    lib = load_library()
+    st = lib.kda_conv_compact_align(ctypes.byref(cc), _ptr(conv_state), _ptr(cu_seqlens),
+                                    _ptr(state_indices), B, _ptr(num_accepted),
+                                    ctypes.byref(al), _ptr(error_word), _stream_ptr(dev))
+    _check("kda_conv_compact_align", st)

@@ -19,6 +19,7 @@ SOURCES = [os.path.join(CSRC, "kda_kernels.cu"), os.path.join(CSRC, "kda_conv.cu
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "kda_device.cuh"),
     os.path.join(CSRC, "kda_async.cuh"),
+    os.path.join(CSRC, "kda_align.cuh"),
     os.path.join(ROOT, "include", "kda.h"),
 ]
 LIBRARY = os.path.join(PKG, "libkda.so")

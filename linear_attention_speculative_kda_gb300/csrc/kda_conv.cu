@@ -14,11 +14,14 @@
 //  - column-major (channel stride 1) with 16-byte rows: a thread moves 16
 //    bytes of channels through the window's columns;
 //  - anything else: a thread moves one channel, element by element.
+// Align mode (paged blocks) copies from the source slot into the final and
+// boundary blocks with the element-wise form.
 // The public contract is in include/kda.h (kda_conv_compact).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/kda.h"
+#include "kda_align.cuh"
 
 namespace kda_conv {
 
@@ -152,19 +155,88 @@ __global__ void __launch_bounds__(kThreads) column_kernel(const Params p) {
     }
 }
 
+// Align mode: per row, the window at column n - 1 of the source slot goes to
+// the final block and the window at column boundary_len - 1 to the boundary
+// block (when the step reaches one), both read before either is written.
+struct AlignArgs {
+    const int32_t *block_table, *num_computed, *request_indices;
+    long long bt_stride;
+    int bt_width, block_size, num_requests;
+};
+
+__device__ __forceinline__ void flag(const Params &p, int bits) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, bits);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) align_kernel(const Params p, const AlignArgs a) {
+    for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+        const int len = p.cu[b + 1] - p.cu[b];
+        const int slot = p.slots[b];
+        if (len < 0 || len > p.Q) {
+            flag(p, KDA_ROW_BAD_LENGTH);
+            continue;
+        }
+        if (slot >= p.S) {
+            flag(p, KDA_ROW_BAD_SLOT);
+            continue;
+        }
+        const int req = a.request_indices != nullptr ? a.request_indices[b] : b;
+        if (req < 0 || req >= a.num_requests) {
+            flag(p, KDA_ROW_BAD_BLOCK);
+            continue;
+        }
+        const int n = min(max(p.acc[req], 0), min(len, p.Q));
+        if (slot <= 0 || n <= 0) continue;
+        const kda_blocks::Blocks bl =
+            kda_blocks::plan(a.block_table + (long long)req * a.bt_stride, a.bt_width,
+                             a.block_size, a.num_computed[req], n);
+        if (bl.bad) {
+            flag(p, KDA_ROW_BAD_BLOCK);
+            continue;
+        }
+        if (bl.final_block >= p.S || bl.boundary >= p.S) {
+            flag(p, KDA_ROW_BAD_SLOT);
+            continue;
+        }
+        if (bl.final_block <= 0) continue;
+        T *base = reinterpret_cast<T *>(p.conv);
+        const long long src = (long long)slot * p.stride_slot;
+        const long long fin = (long long)bl.final_block * p.stride_slot;
+        const long long bnd = (long long)bl.boundary * p.stride_slot;
+        for (int d = blockIdx.x * kThreads + threadIdx.x; d < p.C; d += gridDim.x * kThreads) {
+            const long long ch = (long long)d * p.stride_dim;
+            T wf[KDA_MAX_CONV_HISTORY], wb[KDA_MAX_CONV_HISTORY];
+#pragma unroll
+            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h) {
+                if (h < p.hist) {
+                    wf[h] = base[src + ch + (long long)(n - 1 + h) * p.stride_col];
+                    if (bl.boundary > 0)
+                        wb[h] = base[src + ch + (long long)(bl.boundary_len - 1 + h) * p.stride_col];
+                }
+            }
+            if (bl.boundary > 0) {
+#pragma unroll
+                for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
+                    if (h < p.hist) base[bnd + ch + (long long)h * p.stride_col] = wb[h];
+            }
+#pragma unroll
+            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
+                if (h < p.hist) base[fin + ch + (long long)h * p.stride_col] = wf[h];
+        }
+    }
+}
+
 bool aligned(const void *ptr, uintptr_t bytes) {
     return (reinterpret_cast<uintptr_t>(ptr) & (bytes - 1)) == 0;
 }
 
-}  // namespace kda_conv
-
-extern "C" {
-
-kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
-                            const int32_t *cu_seqlens, const int32_t *state_indices,
-                            int32_t B, const int32_t *num_accepted,
-                            int32_t *error_word, void *stream) {
-    using namespace kda_conv;
+// Checks shared by both entry points; fills p.  KDA_OK with p.B == 0 means
+// there is nothing to launch.
+kda_status conv_params(const kda_conv_config *cc, void *conv_state, const int32_t *cu_seqlens,
+                       const int32_t *state_indices, int32_t B, const int32_t *num_accepted,
+                       int32_t *error_word, Params &p) {
+    p.B = 0;
     if (cc == nullptr) return KDA_ERR_INVALID_ARG;
     if (cc->num_slots < 1 || cc->conv_dim < 1 || cc->window < 1 || cc->reserved != 0)
         return KDA_ERR_INVALID_ARG;
@@ -184,7 +256,6 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
         (error_word != nullptr && !aligned(error_word, 4)))
         return KDA_ERR_INVALID_ARG;
 
-    Params p;
     p.conv = static_cast<unsigned char *>(conv_state);
     p.stride_slot = cc->stride_slot;
     p.stride_dim = cc->stride_dim;
@@ -199,6 +270,22 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
     p.acc = num_accepted;
     p.err = error_word;
     p.elem_bytes = cc->elem_bytes;
+    return KDA_OK;
+}
+
+}  // namespace kda_conv
+
+extern "C" {
+
+kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
+                            const int32_t *cu_seqlens, const int32_t *state_indices,
+                            int32_t B, const int32_t *num_accepted,
+                            int32_t *error_word, void *stream) {
+    using namespace kda_conv;
+    Params p;
+    const kda_status status = conv_params(cc, conv_state, cu_seqlens, state_indices, B,
+                                          num_accepted, error_word, p);
+    if (status != KDA_OK || p.B == 0) return status;
     const int rows = B < kMaxRowsPerGrid ? B : kMaxRowsPerGrid;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const long long eb = cc->elem_bytes;
@@ -227,6 +314,41 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
         else
             compact_kernel<uint32_t><<<grid, kThreads, 0, st>>>(p);
     }
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_conv_compact_align(const kda_conv_config *cc, void *conv_state,
+                                  const int32_t *cu_seqlens, const int32_t *state_indices,
+                                  int32_t B, const int32_t *num_accepted, const kda_align *align,
+                                  int32_t *error_word, void *stream) {
+    using namespace kda_conv;
+    Params p;
+    const kda_status st = conv_params(cc, conv_state, cu_seqlens, state_indices, B,
+                                      num_accepted, error_word, p);
+    if (st != KDA_OK || p.B == 0) return st;
+    if (align == nullptr || align->reserved != 0 || !align->block_table || !align->num_computed)
+        return KDA_ERR_INVALID_ARG;
+    if (align->block_table_width < 1 || align->block_table_stride < align->block_table_width ||
+        align->num_requests < 1 || align->block_size < cc->window)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned(align->block_table, 4) || !aligned(align->num_computed, 4) ||
+        (align->request_indices != nullptr && !aligned(align->request_indices, 4)))
+        return KDA_ERR_INVALID_ARG;
+    AlignArgs a;
+    a.block_table = align->block_table;
+    a.num_computed = align->num_computed;
+    a.request_indices = align->request_indices;
+    a.bt_stride = align->block_table_stride;
+    a.bt_width = align->block_table_width;
+    a.block_size = align->block_size;
+    a.num_requests = align->num_requests;
+    const int rows = B < kMaxRowsPerGrid ? B : kMaxRowsPerGrid;
+    const dim3 grid((cc->conv_dim + kThreads - 1) / kThreads, rows);
+    cudaStream_t stv = static_cast<cudaStream_t>(stream);
+    if (cc->elem_bytes == 2)
+        align_kernel<uint16_t><<<grid, kThreads, 0, stv>>>(p, a);
+    else
+        align_kernel<uint32_t><<<grid, kThreads, 0, stv>>>(p, a);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -39,6 +39,7 @@ constexpr int kBadSlot = 2;
 constexpr int kBadRecord = 4;
 constexpr int kBadPending = 8;
 constexpr int kErrWaitTimeout = 16;
+constexpr int kBadBlock = 32;
 
 // Everything a launch needs; passed by value as the kernel parameter.
 struct Params {
@@ -59,6 +60,10 @@ struct Params {
     __nv_bfloat16 *out;
     float *traj;
     int *err;
+    // align-mode commit (block_table == nullptr: off)
+    const int *block_table, *num_computed, *request_indices;
+    long long bt_stride;
+    int bt_width, block_size, num_requests;
 };
 
 // ---------------------------------------------------------------- helpers --

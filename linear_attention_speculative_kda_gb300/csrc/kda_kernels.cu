@@ -15,6 +15,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include "kda_align.cuh"
 #include "kda_async.cuh"
 #include "kda_device.cuh"
 #include "../../include/kda.h"
@@ -26,7 +27,7 @@ static_assert(kD == KDA_HEAD_DIM, "head dim mismatch");
 static_assert(kMaxQ == KDA_MAX_WINDOW, "window mismatch");
 static_assert(kBadLength == KDA_ROW_BAD_LENGTH && kBadSlot == KDA_ROW_BAD_SLOT &&
                   kBadRecord == KDA_ROW_BAD_RECORD && kBadPending == KDA_ROW_BAD_PENDING &&
-                  kErrWaitTimeout == KDA_ERR_WAIT_TIMEOUT,
+                  kErrWaitTimeout == KDA_ERR_WAIT_TIMEOUT && kBadBlock == KDA_ROW_BAD_BLOCK,
               "error-word bits mismatch");
 
 // Row metadata shared by all kernels: token range, slot and record slot,
@@ -60,14 +61,33 @@ __device__ __forceinline__ __nv_bfloat16 *record_base(const Params &p, int r, in
 // A work item is one (row, head) tile with something to do.  Mode decides
 // what: the verify runs `p` folded (pending) record tokens then `T` new
 // tokens; the commit and the flush replay `p` record tokens.  Every mode
-// stores the state when p > 0.
+// stores the state after the p-th token, to slot `dst` (the row's own slot,
+// or the final block of an align-mode commit); an align-mode commit also
+// stores the state after `mid_len` tokens to block `mid` (0: none).
 
 enum class Mode { kVerify, kCommit, kFlush };
 
 struct Work {
     int tile;  // -1: none
     int head, slot, r, bos, T, p;
+    int dst, mid, mid_len;
 };
+
+// Align-mode targets of a committing row of request `req` (the plan is in
+// kda_align.cuh): the final block, and the boundary block when the boundary
+// comes before the last token (a boundary at the last token is the final
+// block itself).  Returns the error bits; w.dst = 0 when the row commits
+// nothing.
+__device__ __forceinline__ int align_targets(const Params &p, int req, int n, Work &w) {
+    const kda_blocks::Blocks bl = kda_blocks::plan(p.block_table + (long long)req * p.bt_stride,
+                                                 p.bt_width, p.block_size, p.num_computed[req], n);
+    if (bl.bad) return kBadBlock;
+    if (bl.final_block >= p.S || bl.boundary >= p.S) return kBadSlot;
+    w.dst = bl.final_block > 0 ? bl.final_block : 0;
+    w.mid = (bl.boundary > 0 && bl.boundary_len < n) ? bl.boundary : 0;
+    w.mid_len = w.mid > 0 ? bl.boundary_len : 0;
+    return 0;
+}
 
 // Plan one tile: row checks, the commit plan (n = clamp(accepted, 0,
 // min(T, Q)), valid iff slot > 0, n > 0, r >= 0), the deferred commit's
@@ -96,8 +116,29 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         T = row.T;
         if (T == 0 && fold == 0) return false;
     } else if constexpr (kMode == Mode::kCommit) {
-        const int n = min(max(p.num_accepted[b], 0), min(row.T, p.Q));
-        const bool valid = row.slot > 0 && n > 0 && row.r >= 0;
+        // align mode reads the accepted count, num_computed and the block
+        // table of the row's request
+        int req = b;
+        if (p.block_table != nullptr) {
+            if (p.request_indices != nullptr) req = p.request_indices[b];
+            if (req < 0 || req >= p.num_requests) {
+                if (head == 0) flag_error(p.err, kBadBlock);
+                return false;
+            }
+        }
+        const int n = min(max(p.num_accepted[req], 0), min(row.T, p.Q));
+        bool valid = row.slot > 0 && n > 0 && row.r >= 0;
+        w.dst = row.slot;
+        w.mid = 0;
+        w.mid_len = 0;
+        if (p.block_table != nullptr && valid) {
+            const int bad_align = align_targets(p, req, n, w);
+            if (bad_align) {
+                if (head == 0) flag_error(p.err, bad_align);
+                return false;
+            }
+            valid = w.dst > 0;
+        }
         if (p.pending_out != nullptr) {
             const bool now = p.eager != nullptr && p.eager[b] != 0;
             if (head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
@@ -122,6 +163,11 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
     w.bos = row.bos;
     w.T = T;
     w.p = fold;
+    if constexpr (kMode != Mode::kCommit) {
+        w.dst = row.slot;
+        w.mid = 0;
+        w.mid_len = 0;
+    }
     return true;
 }
 
@@ -164,7 +210,8 @@ __device__ __forceinline__ void reg_dealloc() {
 }
 
 struct ItemInfo {
-    int tile, slot, head, bos, T, p, end, pad;
+    int tile, slot, head, bos, T, p, end;
+    int dst, mid, mid_len, pad0, pad1;
 };
 
 struct WorkList {
@@ -173,6 +220,9 @@ struct WorkList {
     int r[kPlanSize];
     int bos[kPlanSize];
     int tp[kPlanSize];   // T | p << 8
+    int dst[kPlanSize];
+    int mid[kPlanSize];  // boundary block, or 0
+    int mid_len[kPlanSize];
     int warp_count[kProducerWarps];
     int count;
     int pad;
@@ -288,6 +338,9 @@ __device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles
         list.r[pos] = w.r;
         list.bos[pos] = w.bos;
         list.tp[pos] = w.T | (w.p << 8);
+        list.dst[pos] = w.dst;
+        list.mid[pos] = w.mid;
+        list.mid_len[pos] = w.mid_len;
     }
     producer_sync();
     return total;
@@ -319,6 +372,9 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
     w.bos = list.bos[i];
     w.T = list.tp[i] & 0xff;
     w.p = list.tp[i] >> 8;
+    w.dst = list.dst[i];
+    w.mid = list.mid[i];
+    w.mid_len = list.mid_len[i];
     return w;
 }
 
@@ -486,6 +542,9 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             it.T = cur.T;
             it.p = cur.p;
             it.end = 0;
+            it.dst = cur.dst;
+            it.mid = cur.mid;
+            it.mid_len = cur.mid_len;
         }
         producer_sync();  // all token vectors and the item info written
         if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
@@ -527,9 +586,12 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         load_tile(h, staging, L);
         mbar_arrive(&sy.empty_state[c]);
         const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
-        float *tile = p.pool + ((size_t)it.slot * p.H + it.head) * (size_t)(kD * kD);
-        for (int u = 0; u < it.p; ++u) token_plain(h, tv, u, L);
-        if (it.p > 0) store_tile(h, tile, L);
+        for (int u = 0; u < it.p; ++u) {
+            token_plain(h, tv, u, L);
+            if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
+                store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD), L);
+        }
+        if (it.p > 0) store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
         if constexpr (kMode == Mode::kVerify) {
             for (int t = 0; t < it.T; ++t) {
                 const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
@@ -666,6 +728,26 @@ kda_status launch_step(const Params &p, bool bounded, bool fold, cudaStream_t st
     return finish_launch();
 }
 
+// Host checks of an align description; fills the Params fields.
+kda_status set_align(const kda_align *al, int window, Params &p) {
+    if (al == nullptr || al->reserved != 0) return KDA_ERR_INVALID_ARG;
+    if (!al->block_table || !al->num_computed) return KDA_ERR_INVALID_ARG;
+    if (al->block_table_width < 1 || al->block_table_stride < al->block_table_width ||
+        al->num_requests < 1 || al->block_size < window)
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned(al->block_table, 4) || !aligned(al->num_computed, 4) ||
+        (al->request_indices != nullptr && !aligned(al->request_indices, 4)))
+        return KDA_ERR_INVALID_ARG;
+    p.block_table = al->block_table;
+    p.bt_stride = al->block_table_stride;
+    p.bt_width = al->block_table_width;
+    p.block_size = al->block_size;
+    p.num_requests = al->num_requests;
+    p.num_computed = al->num_computed;
+    p.request_indices = al->request_indices;
+    return KDA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -748,6 +830,38 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     p.records = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(records));
     p.pending_out = pending;
     p.eager = eager;
+    p.err = error_word;
+
+    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,
+                                           static_cast<cudaStream_t>(stream));
+}
+
+kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const float *g_bias,
+                            float *state_pool, const int32_t *cu_seqlens,
+                            const int32_t *state_indices, int32_t B,
+                            const int32_t *num_accepted, const int32_t *record_rows,
+                            const void *records, const kda_align *align,
+                            int32_t *error_word, void *stream) {
+    kda_status st = check_config(cfg);
+    if (st != KDA_OK) return st;
+    if (B < 0) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
+    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
+    if (st != KDA_OK) return st;
+    if (!cu_seqlens || !num_accepted) return KDA_ERR_INVALID_ARG;
+    if (!aligned(cu_seqlens, 4) || !aligned(num_accepted, 4)) return KDA_ERR_INVALID_ARG;
+
+    Params p = base_params(cfg, B);
+    st = set_align(align, cfg->window, p);
+    if (st != KDA_OK) return st;
+    p.A_log = A_log;
+    p.g_bias = g_bias;
+    p.pool = state_pool;
+    p.cu_seqlens = cu_seqlens;
+    p.state_indices = state_indices;
+    p.record_rows = record_rows;
+    p.num_accepted = num_accepted;
+    p.records = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(records));
     p.err = error_word;
 
     return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,

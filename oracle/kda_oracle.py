@@ -471,6 +471,8 @@ def _align_row(layer, cache_slots, T, slot, num_accepted, num_computed, block_ro
     n = commit_len(num_accepted, T, layer.window)
     if slot <= 0 or n <= 0:
         return None, None
+    if int(num_computed) < 0:
+        return None, "block"
     plan = align_plan(n, int(num_computed), block_row, block_size)
     if plan is None:
         return None, "block"
@@ -506,11 +508,15 @@ def commit_align(layer: Layer, cache: Cache, step: Step, num_accepted, block_tab
         if bad:
             return RowIssue(b, bad)
         req = b if request_indices is None else int(request_indices[b])
+        if req < 0 or req >= len(block_table):
+            return RowIssue(b, "block")
+        if r < 0:  # no records: nothing to replay
+            return None
         plan, bad = _align_row(layer, cache.num_slots, T, slot, num_accepted[req],
                                num_computed[req], block_table[req], block_size)
         if bad:
             return RowIssue(b, bad)
-        if plan is None or r < 0:
+        if plan is None:
             return None
         for h in heads:
             # both replays start from the checkpoint as it was before the commit
@@ -550,6 +556,9 @@ def conv_compact_align(conv, cu_seqlens, state_indices, num_accepted, window: in
             issues.append(RowIssue(b, "slot"))
             continue
         req = b if request_indices is None else int(request_indices[b])
+        if req < 0 or req >= len(block_table):
+            issues.append(RowIssue(b, "block"))
+            continue
         plan, bad = _align_row(layer, S, T, slot, num_accepted[req], num_computed[req],
                                block_table[req], block_size)
         if bad:

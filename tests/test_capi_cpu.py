@@ -135,3 +135,54 @@ def test_conv_compact_host_checks(lib):
     assert _conv(lib, cu=FAKE + 2) == api.KDA_ERR_INVALID_ARG
     # B == 0: nothing to do, and no pointer is looked at
     assert _conv(lib, B=0, conv=None, cu=None, slots=None, acc=None) == api.KDA_OK
+
+
+def _align(**kw):
+    base = dict(block_table=FAKE, block_table_stride=8, block_table_width=8, block_size=16,
+                num_requests=4, reserved=0, num_computed=FAKE, request_indices=None)
+    base.update(kw)
+    return api.KdaAlign(**base)
+
+
+def _commit_align(lib, al, cfg=None, B=3, **ptrs):
+    p = dict(a_log=FAKE, g_bias=FAKE, pool=FAKE, cu=FAKE, slots=FAKE, acc=FAKE, rr=None,
+             records=FAKE, err=None)
+    p.update(ptrs)
+    cfg = _cfg() if cfg is None else cfg
+    alp = None if al is None else ctypes.byref(al)
+    return lib.kda_commit_align(ctypes.byref(cfg), p["a_log"], p["g_bias"], p["pool"], p["cu"],
+                                p["slots"], B, p["acc"], p["rr"], p["records"], alp, p["err"],
+                                None)
+
+
+def test_commit_align_host_checks(lib):
+    assert _commit_align(lib, None) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(block_table=None)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(num_computed=None)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(block_size=3)) == api.KDA_ERR_INVALID_ARG   # < window 4
+    assert _commit_align(lib, _align(block_table_width=0)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(block_table_stride=4)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(num_requests=0)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(reserved=1)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(block_table=FAKE + 2)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(request_indices=FAKE + 1)) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(), acc=None) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(), cfg=_cfg(window=9)) == api.KDA_ERR_UNSUPPORTED
+    assert _commit_align(lib, _align(), B=-1) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, None, B=0) == api.KDA_OK
+
+
+def test_conv_compact_align_host_checks(lib):
+    cc = api.KdaConvConfig(num_slots=8, conv_dim=64, width=6, window=4, elem_bytes=2, reserved=0,
+                           stride_slot=64 * 6, stride_dim=6, stride_col=1)
+
+    def call(al, B=3, cc=cc):
+        alp = None if al is None else ctypes.byref(al)
+        return lib.kda_conv_compact_align(ctypes.byref(cc), FAKE, FAKE, FAKE, B, FAKE, alp, None,
+                                          None)
+
+    assert call(None) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(block_size=2)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(num_computed=None)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), B=-1) == api.KDA_ERR_INVALID_ARG
+    assert call(None, B=0) == api.KDA_OK

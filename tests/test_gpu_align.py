@@ -1,0 +1,176 @@
+"""GPU parity of the align-mode commit and conv compaction (paged blocks)
+against the oracle, and bit-exactness of the stored blocks against the GPU
+verify trajectory.  Tolerances as in test_gpu_parity: fp32 states normwise
+1e-5 per tile against the oracle; the stored states bit-identical to the
+trajectory the verify computed; conv windows bit-identical."""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_speculative_kda_gb300 import api
+from linear_attention_speculative_kda_gb300 import workloads as W
+from oracle import kda_oracle as O
+from tests.helpers import GpuRun, assert_state_close, oracle_cache, oracle_layer, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+WIDTH = 6
+
+
+def _case(Q, bounded=False, seed=40, B=8):
+    lens = [Q, Q, max(1, Q - 1), Q, 2 if Q >= 2 else 1, Q, Q, 1][:B]
+    sources = list(range(1, B + 1))
+    sources[3] = 0                                     # a null row
+    S = 1 + B + B * WIDTH
+    kw = dict(bounded=True, lower_bound=-5.0) if bounded else {}
+    wl = W.custom(B=B, H=2, Q=Q, lens=lens, S=S, seed=seed, slots=sources, **kw)
+    rng = np.random.default_rng(seed)
+    # request b owns blocks 1 + B + b*WIDTH .. ; a permuted request order
+    table = (1 + B + np.arange(B * WIDTH)).reshape(B, WIDTH).astype(np.int32)
+    bs = max(Q, 4)
+    num_computed = rng.integers(0, bs * (WIDTH - 1), size=B).astype(np.int32)
+    return wl, table, num_computed, bs
+
+
+def _run_align(g, wl, table, nc, bs, request_indices=None, acc=None):
+    d = g.dev
+    i32 = dict(dtype=torch.int32, device=d)
+    acc = g.steps[0]["num_accepted"] if acc is None else torch.tensor(acc, **i32)
+    api.kda_commit_align(g.A_log, g.g_bias, g.pool, g.cu, g.slots, acc, g.records,
+                         torch.tensor(table, **i32), torch.tensor(nc, **i32), block_size=bs,
+                         request_indices=None if request_indices is None
+                         else torch.tensor(request_indices, **i32),
+                         error_word=g.err, **g.kw())
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("Q,bounded", [(4, False), (8, False), (8, True), (1, False)])
+def test_commit_align_against_oracle_and_trajectory(Q, bounded):
+    wl, table, nc, bs = _case(Q, bounded, seed=40 + Q)
+    g = GpuRun(wl, with_traj=True)
+    g.verify()
+    torch.cuda.synchronize()
+    traj = g.traj.clone()
+    _run_align(g, wl, table, nc, bs)
+    assert int(g.err.item()) == 0
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)
+    acc = wl.steps[0].num_accepted.numpy()
+    assert O.commit_align(layer, cache, step, acc, table, nc, bs) == []
+    pool = g.pool.cpu().numpy()
+    cu = wl.cu_seqlens.numpy()
+    written = set(cache.written)
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].astype(np.float64), ref)
+    # bit-exact against the trajectory at the final and boundary tokens
+    tr = traj.cpu()
+    for b in range(wl.spec.B):
+        slot = int(wl.state_indices[b])
+        n = O.commit_len(acc[b], cu[b + 1] - cu[b], Q)
+        if slot <= 0 or n <= 0:
+            continue
+        plan = O.align_plan(n, int(nc[b]), table[b], bs)
+        for h in range(wl.spec.H):
+            assert torch.equal(g.pool[plan.final, h].cpu(), tr[cu[b] + n - 1, h])
+            if plan.boundary > 0 and plan.boundary_len < n:
+                assert torch.equal(g.pool[plan.boundary, h].cpu(),
+                                   tr[cu[b] + plan.boundary_len - 1, h])
+    # everything else, the sources included, is untouched
+    pool0 = g.pool0.cpu().numpy()
+    for slot in range(pool.shape[0]):
+        for h in range(wl.spec.H):
+            if (slot, h) not in written:
+                assert np.array_equal(pool[slot, h], pool0[slot, h])
+
+
+def test_blocks_at_source_equal_the_plain_commit():
+    wl, _, nc, bs = _case(4, seed=50)
+    table = np.repeat(wl.state_indices.numpy()[:, None], WIDTH, axis=1).astype(np.int32)
+    a, p = GpuRun(wl), GpuRun(wl)
+    a.verify()
+    p.verify()
+    _run_align(a, wl, table, nc, bs)
+    p.commit()
+    torch.cuda.synchronize()
+    assert int(a.err.item()) == 0 and int(p.err.item()) == 0
+    assert torch.equal(a.pool, p.pool)
+
+
+def test_request_indices_permute_the_tables():
+    wl, table, nc, bs = _case(4, seed=51)
+    B = wl.spec.B
+    perm = np.random.default_rng(1).permutation(B).astype(np.int32)
+    # request perm[b] holds row b's table, count and accepted tokens
+    table_p = np.zeros_like(table)
+    nc_p = np.zeros_like(nc)
+    acc = wl.steps[0].num_accepted.numpy()
+    acc_p = np.zeros_like(acc)
+    table_p[perm] = table
+    nc_p[perm] = nc
+    acc_p[perm] = acc
+    a, p = GpuRun(wl), GpuRun(wl)
+    a.verify()
+    p.verify()
+    _run_align(a, wl, table, nc, bs)
+    _run_align(p, wl, table_p, nc_p, bs, request_indices=perm, acc=acc_p.tolist())
+    assert int(a.err.item()) == 0 and int(p.err.item()) == 0
+    assert torch.equal(a.pool, p.pool)
+
+
+def test_bad_blocks_are_flagged_and_skipped():
+    wl, table, nc, bs = _case(4, seed=52)
+    table = table.copy()
+    nc = nc.copy()
+    S = wl.spec.S
+    table[0, :] = S + 5                      # final block past the pool
+    nc[1] = bs * WIDTH + bs - 1              # boundary block past the table
+    g = GpuRun(wl)
+    g.verify()
+    acc = np.full(wl.spec.B, 2, dtype=np.int32)
+    _run_align(g, wl, table, nc, bs, acc=acc.tolist())
+    assert int(g.err.item()) == (api.ROW_BAD_SLOT | api.ROW_BAD_BLOCK)
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)
+    issues = O.commit_align(layer, cache, step, acc, table, nc, bs)
+    assert {(i.row, i.reason) for i in issues} == {(0, "slot"), (1, "block")}
+    pool = g.pool.cpu().numpy()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].astype(np.float64), ref)
+
+
+@pytest.mark.parametrize("layout", ["dim_first", "col_first"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_conv_compact_align_bit_exact(layout, dtype):
+    rng = np.random.default_rng(60)
+    Q, B, C, bs = 4, 9, 200, 4
+    width_bt = 5
+    S = 1 + B + B * width_bt
+    conv_w = 3 + Q - 1
+    conv = W.conv_state(S, C, conv_w, dtype=dtype, seed=61, layout=layout)
+    lens = rng.integers(0, Q + 1, size=B)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    slots = np.arange(1, B + 1, dtype=np.int32)
+    slots[2] = 0
+    table = (1 + B + np.arange(B * width_bt)).reshape(B, width_bt).astype(np.int32)
+    nc = rng.integers(0, bs * (width_bt - 1), size=B).astype(np.int32)
+    acc = rng.integers(-1, Q + 2, size=B).astype(np.int32)
+    dev = torch.device("cuda:0")
+    if layout == "dim_first":
+        dconv = conv.to(dev)
+    else:
+        dconv = conv.transpose(1, 2).contiguous().to(dev).transpose(1, 2)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = lambda a: torch.tensor(a, dtype=torch.int32, device=dev)  # noqa: E731
+    api.kda_conv_compact_align(dconv, t(cu), t(slots), t(acc), t(table), t(nc), block_size=bs,
+                               window=Q, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bits = {torch.bfloat16: torch.int16, torch.float32: torch.int32}[dtype]
+    raw = conv.contiguous().view(bits).numpy()
+    want, issues = O.conv_compact_align(raw, cu, slots, acc, Q, table, nc, bs)
+    assert issues == []
+    got = dconv.cpu().contiguous().view(bits).numpy()
+    assert np.array_equal(got, want)
