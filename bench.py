@@ -515,6 +515,79 @@ def measure_conv_compact(wl: W.Workload, device, iters: int, warmup: int, peak: 
             "gbs": b / (us / 1e6) / 1e9, "frac": b / (us / 1e6) / 1e9 / peak}
 
 
+def align_commit_bytes(wl: W.Workload, table, num_computed, block_size: int, acc) -> int:
+    """Algorithmic bytes of one align-mode commit: every committing (row,
+    head) reads its checkpoint and n records and writes the final block, plus
+    the boundary block when the boundary comes before the last token."""
+    lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
+    slots = wl.state_indices.tolist()
+    total = 0
+    for b in range(wl.spec.B):
+        n = min(max(int(acc[b]), 0), lens[b], wl.spec.Q)
+        if slots[b] <= 0 or n <= 0:
+            continue
+        c = int(num_computed[b])
+        boundary = (c // block_size + 1) * block_size
+        mid = c + n >= boundary and boundary - c < n
+        total += 65536 + n * 770 + 65536 * (2 if mid else 1)
+    return total * wl.spec.H
+
+
+def measure_commit_align(wl: W.Workload, device, iters: int, warmup: int, peak: float):
+    """The align-mode commit on the workload's rows, timed alone: a pool with
+    the row checkpoints and two blocks per request (block size 16; each
+    request's num_computed drawn so that some steps cross a block boundary),
+    records from one verify of the first step."""
+    from linear_attention_speculative_kda_gb300 import api
+    sp = wl.spec
+    B, H, D = sp.B, sp.H, sp.D
+    width, bs = 2, 16
+    S = 1 + B + B * width
+    gen = torch.Generator().manual_seed(17)
+    i32 = dict(dtype=torch.int32, device=device)
+    pool = torch.empty((S, H, D, D), dtype=torch.float32, device=device).normal_(0.0, 0.05)
+    slots = torch.where(wl.state_indices > 0, torch.arange(1, B + 1, dtype=torch.int32),
+                        torch.zeros(B, dtype=torch.int32))
+    table = (1 + B + torch.arange(B * width, dtype=torch.int32)).reshape(B, width)
+    num_computed = torch.randint(0, bs, (B,), generator=gen, dtype=torch.int32)
+    st = wl.steps[0]
+    records = api.allocate_records(H, sp.Q, sp.record_slots, device)
+    out = torch.empty((wl.total_tokens, H, D), dtype=torch.bfloat16, device=device)
+    qkv, beta, g_raw = st.qkv.to(device), st.beta_buf.to(device), st.g_raw.to(device)
+    cu, dslots = wl.cu_seqlens.to(**i32), slots.to(**i32)
+    A_log, g_bias = wl.A_log.to(device), wl.g_bias.to(device)
+    rr = None if wl.record_rows is None else wl.record_rows.to(**i32)
+    kw = dict(window=sp.Q, record_slots=sp.record_slots,
+              lower_bound=sp.lower_bound if sp.bounded else None)
+    api.kda_verify(qkv[:, 0], qkv[:, 1], qkv[:, 2], g_raw, beta[:, :H], A_log, g_bias, pool, cu,
+                   dslots, records, out, record_rows=rr, **kw)
+    acc = st.num_accepted.to(**i32)
+    dtable, dnc = table.to(**i32), num_computed.to(**i32)
+    err = torch.zeros(1, **i32)
+
+    def launch():
+        api.kda_commit_align(A_log, g_bias, pool, cu, dslots, acc, records, dtable, dnc,
+                             block_size=bs, record_rows=rr, error_word=err, **kw)
+
+    for _ in range(warmup):
+        launch()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(iters):
+        launch()
+    stop.record()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the align commit")
+    us = start.elapsed_time(stop) * 1e3 / iters
+    b = align_commit_bytes(wl, table, num_computed.tolist(), bs, st.num_accepted.tolist())
+    del pool, records
+    return {"blocks_per_request": width, "block_size": bs, "launches": iters, "avg_us": us,
+            "bytes_per_launch": b, "gbs": b / (us / 1e6) / 1e9,
+            "frac": b / (us / 1e6) / 1e9 / peak}
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     device = torch.device("cuda", local)
@@ -601,6 +674,10 @@ def run_ours(args):
     conv = {lay: measure_conv_compact(wl, device, max(20, args.steps // 4), args.warmup, peak,
                                       layout=lay) for lay in ("dim_first", "col_first")}
 
+    # the align-mode (paged-block) commit on the same rows, timed on its own
+    del hio
+    align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, args.cpu_budget)
@@ -612,7 +689,7 @@ def run_ours(args):
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
             "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
-            "extras": {"conv_compact": conv}}
+            "extras": {"conv_compact": conv, "commit_align": align}}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:

@@ -338,9 +338,11 @@ __device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles
         list.r[pos] = w.r;
         list.bos[pos] = w.bos;
         list.tp[pos] = w.T | (w.p << 8);
-        list.dst[pos] = w.dst;
-        list.mid[pos] = w.mid;
-        list.mid_len[pos] = w.mid_len;
+        if constexpr (kMode == Mode::kCommit) {
+            list.dst[pos] = w.dst;
+            list.mid[pos] = w.mid;
+            list.mid_len[pos] = w.mid_len;
+        }
     }
     producer_sync();
     return total;
@@ -372,9 +374,15 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
     w.bos = list.bos[i];
     w.T = list.tp[i] & 0xff;
     w.p = list.tp[i] >> 8;
-    w.dst = list.dst[i];
-    w.mid = list.mid[i];
-    w.mid_len = list.mid_len[i];
+    if constexpr (kMode == Mode::kCommit) {
+        w.dst = list.dst[i];
+        w.mid = list.mid[i];
+        w.mid_len = list.mid_len[i];
+    } else {  // the other modes store to the row's own slot
+        w.dst = w.slot;
+        w.mid = 0;
+        w.mid_len = 0;
+    }
     return w;
 }
 
@@ -588,8 +596,11 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         for (int u = 0; u < it.p; ++u) {
             token_plain(h, tv, u, L);
-            if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
-                store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD), L);
+            if constexpr (kMode == Mode::kCommit) {
+                if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
+                    store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD),
+                               L);
+            }
         }
         if (it.p > 0) store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
         if constexpr (kMode == Mode::kVerify) {

@@ -152,3 +152,11 @@ def test_conv_compact_bytes_counts_committed_rows():
                   slots=[1, 2, 3, 0, 5, 6])
     acc = [2, 3, 0, 4, 9, -1]  # committed: rows 0 (n 2) and 4 (n clamped to 2)
     assert bench.conv_compact_bytes(wl, 768, 3, 2, acc) == 2 * 2 * 768 * 3 * 2
+
+
+def test_align_commit_bytes_by_rows():
+    wl = W.custom(B=4, H=2, Q=4, lens=[4, 4, 2, 4], S=10, seed=9, slots=[1, 2, 0, 3])
+    acc = [3, 4, 2, 0]            # row 2 is null, row 3 commits nothing
+    nc = [14, 0, 0, 0]            # row 0 reaches the boundary at 16 after 2 of 3 tokens
+    per_head = (65536 + 3 * 770 + 2 * 65536) + (65536 + 4 * 770 + 65536)
+    assert bench.align_commit_bytes(wl, None, nc, 16, acc) == 2 * per_head
