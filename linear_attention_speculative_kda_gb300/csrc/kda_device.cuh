@@ -166,18 +166,19 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 // One buffer of per-token vectors (fp32): slots [0, p) are folded (recorded)
 // tokens, [p, p + T) the new ones; q^ only for new tokens.
 struct TokView {
-    float *kh, *e, *v, *qh, *beta;
+    float *kh, *e, *v, *qh, *beta, *kq;
     __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q) {
         kh = reinterpret_cast<float *>(base);
         e = kh + slots * kD;
         v = e + slots * kD;
         qh = v + slots * kD;
         beta = qh + Q * kD;
+        kq = beta + ((slots + 3) / 4) * 4;  // k^ . q^ of each new token
     }
 };
 
 __host__ __device__ inline int tok_buffer_bytes(int slots, int Q) {
-    return (3 * slots + Q) * kD * 4 + ((slots * 4 + 15) / 16) * 16;
+    return (3 * slots + Q) * kD * 4 + ((slots + 3) / 4) * 16 + ((Q + 3) / 4) * 16;
 }
 
 // ------------------------------------------------------------ state tile --
@@ -232,6 +233,35 @@ __device__ __forceinline__ void row_partials(const Tile &h, const float *x, cons
     for (int i = 0; i < 8; ++i) part[i] = __fadd_rn(acc[i].x, acc[i].y);
 }
 
+// Row dot products with two vectors in one pass (each in the order of
+// row_partials, so the first is bit-identical to row_partials(h, x)).
+__device__ __forceinline__ void row_partials2(const Tile &h, const float *x, const float *y,
+                                              const Lane &L, float (&px)[8], float (&py)[8]) {
+    float2 ax[8], ay[8];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 xx = ld_cols(x, L, m);
+        const float4 yy = ld_cols(y, L, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (m == 0) {
+                ax[i] = mul2(h[i][0].x, h[i][0].y, xx.x, xx.y);
+                ay[i] = mul2(h[i][0].x, h[i][0].y, yy.x, yy.y);
+            } else {
+                ax[i] = fma2(h[i][m].x, h[i][m].y, xx.x, xx.y, ax[i]);
+                ay[i] = fma2(h[i][m].x, h[i][m].y, yy.x, yy.y, ay[i]);
+            }
+            ax[i] = fma2(h[i][m].z, h[i][m].w, xx.z, xx.w, ax[i]);
+            ay[i] = fma2(h[i][m].z, h[i][m].w, yy.z, yy.w, ay[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        px[i] = __fadd_rn(ax[i].x, ax[i].y);
+        py[i] = __fadd_rn(ay[i].x, ay[i].y);
+    }
+}
+
 // Sum the 8 row partials over the 8 lanes of the row group (lane bits 0..2)
 // by a transpose-reduce: after it, lane j holds the full sum of row j.
 __device__ __forceinline__ float reduce_rows(const float (&part)[8], int j) {
@@ -279,10 +309,8 @@ __device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int s
 
 // v' = beta (v - u) for the lane's row, shared with the row group, then the
 // rank-one update S <- S + v' k^T.
-__device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slot, float u,
-                                             const Lane &L) {
-    const float vr = tv.v[slot * kD + L.row(L.j)];
-    const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
+__device__ __forceinline__ void delta_update_vp(Tile &h, const TokView &tv, int slot, float vp,
+                                                const Lane &L) {
     const int base = L.lane & ~7;
     float vpi[8];
 #pragma unroll
@@ -302,6 +330,12 @@ __device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slo
     }
 }
 
+__device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slot, float u,
+                                             const Lane &L) {
+    const float vr = tv.v[slot * kD + L.row(L.j)];
+    delta_update_vp(h, tv, slot, __fmul_rn(tv.beta[slot], __fsub_rn(vr, u)), L);
+}
+
 // One token without output (commit replay, deferred fold, flush).
 __device__ __forceinline__ void token_plain(Tile &h, const TokView &tv, int slot, const Lane &L) {
     float part[8];
@@ -309,14 +343,31 @@ __device__ __forceinline__ void token_plain(Tile &h, const TokView &tv, int slot
     delta_update(h, tv, slot, reduce_rows(part, L.j), L);
 }
 
-// One token with output o = S q^ (after the update) to out_row (bf16).
+// One token with its output o = S' q^ (S' the state after the token) to
+// out_row (bf16), from the decayed state D = S diag(e) in one pass:
+// S' q^ = D q^ + v' (k^ . q^), so u = D k^ and D q^ share the pass and the
+// reduction.  The state update is the one token_plain does (same bits).
 __device__ __forceinline__ void token_out(Tile &h, const TokView &tv, int slot, int qslot,
                                           const Lane &L, __nv_bfloat16 *out_row) {
-    token_plain(h, tv, slot, L);
-    float part[8];
-    row_partials(h, tv.qh + qslot * kD, L, part);
-    const float o = reduce_rows(part, L.j);
-    out_row[L.row(L.j)] = __float2bfloat16_rn(o);
+    const float *e = tv.e + slot * kD;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const float4 ee = ld_cols(e, L, m);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float2 lo = mul2(h[i][m].x, h[i][m].y, ee.x, ee.y);
+            const float2 hi = mul2(h[i][m].z, h[i][m].w, ee.z, ee.w);
+            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+    }
+    float pu[8], po[8];
+    row_partials2(h, tv.kh + slot * kD, tv.qh + qslot * kD, L, pu, po);
+    const float u = reduce_rows(pu, L.j);
+    const float dq = reduce_rows(po, L.j);
+    const float vr = tv.v[slot * kD + L.row(L.j)];
+    const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
+    out_row[L.row(L.j)] = __float2bfloat16_rn(__fmaf_rn(vp, tv.kq[qslot], dq));
+    delta_update_vp(h, tv, slot, vp, L);
 }
 
 }  // namespace kda

@@ -472,12 +472,19 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
             sq = __fmaf_rn(q.y, q.y, sq);
             sq = __fmaf_rn(q.z, q.z, sq);
             sq = __fmaf_rn(q.w, q.w, sq);
+            float skq = __fmul_rn(k.x, q.x);
+            skq = __fmaf_rn(k.y, q.y, skq);
+            skq = __fmaf_rn(k.z, q.z, skq);
+            skq = __fmaf_rn(k.w, q.w, skq);
             const float iq = inv_l2(warp_allsum(sq));
+            const float dkq = warp_allsum(skq);
             *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
                 make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.y, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.z, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.w, iq), p.scale));
+            // k^ . q^ from the raw dot product and the two norms
+            if (lane == 0) tv.kq[t] = __fmul_rn(__fmul_rn(__fmul_rn(dkq, ik), iq), p.scale);
             uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
             dst[lane] = kb;
             dst[kRecV / 4 + lane] = vb;
