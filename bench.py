@@ -472,12 +472,38 @@ def conv_compact_bytes(wl: W.Workload, conv_dim: int, hist: int, elem_bytes: int
     return 2 * rows * conv_dim * hist * elem_bytes
 
 
+def time_launches(launch, iters: int, warmup: int):
+    """Average device time (us) of ``launch(k)`` for k in range(iters),
+    replayed from one CUDA graph so that the host's per-call cost does not
+    show in short launches.  Returns (us, how)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(warmup):
+            launch(k)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for k in range(iters):
+            launch(k)
+    graph.replay()
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    graph.replay()
+    stop.record()
+    torch.cuda.synchronize()
+    del graph
+    return start.elapsed_time(stop) * 1e3 / iters, "cuda graph"
+
+
 def measure_conv_compact(wl: W.Workload, device, iters: int, warmup: int, peak: float,
                          layout: str = "dim_first"):
     """The conv-state compaction of the workload's commit (bf16 pool
     [S, 3*H*D, history + Q - 1], channel-major or column-major), timed alone
-    with CUDA events.  Three pool copies in rotation keep each launch's pool
-    out of L2."""
+    from a CUDA graph replay.  Three pool copies in rotation keep each
+    launch's pool out of L2."""
     from linear_attention_speculative_kda_gb300 import api
     S, C, width = W.conv_shape(wl.spec)
 
@@ -495,21 +521,12 @@ def measure_conv_compact(wl: W.Workload, device, iters: int, warmup: int, peak: 
     def launch(k):
         api.kda_conv_compact(pools[k % 3], cu, slots, acc, window=wl.spec.Q, error_word=err)
 
-    for k in range(warmup):
-        launch(k)
-    torch.cuda.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for k in range(iters):
-        launch(k)
-    stop.record()
-    torch.cuda.synchronize()
+    us, how = time_launches(launch, iters, warmup)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the conv compaction")
-    us = start.elapsed_time(stop) * 1e3 / iters
     b = conv_compact_bytes(wl, C, width - wl.spec.Q + 1, 2, wl.steps[0].num_accepted.tolist())
     del pools
-    return {"shape": [S, C, width], "dtype": "bf16",
+    return {"shape": [S, C, width], "dtype": "bf16", "timing": how,
             "layout": "channel-major" if layout == "dim_first" else "column-major",
             "launches": iters, "avg_us": us, "bytes_per_launch": b,
             "gbs": b / (us / 1e6) / 1e9, "frac": b / (us / 1e6) / 1e9 / peak}
@@ -537,7 +554,8 @@ def measure_commit_align(wl: W.Workload, device, iters: int, warmup: int, peak: 
     """The align-mode commit on the workload's rows, timed alone: a pool with
     the row checkpoints and two blocks per request (block size 16; each
     request's num_computed drawn so that some steps cross a block boundary),
-    records from one verify of the first step."""
+    records from one verify of the first step; timed from a CUDA graph
+    replay."""
     from linear_attention_speculative_kda_gb300 import api
     sp = wl.spec
     B, H, D = sp.B, sp.H, sp.D
@@ -565,25 +583,17 @@ def measure_commit_align(wl: W.Workload, device, iters: int, warmup: int, peak: 
     dtable, dnc = table.to(**i32), num_computed.to(**i32)
     err = torch.zeros(1, **i32)
 
-    def launch():
+    def launch(_k):
         api.kda_commit_align(A_log, g_bias, pool, cu, dslots, acc, records, dtable, dnc,
                              block_size=bs, record_rows=rr, error_word=err, **kw)
 
-    for _ in range(warmup):
-        launch()
-    torch.cuda.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(iters):
-        launch()
-    stop.record()
-    torch.cuda.synchronize()
+    us, how = time_launches(launch, iters, warmup)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item())} in the align commit")
-    us = start.elapsed_time(stop) * 1e3 / iters
     b = align_commit_bytes(wl, table, num_computed.tolist(), bs, st.num_accepted.tolist())
     del pool, records
-    return {"blocks_per_request": width, "block_size": bs, "launches": iters, "avg_us": us,
+    return {"blocks_per_request": width, "block_size": bs, "timing": how, "launches": iters,
+            "avg_us": us,
             "bytes_per_launch": b, "gbs": b / (us / 1e6) / 1e9,
             "frac": b / (us / 1e6) / 1e9 / peak}
 
@@ -671,12 +681,16 @@ def run_ours(args):
            "d2h_bytes_per_step": hio.d2h, "ms_per_step": e_ms / args.steps}
 
     # the commit's conv-state compaction, a separate launch, timed on its own
-    conv = {lay: measure_conv_compact(wl, device, max(20, args.steps // 4), args.warmup, peak,
-                                      layout=lay) for lay in ("dim_first", "col_first")}
+    conv = None
+    if not args.no_extras:
+        conv = {lay: measure_conv_compact(wl, device, max(20, args.steps // 4), args.warmup,
+                                          peak, layout=lay) for lay in ("dim_first", "col_first")}
 
     # the align-mode (paged-block) commit on the same rows, timed on its own
     del hio
-    align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
+    align = None
+    if not args.no_extras:
+        align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -689,7 +703,8 @@ def run_ours(args):
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
             "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
-            "extras": {"conv_compact": conv, "commit_align": align}}
+            "extras": None if args.no_extras else {"conv_compact": conv,
+                                                   "commit_align": align}}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:
@@ -738,6 +753,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the separately timed conv compaction and align commit")
     ap.add_argument("--reference-rows", type=int, default=8)
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
