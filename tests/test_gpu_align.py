@@ -174,3 +174,56 @@ def test_conv_compact_align_bit_exact(layout, dtype):
     assert issues == []
     got = dconv.cpu().contiguous().view(bits).numpy()
     assert np.array_equal(got, want)
+
+
+def test_full_size_align_commit():
+    """deferred2's rows at full size (1024 requests x 16 heads) with two
+    blocks per request, as the benchmark runs the align commit: every stored
+    block equals the verify trajectory bit for bit, and a sample of tiles is
+    checked against the oracle."""
+    wl = W.generate("deferred2", pool=False)
+    sp = wl.spec
+    B, H, D, width, bs = sp.B, sp.H, sp.D, 2, 16
+    S = 1 + B + B * width
+    gen = torch.Generator().manual_seed(3)
+    pool_cpu = torch.randn((S, H, D, D), generator=gen) * 0.05
+    sources = torch.where(wl.state_indices > 0, torch.arange(1, B + 1, dtype=torch.int32),
+                          torch.zeros(B, dtype=torch.int32))
+    wl.pool = pool_cpu
+    wl.state_indices = sources
+    wl.spec = W.Spec(**{**sp.__dict__, "S": S})
+    table = (1 + B + np.arange(B * width)).reshape(B, width).astype(np.int32)
+    nc = torch.randint(0, bs, (B,), generator=gen, dtype=torch.int32).numpy()
+    g = GpuRun(wl, with_traj=True, sentinel=False)
+    g.verify()
+    torch.cuda.synchronize()
+    _run_align(g, wl, table, nc, bs)
+    assert int(g.err.item()) == 0
+    acc = wl.steps[0].num_accepted.numpy()
+    cu = wl.cu_seqlens.numpy()
+    fin_s, fin_t, mid_s, mid_t = [], [], [], []
+    for b in range(B):
+        n = O.commit_len(int(acc[b]), cu[b + 1] - cu[b], sp.Q)
+        if int(sources[b]) <= 0 or n <= 0:
+            continue
+        plan = O.align_plan(n, int(nc[b]), table[b], bs)
+        fin_s.append(plan.final)
+        fin_t.append(int(cu[b]) + n - 1)
+        if plan.boundary > 0 and plan.boundary_len < n:
+            mid_s.append(plan.boundary)
+            mid_t.append(int(cu[b]) + plan.boundary_len - 1)
+    assert fin_s and mid_s
+    dev = g.pool.device
+    assert torch.equal(g.pool[torch.tensor(fin_s, device=dev)], g.traj[torch.tensor(fin_t, device=dev)])
+    assert torch.equal(g.pool[torch.tensor(mid_s, device=dev)], g.traj[torch.tensor(mid_t, device=dev)])
+    # a sample against the oracle
+    rng = np.random.default_rng(0)
+    rows = sorted(rng.choice(B, size=16, replace=False).tolist())
+    heads = sorted(rng.choice(H, size=2, replace=False).tolist())
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step, rows=rows, heads=heads)
+    assert O.commit_align(layer, cache, step, acc, table, nc, bs, rows=rows, heads=heads) == []
+    assert cache.written
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(g.pool[slot, h].double().cpu().numpy(), ref)
