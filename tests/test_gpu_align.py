@@ -41,7 +41,7 @@ def _run_align(g, wl, table, nc, bs, request_indices=None, acc=None):
                          torch.tensor(table, **i32), torch.tensor(nc, **i32), block_size=bs,
                          request_indices=None if request_indices is None
                          else torch.tensor(request_indices, **i32),
-                         error_word=g.err, **g.kw())
+                         record_rows=g.record_rows, error_word=g.err, **g.kw())
     torch.cuda.synchronize()
 
 
