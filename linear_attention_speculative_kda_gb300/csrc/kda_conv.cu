@@ -133,8 +133,10 @@ __global__ void __launch_bounds__(kThreads) staged_kernel(const Params p, int ru
     }
 }
 
-// Column-major with 16-byte rows: thread i moves bytes [16 i, 16 i + 16) of
-// every window column of the row's slot.
+// Column-major with 16-byte rows: a thread moves kVec 16-byte pieces of
+// channels (kVec * kThreads apart) through the window's columns, all loads
+// before any store; kHist bounds the history.
+template <int kHist, int kVec>
 __global__ void __launch_bounds__(kThreads) column_kernel(const Params p) {
     const long long col_bytes = p.stride_col * p.elem_bytes;
     const int vecs = p.C * p.elem_bytes / 16;
@@ -142,15 +144,24 @@ __global__ void __launch_bounds__(kThreads) column_kernel(const Params p) {
         const int n = row_count(p, b);
         if (n <= 0) continue;
         unsigned char *slot_base = p.conv + (long long)p.slots[b] * p.stride_slot * p.elem_bytes;
-        for (int i = blockIdx.x * kThreads + threadIdx.x; i < vecs; i += gridDim.x * kThreads) {
-            uint4 w[KDA_MAX_CONV_HISTORY];
+        const uint4 *src = reinterpret_cast<const uint4 *>(slot_base + (n - 1) * col_bytes);
+        uint4 *dst = reinterpret_cast<uint4 *>(slot_base);
+        const long long col_vecs = col_bytes / 16;
+        for (int i0 = blockIdx.x * kThreads * kVec + threadIdx.x; i0 < vecs;
+             i0 += gridDim.x * kThreads * kVec) {
+            uint4 w[kVec][kHist];
 #pragma unroll
-            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
-                if (h < p.hist)
-                    w[h] = reinterpret_cast<const uint4 *>(slot_base + (n - 1 + h) * col_bytes)[i];
+            for (int v = 0; v < kVec; ++v)
 #pragma unroll
-            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
-                if (h < p.hist) reinterpret_cast<uint4 *>(slot_base + h * col_bytes)[i] = w[h];
+                for (int h = 0; h < kHist; ++h)
+                    if (h < p.hist && i0 + v * kThreads < vecs)
+                        w[v][h] = src[h * col_vecs + i0 + v * kThreads];
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+#pragma unroll
+                for (int h = 0; h < kHist; ++h)
+                    if (h < p.hist && i0 + v * kThreads < vecs)
+                        dst[h * col_vecs + i0 + v * kThreads] = w[v][h];
         }
     }
 }
@@ -305,8 +316,14 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
     } else if (slots16 && cc->stride_dim == 1 && ((long long)cc->conv_dim * eb) % 16 == 0 &&
                (cc->stride_col * eb) % 16 == 0) {
         const int vecs = (int)((long long)cc->conv_dim * eb / 16);
-        const dim3 grid((vecs + kThreads - 1) / kThreads, rows);
-        column_kernel<<<grid, kThreads, 0, st>>>(p);
+        if (p.hist <= 4) {
+            constexpr int kVec = 4;
+            const dim3 grid((vecs + kThreads * kVec - 1) / (kThreads * kVec), rows);
+            column_kernel<4, kVec><<<grid, kThreads, 0, st>>>(p);
+        } else {
+            const dim3 grid((vecs + kThreads - 1) / kThreads, rows);
+            column_kernel<KDA_MAX_CONV_HISTORY, 1><<<grid, kThreads, 0, st>>>(p);
+        }
     } else {
         const dim3 grid((cc->conv_dim + kThreads - 1) / kThreads, rows);
         if (cc->elem_bytes == 2)
