@@ -133,6 +133,77 @@ __global__ void __launch_bounds__(kThreads) staged_kernel(const Params p, int ru
     }
 }
 
+// Channel-major, dense, small units: a unit is the fewest whole channels
+// whose bytes make 16-byte pieces (at most 4 channels, 64 bytes).  A thread
+// loads kUnits units with 16-byte loads into its own slice of shared memory,
+// moves each channel's window there, and stores the units back: no barrier,
+// and every load is in flight before the first store.  Piece v of unit k of
+// thread t sits at 16 * ((4k + v) * kThreads + t), so a warp's 16-byte
+// accesses fall on distinct banks.
+constexpr int kUnitMaxBytes = 64;
+
+template <typename T, int kUnits>
+__global__ void __launch_bounds__(kThreads) unit_kernel(const Params p, int unit_chans) {
+    __shared__ __align__(16) unsigned char stage[kThreads * kUnits * kUnitMaxBytes];
+    const int W = (int)p.stride_dim;  // = width
+    const int unit_bytes = unit_chans * W * (int)sizeof(T);
+    const int uv = unit_bytes / 16;    // 16-byte pieces per unit, <= 4
+    const int units = p.C / unit_chans;
+    constexpr int kPieces = kUnitMaxBytes / 16;
+    for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+        const int n = row_count(p, b);
+        if (n <= 0) continue;
+        unsigned char *slot_base =
+            p.conv + (long long)p.slots[b] * p.stride_slot * (long long)sizeof(T);
+        for (int u0 = blockIdx.x * kThreads * kUnits + threadIdx.x; u0 < units;
+             u0 += gridDim.x * kThreads * kUnits) {
+            uint4 r[kUnits][kUnitMaxBytes / 16];
+#pragma unroll
+            for (int k = 0; k < kUnits; ++k) {
+                const int u = u0 + k * kThreads;
+                const uint4 *src = reinterpret_cast<const uint4 *>(slot_base + (long long)u * unit_bytes);
+#pragma unroll
+                for (int v = 0; v < kUnitMaxBytes / 16; ++v)
+                    if (u < units && v < uv) r[k][v] = src[v];
+            }
+            constexpr int kPer = 16 / (int)sizeof(T);  // elements per piece
+#pragma unroll
+            for (int k = 0; k < kUnits; ++k) {
+                uint4 *sv = reinterpret_cast<uint4 *>(stage) + (k * kPieces) * kThreads + threadIdx.x;
+#pragma unroll
+                for (int v = 0; v < kPieces; ++v)
+                    if (v < uv) sv[v * kThreads] = r[k][v];
+                // element e of the unit: piece e / kPer, slot e % kPer
+                T *se = reinterpret_cast<T *>(sv);
+                for (int c = 0; c < unit_chans; ++c) {
+                    T w[4];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int e = c * W + n - 1 + h;
+                        if (h < p.hist) w[h] = se[(e / kPer) * kThreads * kPer + e % kPer];
+                    }
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const int e = c * W + h;
+                        if (h < p.hist) se[(e / kPer) * kThreads * kPer + e % kPer] = w[h];
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < kPieces; ++v)
+                    if (v < uv) r[k][v] = sv[v * kThreads];
+            }
+#pragma unroll
+            for (int k = 0; k < kUnits; ++k) {
+                const int u = u0 + k * kThreads;
+                uint4 *dst = reinterpret_cast<uint4 *>(slot_base + (long long)u * unit_bytes);
+#pragma unroll
+                for (int v = 0; v < kUnitMaxBytes / 16; ++v)
+                    if (u < units && v < uv) dst[v] = r[k][v];
+            }
+        }
+    }
+}
+
 // Column-major with 16-byte rows: a thread moves kVec 16-byte pieces of
 // channels (kVec * kThreads apart) through the window's columns, all loads
 // before any store; kHist bounds the history.
@@ -306,7 +377,17 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
     long long unit = 1;
     while ((unit * chan_bytes) % 16 != 0) ++unit;
     if (slots16 && cc->stride_col == 1 && cc->stride_dim == cc->width &&
-        cc->conv_dim % unit == 0 && unit * chan_bytes <= kStageBytes) {
+        cc->conv_dim % unit == 0 && unit <= 4 && unit * chan_bytes <= kUnitMaxBytes &&
+        p.hist <= 4) {
+        constexpr int kUnits = 2;
+        const int units = (int)(cc->conv_dim / unit);
+        const dim3 grid((units + kThreads * kUnits - 1) / (kThreads * kUnits), rows);
+        if (cc->elem_bytes == 2)
+            unit_kernel<uint16_t, kUnits><<<grid, kThreads, 0, st>>>(p, (int)unit);
+        else
+            unit_kernel<uint32_t, kUnits><<<grid, kThreads, 0, st>>>(p, (int)unit);
+    } else if (slots16 && cc->stride_col == 1 && cc->stride_dim == cc->width &&
+               cc->conv_dim % unit == 0 && unit * chan_bytes <= kStageBytes) {
         const int run = (int)(unit * (kStageBytes / (unit * chan_bytes)));
         const dim3 grid((cc->conv_dim + run - 1) / run, rows);
         if (cc->elem_bytes == 2)
