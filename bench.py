@@ -99,13 +99,20 @@ def hbm_peak():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# the sources of the verify / commit kernel (the conv kernel has its own file)
+STEP_SOURCES = ("kda_align.cuh", "kda_async.cuh", "kda_device.cuh", "kda_kernels.cu")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the verify / commit kernel's sources: a profile taken on other
+    sources no longer describes the kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_speculative_kda_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if not name.endswith((".cu", ".cuh")):
+    for name in STEP_SOURCES:
+        path = os.path.join(csrc, name)
+        if not os.path.exists(path):
             continue
-        with open(os.path.join(csrc, name), "rb") as fh:
+        with open(path, "rb") as fh:
             h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]

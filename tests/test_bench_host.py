@@ -137,13 +137,16 @@ def test_profiled_traffic_requires_current_sources(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     csrc = tmp_path / "linear_attention_speculative_kda_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    (csrc / "a.cu").write_text("kernel v1")
+    (csrc / "kda_kernels.cu").write_text("kernel v1")
+    (csrc / "kda_conv.cu").write_text("conv v1")
     h = bench.kernel_source_hash()
     (tmp_path / "profiles" / "ncu_w.md").write_text(
         f"source_hash: {h}\ntraffic[verify]: 1234\n")
     assert bench.profiled_traffic("verify", "w") == 1234.0
     assert bench.profiled_traffic("commit", "w") is None
-    (csrc / "a.cu").write_text("kernel v2")
+    (csrc / "kda_conv.cu").write_text("conv v2")   # not the step kernel's source
+    assert bench.profiled_traffic("verify", "w") == 1234.0
+    (csrc / "kda_kernels.cu").write_text("kernel v2")
     assert bench.profiled_traffic("verify", "w") is None
 
 
