@@ -705,7 +705,7 @@ def run_ours(args):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32 state, bf16 activations",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded)", "config": workload_config(wl, world),
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
