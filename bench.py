@@ -464,6 +464,7 @@ def workload_config(wl: W.Workload, world: int):
             "gate": f"bounded lb={sp.lower_bound}" if sp.bounded else "softplus",
             "decode_steps_per_step": sp.steps, "ranks": world,
             "tokens_per_decode_step": wl.total_tokens,
+            "state": "f32", "activations": "bf16",
             "l2": "inputs larger than L2 (state pool %.2f GB)" % (
                 wl.pool.numel() * 4 / 1e9)}
 
