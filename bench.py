@@ -465,8 +465,17 @@ def workload_config(wl: W.Workload, world: int):
             "decode_steps_per_step": sp.steps, "ranks": world,
             "tokens_per_decode_step": wl.total_tokens,
             "state": "f32", "activations": "bf16",
-            "l2": "inputs larger than L2 (state pool %.2f GB)" % (
-                wl.pool.numel() * 4 / 1e9)}
+            "l2": l2_note(wl.pool.numel() * 4)}
+
+
+L2_BYTES = 126 * 2**20   # GB300 L2
+
+
+def l2_note(pool_bytes: int) -> str:
+    if pool_bytes > L2_BYTES:
+        return "inputs larger than L2 (state pool %.2f GB)" % (pool_bytes / 1e9)
+    return "state pool %.3f GB fits in L2 and is not flushed (latency-bound small case)" % (
+        pool_bytes / 1e9)
 
 
 def conv_compact_bytes(wl: W.Workload, conv_dim: int, hist: int, elem_bytes: int, acc) -> int:

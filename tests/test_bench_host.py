@@ -163,3 +163,8 @@ def test_align_commit_bytes_by_rows():
     nc = [14, 0, 0, 0]            # row 0 reaches the boundary at 16 after 2 of 3 tokens
     per_head = (65536 + 3 * 770 + 2 * 65536) + (65536 + 4 * 770 + 65536)
     assert bench.align_commit_bytes(wl, None, nc, 16, acc) == 2 * per_head
+
+
+def test_l2_note_is_truthful():
+    assert bench.l2_note(2 * 10**9).startswith("inputs larger than L2")
+    assert "fits in L2" in bench.l2_note(2 * 2**20)
