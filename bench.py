@@ -468,7 +468,7 @@ def workload_config(wl: W.Workload, world: int):
             "l2": l2_note(wl.pool.numel() * 4)}
 
 
-L2_BYTES = 126 * 2**20   # GB300 L2
+L2_BYTES = 129 * 10**6   # GB300 L2
 
 
 def l2_note(pool_bytes: int) -> str:
