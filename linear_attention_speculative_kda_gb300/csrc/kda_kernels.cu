@@ -521,8 +521,9 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     while (cur.tile >= 0) {
         const int c = n & 1;
         const int use_c = n >> 1;
-        // checkpoint of `cur` into consumer c's staging buffer
-        if (pt == 0) {
+        // checkpoint of `cur` into consumer c's staging buffer, issued by the
+        // last warp, which has the fewest tokens to prepare
+        if (pt == kProducerThreads - 32) {
             if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
             if (ok)
                 issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
