@@ -642,6 +642,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
         fence_mbar_init();
     }
     __syncthreads();
+    // let the next launch start its set-up, and wait for the previous one
+    // before any global memory is touched
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Register split: the launch gives every thread kLaunchRegs; the producer
     // warpgroup hands registers back and the consumers take them, so that
     // 2 * 128 * kConsumerRegs + 128 * kProducerRegs == 384 * kLaunchRegs.
@@ -743,7 +747,21 @@ kda_status launch_step(const Params &p, bool bounded, bool fold, cudaStream_t st
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared) != cudaSuccess)
         return KDA_ERR_CUDA;
-    kern<<<grid, kda::kBlockThreads, lay.total, stream>>>(p, (int)tiles, fold ? 1 : 0);
+    // programmatic dependent launch: the next launch's CTAs may start their
+    // set-up while this grid's last CTAs finish; they wait for it before
+    // touching memory
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kda::kBlockThreads);
+    lc.dynamicSmemBytes = lay.total;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, kern, p, (int)tiles, fold ? 1 : 0) != cudaSuccess)
+        return KDA_ERR_CUDA;
     return finish_launch();
 }
 
