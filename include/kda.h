@@ -63,7 +63,7 @@ extern "C" {
 typedef enum kda_status {
     KDA_OK = 0,
     KDA_ERR_INVALID_ARG = 1,  /* a pointer, size, stride or alignment is wrong */
-    KDA_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, Q > 8 */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, Q > 8, H > 32767 */
     KDA_ERR_CUDA = 3          /* the kernel launch failed */
 } kda_status;
 
@@ -82,11 +82,12 @@ typedef enum kda_status {
 
 #define KDA_HEAD_DIM 128
 #define KDA_MAX_WINDOW 8
+#define KDA_MAX_HEADS 32767
 /* elements (bf16) per token record: k, v, g_raw (3 x 128), beta_raw, padding */
 #define KDA_RECORD_STRIDE 392
 
 typedef struct kda_config {
-    int32_t num_heads;        /* H >= 1 */
+    int32_t num_heads;        /* 1 <= H <= KDA_MAX_HEADS */
     int32_t head_dim;         /* must be 128 (K = V) */
     int32_t window;           /* Q = 1 + num_spec, 1..8 */
     int32_t num_slots;        /* S: slots of the state pool (slot 0 = null) */

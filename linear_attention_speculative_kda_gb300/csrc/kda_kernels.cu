@@ -219,7 +219,7 @@ struct WorkList {
     int slot[kPlanSize];
     int r[kPlanSize];
     int bos[kPlanSize];
-    int tp[kPlanSize];   // T | p << 8
+    int tp[kPlanSize];   // T | p << 8 | head << 16
     int dst[kPlanSize];
     int mid[kPlanSize];  // boundary block, or 0
     int mid_len[kPlanSize];
@@ -337,7 +337,7 @@ __device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles
         list.slot[pos] = w.slot;
         list.r[pos] = w.r;
         list.bos[pos] = w.bos;
-        list.tp[pos] = w.T | (w.p << 8);
+        list.tp[pos] = w.T | (w.p << 8) | (w.head << 16);
         if constexpr (kMode == Mode::kCommit) {
             list.dst[pos] = w.dst;
             list.mid[pos] = w.mid;
@@ -368,12 +368,12 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
     }
     const int i = c.idx++;
     w.tile = list.tile[i];
-    w.head = w.tile % p.H;
     w.slot = list.slot[i];
     w.r = list.r[i];
     w.bos = list.bos[i];
     w.T = list.tp[i] & 0xff;
-    w.p = list.tp[i] >> 8;
+    w.p = (list.tp[i] >> 8) & 0xff;
+    w.head = list.tp[i] >> 16;
     if constexpr (kMode == Mode::kCommit) {
         w.dst = list.dst[i];
         w.mid = list.mid[i];
@@ -677,6 +677,7 @@ kda_status check_config(const kda_config *cfg) {
         return KDA_ERR_INVALID_ARG;
     if (cfg->window < 1) return KDA_ERR_INVALID_ARG;
     if (cfg->head_dim != KDA_HEAD_DIM || cfg->window > KDA_MAX_WINDOW) return KDA_ERR_UNSUPPORTED;
+    if (cfg->num_heads > KDA_MAX_HEADS) return KDA_ERR_UNSUPPORTED;
     if (cfg->use_lower_bound != 0 && cfg->use_lower_bound != 1) return KDA_ERR_INVALID_ARG;
     if (cfg->use_lower_bound == 1 && !(cfg->lower_bound < 0.0f && isfinite(cfg->lower_bound)))
         return KDA_ERR_INVALID_ARG;

@@ -72,6 +72,7 @@ def test_verify_host_checks(lib):
     assert _verify(lib, None) == api.KDA_ERR_INVALID_ARG
     assert _verify(lib, _cfg(head_dim=64)) == api.KDA_ERR_UNSUPPORTED
     assert _verify(lib, _cfg(window=9)) == api.KDA_ERR_UNSUPPORTED
+    assert _verify(lib, _cfg(num_heads=32768)) == api.KDA_ERR_UNSUPPORTED
     assert _verify(lib, _cfg(window=0)) == api.KDA_ERR_INVALID_ARG
     assert _verify(lib, _cfg(num_heads=0)) == api.KDA_ERR_INVALID_ARG
     assert _verify(lib, _cfg(), B=-1) == api.KDA_ERR_INVALID_ARG
