@@ -168,3 +168,23 @@ def test_align_commit_bytes_by_rows():
 def test_l2_note_is_truthful():
     assert bench.l2_note(2 * 10**9).startswith("inputs larger than L2")
     assert "fits in L2" in bench.l2_note(2 * 2**20)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The reference arm (the oracle on the host cores) runs without a GPU and
+    prints one JSON line with the fields the benchmark contract names."""
+    import json
+    import subprocess
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--config", "tiny", "--steps", "2", "--warmup", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert res.returncode == 0, res.stderr[-2000:]
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "tiny"
