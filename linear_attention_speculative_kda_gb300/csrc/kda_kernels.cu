@@ -400,7 +400,7 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
         cp_async8(dst + 2 * lane, src + lane);
     }
     if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
-    if (warp == kProducerWarps - 1) {
+    if (warp == kProducerWarps - 2) {  // not the warp that stages checkpoints
         cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
         if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
     }
@@ -551,8 +551,6 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
         if (pt == 0) {
             ItemInfo &it = sy.info[c][b];
-            it.tile = cur.tile;
-            it.slot = cur.slot;
             it.head = cur.head;
             it.bos = cur.bos;
             it.T = cur.T;
