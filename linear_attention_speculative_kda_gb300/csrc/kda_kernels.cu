@@ -400,7 +400,7 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
         cp_async8(dst + 2 * lane, src + lane);
     }
     if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
-    if (warp == kProducerWarps - 2) {  // not the warp that stages checkpoints
+    if (warp == kProducerWarps - 2) {
         cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
         if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
     }
@@ -501,6 +501,14 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
     bulk_load(dst, src, kD * kD * 4, bar);
 }
 
+// Per-item duties of the producer warps, spread so that none carries two:
+// warp 3 (the fewest tokens to prepare, token u going to warp u mod 4)
+// stages the checkpoint, warp 2 copies g_bias and A_log, warp 1 waits for
+// the token buffer, writes the item info and hands the item over, and warp 0
+// copies the record tails.
+constexpr int kStageThread = kProducerThreads - 32;
+constexpr int kHandoffThread = 32;
+
 template <Mode kMode, bool kBounded>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
                              int num_tiles, int pt) {
@@ -521,9 +529,8 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     while (cur.tile >= 0) {
         const int c = n & 1;
         const int use_c = n >> 1;
-        // checkpoint of `cur` into consumer c's staging buffer, issued by the
-        // last warp, which has the fewest tokens to prepare
-        if (pt == kProducerThreads - 32) {
+        // checkpoint of `cur` into consumer c's staging buffer
+        if (pt == kStageThread) {
             if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
             if (ok)
                 issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
@@ -544,12 +551,12 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         // token vectors of `cur` into consumer c's buffer b, once it is free
         const int b = use_c % lay.nbuf;
         const int use_b = use_c / lay.nbuf;
-        if (pt == 0 && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
+        if (pt == kHandoffThread && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
         producer_sync();
         if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
-        if (pt == 0) {
+        if (pt == kHandoffThread) {
             ItemInfo &it = sy.info[c][b];
             it.head = cur.head;
             it.bos = cur.bos;
@@ -561,13 +568,13 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             it.mid_len = cur.mid_len;
         }
         producer_sync();  // all token vectors and the item info written
-        if (pt == 0) mbar_arrive(&sy.full_tok[c][b]);
+        if (pt == kHandoffThread) mbar_arrive(&sy.full_tok[c][b]);
         ++n;
         rb ^= 1;
         cur = nxt;
     }
     // end markers: the next buffer of each consumer says "no more items"
-    if (pt == 0) {
+    if (pt == kHandoffThread) {
         for (int c = 0; c < 2; ++c) {
             const int use_c = (n + 1 - c) >> 1;
             const int b = use_c % lay.nbuf;
