@@ -236,7 +236,8 @@ struct Sync {
     uint64_t empty_tok[2][2];  // the consumer is done with them
     ItemInfo info[2][2];
     int abort;
-    int pad[3];
+    int leave[2];   // per item parity: the producer threads leave (abort seen)
+    int pad;
 };
 
 // Raw bf16 inputs and gate parameters of one item, in channel pairs.
@@ -551,9 +552,13 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         // token vectors of `cur` into consumer c's buffer b, once it is free
         const int b = use_c % lay.nbuf;
         const int use_b = use_c / lay.nbuf;
-        if (pt == kHandoffThread && use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
+        if (pt == kHandoffThread) {
+            if (use_b > 0 && ok) ok = wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p);
+            // one thread decides for all whether to leave, so that they all do
+            sy.leave[n & 1] = *reinterpret_cast<volatile int *>(&sy.abort);
+        }
         producer_sync();
-        if (*reinterpret_cast<volatile int *>(&sy.abort)) return;
+        if (sy.leave[n & 1]) return;
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
         if (pt == kHandoffThread) {
