@@ -79,7 +79,15 @@ def _lib():
             _dbl_p, _dbl_p,
             ctypes.c_double, _dbl_p,
             ctypes.c_int, ctypes.c_double, ctypes.c_double,
-            _dbl_p, _dbl_p, _dbl_p,
+            _dbl_p, _dbl_p, _dbl_p, _dbl_p,
+        ]
+        lib.kda_oracle_fold_deltas.restype = ctypes.c_int
+        lib.kda_oracle_fold_deltas.argtypes = [
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            _dbl_p, _dbl_p, _dbl_p, _dbl_p,
+            ctypes.c_double, _dbl_p,
+            ctypes.c_int, ctypes.c_double,
+            _dbl_p,
         ]
         lib.kda_oracle_gate.restype = ctypes.c_double
         lib.kda_oracle_gate.argtypes = [ctypes.c_double, ctypes.c_double,
@@ -121,6 +129,19 @@ def window(h0, k, v, g_raw, beta_raw, a_log, g_bias, *, q=None,
     (None without q), ``traj`` T x V x K (None unless asked), ``h_final``
     V x K.
     """
+    out, traj, h_final, _ = window_deltas(
+        h0, k, v, g_raw, beta_raw, a_log, g_bias, q=q, bounded=bounded,
+        lower_bound=lower_bound, scale=scale, want_out=want_out, want_traj=want_traj,
+        want_delta=False)
+    return out, traj, h_final
+
+
+def window_deltas(h0, k, v, g_raw, beta_raw, a_log, g_bias, *, q=None,
+                  bounded=False, lower_bound=0.0, scale=1.0, want_out=None,
+                  want_traj=False, want_delta=True):
+    """``window`` plus each token's delta v' = beta (v - H k^) (T x V, the
+    fp32 "correction" the Kimi-K3 deferred context records), as a fourth
+    result (None unless asked)."""
     h0 = _f64(h0)
     V, K = h0.shape
     k = _f64(k).reshape(-1, K)
@@ -136,13 +157,36 @@ def window(h0, k, v, g_raw, beta_raw, a_log, g_bias, *, q=None,
     out = np.empty((T, V), np.float64) if want_out else None
     traj = np.empty((T, V, K), np.float64) if want_traj else None
     h_final = np.empty((V, K), np.float64)
+    delta = np.empty((T, V), np.float64) if want_delta else None
     rc = _lib().kda_oracle_window(
         K, V, T, _ptr(h0), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
         _ptr(beta_raw), float(a_log), _ptr(g_bias), int(bool(bounded)),
-        float(lower_bound), float(scale), _ptr(out), _ptr(traj), _ptr(h_final))
+        float(lower_bound), float(scale), _ptr(out), _ptr(traj), _ptr(h_final),
+        _ptr(delta))
     if rc != 0:
         raise ValueError("oracle window: bad sizes")
-    return out, traj, h_final
+    return out, traj, h_final, delta
+
+
+def fold_deltas(h0, k, g_raw, delta, a_log, g_bias, *, bounded=False, lower_bound=0.0):
+    """The closed form of n tokens whose deltas are known (the Kimi-K3
+    fp32-correction commit): H_n = H_0 diag(P_0) + sum_t d_t (k^_t * P_t)^T,
+    P_t the product of the later tokens' decays (see ``kda_window.c``).
+    ``k``, ``g_raw``: n x K; ``delta``: n x V; returns H_n (V x K)."""
+    h0 = _f64(h0)
+    V, K = h0.shape
+    k = _f64(k).reshape(-1, K)
+    n = k.shape[0]
+    g_raw = _f64(g_raw).reshape(n, K)
+    delta = _f64(delta).reshape(n, V)
+    g_bias = _f64(g_bias).reshape(K)
+    h_final = np.empty((V, K), np.float64)
+    rc = _lib().kda_oracle_fold_deltas(
+        K, V, n, _ptr(h0), _ptr(k), _ptr(g_raw), _ptr(delta), float(a_log), _ptr(g_bias),
+        int(bool(bounded)), float(lower_bound), _ptr(h_final))
+    if rc != 0:
+        raise ValueError("oracle fold: bad sizes")
+    return h_final
 
 
 # ---------------------------------------------------------------------------
@@ -183,12 +227,20 @@ class Cache:
 
     The pool is read lazily from a float32 array ``[S, H, V, K]`` (never
     modified); states the oracle writes are kept as float64 tiles.
+    ``record_format``: "raw" records hold each token's k, v, g_raw and
+    beta_raw and are replayed through the recurrence; "correction" records
+    hold k, g_raw and the token's delta (Kimi-K3's fp32 corrections) and are
+    folded in closed form.
     """
 
-    def __init__(self, pool_f32, record_slots: int, pending=None):
+    def __init__(self, pool_f32, record_slots: int, pending=None,
+                 record_format: str = "raw"):
+        if record_format not in ("raw", "correction"):
+            raise ValueError("record_format must be 'raw' or 'correction'")
         self.pool_src = pool_f32
         self.num_slots = pool_f32.shape[0]
         self.record_slots = record_slots
+        self.record_format = record_format
         self.written: dict[tuple[int, int], np.ndarray] = {}
         self.records: dict[tuple[int, int], dict] = {}
         if pending is None:
@@ -240,9 +292,14 @@ def _row_checks(layer: Layer, cache: Cache, T: int, slot: int, r: int):
 
 def _replay_records(layer, cache, slot, head, r, n):
     """Replay the first n recorded tokens of record slot r from the
-    checkpoint (the commit's replay: q is not needed, so no outputs)."""
+    checkpoint (the commit's replay: q is not needed, so no outputs); with
+    correction records, fold their deltas in closed form instead."""
     rec = cache.records[(r, head)]
     h0 = cache.state(slot, head)
+    if cache.record_format == "correction":
+        return fold_deltas(h0, rec["k"][:n], rec["g"][:n], rec["delta"][:n],
+                           layer.a_log[head], layer.g_bias[head], bounded=layer.bounded,
+                           lower_bound=layer.lower_bound)
     _, _, h = window(h0, rec["k"][:n], rec["v"][:n], rec["g"][:n],
                      rec["beta"][:n], layer.a_log[head], layer.g_bias[head],
                      bounded=layer.bounded, lower_bound=layer.lower_bound,
@@ -262,7 +319,9 @@ def verify(layer: Layer, cache: Cache, step: Step, *, pending: bool = False,
            threads: int = 1) -> VerifyResult:
     """RecoverSSM verify (recoverssm.py ``_verify_kernel``), optionally
     folding pending replays first (context.py: the next verify replays the
-    pending count of the row's record slot in the same pass)."""
+    pending count of the row's record slot in the same pass).  With
+    correction records (``cache.record_format``) each token's record holds
+    its k, g_raw and delta instead of k, v, g_raw and beta_raw."""
     B = len(step.state_indices)
     H, D = layer.num_heads, layer.head_dim
     T_tot = step.k.shape[0]
@@ -291,23 +350,27 @@ def verify(layer: Layer, cache: Cache, step: Step, *, pending: bool = False,
             if T == 0:
                 continue
             sl = slice(bos, bos + T)
-            out, traj, _ = window(
+            out, traj, _, delta = window_deltas(
                 cache.state(slot, h), step.k[sl, h], step.v[sl, h],
                 step.g_raw[sl, h], step.beta_raw[sl, h], layer.a_log[h],
                 layer.g_bias[h], q=step.q[sl, h], bounded=layer.bounded,
                 lower_bound=layer.lower_bound, scale=layer.scale,
-                want_traj=want_traj)
+                want_traj=want_traj, want_delta=cache.record_format == "correction")
             res.out[sl, h] = out
             if want_traj:
                 for t in range(T):
                     res.traj[(bos + t, h)] = traj[t]
             rec = cache.records.setdefault((r, h), {
                 "k": np.zeros((layer.window, D)), "v": np.zeros((layer.window, D)),
-                "g": np.zeros((layer.window, D)), "beta": np.zeros(layer.window)})
+                "g": np.zeros((layer.window, D)), "beta": np.zeros(layer.window),
+                "delta": np.zeros((layer.window, D))})
             rec["k"][:T] = step.k[sl, h]
-            rec["v"][:T] = step.v[sl, h]
             rec["g"][:T] = step.g_raw[sl, h]
-            rec["beta"][:T] = step.beta_raw[sl, h]
+            if delta is not None:      # correction records: k, g_raw and the delta
+                rec["delta"][:T] = delta
+            else:
+                rec["v"][:T] = step.v[sl, h]
+                rec["beta"][:T] = step.beta_raw[sl, h]
         return b
 
     for item in _map_rows(run, list(rows), threads):

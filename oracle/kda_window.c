@@ -69,7 +69,8 @@ double kda_oracle_gate(double x, double a_log, int bounded, double lower_bound)
  * in which case out must be NULL too.
  * out:     T x V, the output of each token (may be NULL);
  * traj:    T x V x K, the state after each token (may be NULL);
- * h_final: V x K, the state after the last token (T == 0: h0).
+ * h_final: V x K, the state after the last token (T == 0: h0);
+ * delta:   T x V, each token's delta v' = beta (v - H k^) (may be NULL).
  * Returns 0, or -1 if a size is out of range or memory runs out. */
 int kda_oracle_window(int K, int V, int T,
                       const double *h0,
@@ -77,7 +78,8 @@ int kda_oracle_window(int K, int V, int T,
                       const double *g_raw, const double *beta_raw,
                       double a_log, const double *g_bias,
                       int bounded, double lower_bound, double scale,
-                      double *out, double *traj, double *h_final)
+                      double *out, double *traj, double *h_final,
+                      double *delta)
 {
     if (K <= 0 || V <= 0 || T < 0)
         return -1;
@@ -143,6 +145,8 @@ int kda_oracle_window(int K, int V, int T,
             double vp = beta * (vt[r] - u);
             for (int c = 0; c < K; ++c)
                 row[c] += vp * kh[c];
+            if (delta != NULL)
+                delta[(size_t)t * V + r] = vp;
         }
 
         /* Output after the update. */
@@ -163,6 +167,82 @@ int kda_oracle_window(int K, int V, int T,
     free(kh);
     free(qh);
     free(decay);
+    return 0;
+}
+
+/* The closed form of n tokens whose deltas are known (the fp32-correction
+ * commit of the Kimi-K3 deferred context: the verify stores each token's
+ * delta, and the commit folds the deltas into the checkpoint without the
+ * state-dependent prediction H k^).  Unrolling the per-token update
+ * H <- H diag(e_t) + d_t k^_t^T over t = 1..n gives
+ *
+ *   H_n = H_0 diag(P_0) + sum_t d_t (k^_t * P_t)^T,
+ *   P_t[c] = prod_{s = t+1..n} e_s[c]          (P_n = 1),
+ *
+ * with e_t = exp(g_t) the gate of token t and k^_t its normalised key.  It
+ * is evaluated here term by term, as written, not as the recurrence.
+ *
+ * k, g_raw: n x K; delta: n x V; g_bias: K; h0, h_final: V x K (they may
+ * be the same buffer).  Returns 0, or -1 on bad sizes or no memory. */
+int kda_oracle_fold_deltas(int K, int V, int n,
+                           const double *h0,
+                           const double *k, const double *g_raw,
+                           const double *delta,
+                           double a_log, const double *g_bias,
+                           int bounded, double lower_bound,
+                           double *h_final)
+{
+    if (K <= 0 || V <= 0 || n < 0)
+        return -1;
+    size_t nk = (size_t)(n > 0 ? n : 1) * (size_t)K;
+    double *kh = (double *)malloc(sizeof(double) * nk);
+    double *e = (double *)malloc(sizeof(double) * nk);
+    double *coef = (double *)malloc(sizeof(double) * nk);
+    double *P = (double *)malloc(sizeof(double) * (size_t)K);
+    double *acc = (double *)malloc(sizeof(double) * (size_t)V * (size_t)K);
+    if (kh == NULL || e == NULL || coef == NULL || P == NULL || acc == NULL) {
+        free(kh);
+        free(e);
+        free(coef);
+        free(P);
+        free(acc);
+        return -1;
+    }
+    for (int t = 0; t < n; ++t) {
+        const double *kt = k + (size_t)t * K;
+        const double *gt = g_raw + (size_t)t * K;
+        double sk = 0.0;
+        for (int c = 0; c < K; ++c)
+            sk += kt[c] * kt[c];
+        double nrm = sqrt(sk + 1e-6);
+        for (int c = 0; c < K; ++c) {
+            kh[(size_t)t * K + c] = kt[c] / nrm;
+            e[(size_t)t * K + c] = exp(kda_oracle_gate(gt[c] + g_bias[c], a_log, bounded,
+                                                       lower_bound));
+        }
+    }
+    /* P runs from P_n = 1 down to P_0; coef_t = k^_t * P_t. */
+    for (int c = 0; c < K; ++c)
+        P[c] = 1.0;
+    for (int t = n - 1; t >= 0; --t) {
+        for (int c = 0; c < K; ++c) {
+            coef[(size_t)t * K + c] = kh[(size_t)t * K + c] * P[c];
+            P[c] *= e[(size_t)t * K + c];
+        }
+    }
+    for (int r = 0; r < V; ++r)
+        for (int c = 0; c < K; ++c) {
+            double s = h0[(size_t)r * K + c] * P[c];
+            for (int t = 0; t < n; ++t)
+                s += delta[(size_t)t * V + r] * coef[(size_t)t * K + c];
+            acc[(size_t)r * K + c] = s;
+        }
+    memcpy(h_final, acc, sizeof(double) * (size_t)V * (size_t)K);
+    free(kh);
+    free(e);
+    free(coef);
+    free(P);
+    free(acc);
     return 0;
 }
 
