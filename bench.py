@@ -43,6 +43,16 @@ FALLBACK_BF16_TFLOPS = 1900.0
 STATE_BYTES = 128 * 128 * 4          # one fp32 state tile
 TOKEN_BYTES = 2052                   # q, k, v, g_raw, beta read + out, records written
 RECORD_BYTES = 770                   # raw k, v, g_raw, beta read back by a replay
+# correction records: fp32 delta + bf16 k + bf16 g_raw (1024 bytes) per token
+CORR_TOKEN_BYTES = 1024 + 2 + 256 + 1024
+CORR_RECORD_BYTES = 1024
+
+
+def format_bytes(record_format: str):
+    """(bytes a verify moves per new token, bytes a replay reads per record)."""
+    if record_format == "correction":
+        return CORR_TOKEN_BYTES, CORR_RECORD_BYTES
+    return TOKEN_BYTES, RECORD_BYTES
 
 
 # ---------------------------------------------------------------- helpers --
@@ -226,9 +236,10 @@ class ClockSampler:
 
 # ------------------------------------------------------- algorithmic bytes --
 
-def plan_bytes(wl: W.Workload):
+def plan_bytes(wl: W.Workload, record_format: str = "raw"):
     """Algorithmic bytes of each launch of one step, from the drawn lengths,
     accepted counts, eager masks and the pending replays they imply."""
+    tok_b, rec_b = format_bytes(record_format)
     sp = wl.spec
     H = sp.H
     lens = wl.lens.numpy().astype(np.int64)
@@ -241,21 +252,21 @@ def plan_bytes(wl: W.Workload):
     launches = []
     if not sp.deferred:
         n = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
-        vb = np.where(live & (lens > 0), STATE_BYTES + lens * TOKEN_BYTES, 0).sum() * H
-        cb = np.where(live & (n > 0), 2 * STATE_BYTES + n * RECORD_BYTES, 0).sum() * H
+        vb = np.where(live & (lens > 0), STATE_BYTES + lens * tok_b, 0).sum() * H
+        cb = np.where(live & (n > 0), 2 * STATE_BYTES + n * rec_b, 0).sum() * H
         launches = [("verify", float(vb)), ("commit", float(cb))]
         return launches
     n1 = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
     eager1 = wl.steps[0].eager.numpy().astype(bool)
     n2 = commit_n(wl.steps[1].num_accepted.numpy().astype(np.int64))
     valid1 = live & (n1 > 0)
-    v1 = np.where(live & (lens > 0), STATE_BYTES + lens * TOKEN_BYTES, 0).sum() * H
-    c1 = np.where(valid1 & eager1, 2 * STATE_BYTES + n1 * RECORD_BYTES, 0).sum() * H
+    v1 = np.where(live & (lens > 0), STATE_BYTES + lens * tok_b, 0).sum() * H
+    c1 = np.where(valid1 & eager1, 2 * STATE_BYTES + n1 * rec_b, 0).sum() * H
     pend = np.where(valid1 & ~eager1, n1, 0)
     v2 = np.where(live & ((lens > 0) | (pend > 0)),
-                  STATE_BYTES + lens * TOKEN_BYTES
-                  + np.where(pend > 0, STATE_BYTES + pend * RECORD_BYTES, 0), 0).sum() * H
-    c2 = np.where(live & (n2 > 0), 2 * STATE_BYTES + n2 * RECORD_BYTES, 0).sum() * H
+                  STATE_BYTES + lens * tok_b
+                  + np.where(pend > 0, STATE_BYTES + pend * rec_b, 0), 0).sum() * H
+    c2 = np.where(live & (n2 > 0), 2 * STATE_BYTES + n2 * rec_b, 0).sum() * H
     return [("verify", float(v1)), ("commit_deferred", float(c1)),
             ("verify_fused", float(v2)), ("commit", float(c2))]
 
@@ -269,7 +280,7 @@ def units_per_step(wl: W.Workload) -> int:
 class Engine:
     """Device-resident buffers of one workload and the step's launches."""
 
-    def __init__(self, wl: W.Workload, device):
+    def __init__(self, wl: W.Workload, device, record_format: str = "raw"):
         from linear_attention_speculative_kda_gb300 import api
         self.api = api
         self.wl = wl
@@ -282,13 +293,15 @@ class Engine:
         self.cu = wl.cu_seqlens.to(d)
         self.slots = wl.state_indices.to(d)
         self.rr = None if wl.record_rows is None else wl.record_rows.to(d)
-        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d)
+        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d,
+                                            record_format=record_format)
         self.pending = torch.zeros(sp.record_slots, dtype=torch.int32, device=d)
         self.err = torch.zeros(1, dtype=torch.int32, device=d)
         self.all_eager = torch.ones(sp.B, dtype=torch.uint8, device=d)
         self.steps = self.new_input_set()
         self.kw = dict(window=sp.Q, record_slots=sp.record_slots,
-                       lower_bound=sp.lower_bound if sp.bounded else None)
+                       lower_bound=sp.lower_bound if sp.bounded else None,
+                       record_format=record_format)
 
     def new_input_set(self):
         """Device copies of every decode step's inputs, plus output buffers."""
@@ -396,7 +409,7 @@ class HostIO:
 
 # -------------------------------------------------------------- CPU side --
 
-def oracle_sample_run(wl: W.Workload, rows, threads: int):
+def oracle_sample_run(wl: W.Workload, rows, threads: int, record_format: str = "raw"):
     """The oracle on a sample of rows of the workload's whole step; returns
     (units processed, seconds)."""
     from oracle import kda_oracle as O
@@ -411,7 +424,7 @@ def oracle_sample_run(wl: W.Workload, rows, threads: int):
                     wl.cu_seqlens.numpy(), wl.state_indices.numpy(),
                     None if wl.record_rows is None else wl.record_rows.numpy())
              for st in wl.steps]
-    cache = O.Cache(wl.pool.numpy(), sp.record_slots)
+    cache = O.Cache(wl.pool.numpy(), sp.record_slots, record_format=record_format)
     t0 = time.perf_counter()
     if not sp.deferred:
         O.verify(layer, cache, steps[0], rows=rows, threads=threads)
@@ -429,7 +442,7 @@ def oracle_sample_run(wl: W.Workload, rows, threads: int):
     return len(rows) * sp.H * sp.steps, dt
 
 
-def cpu_baseline(wl: W.Workload, budget_s: float):
+def cpu_baseline(wl: W.Workload, budget_s: float, record_format: str = "raw"):
     """Time the oracle on growing samples of rows until ``budget_s`` seconds
     of CPU work have been measured (or the whole batch is done)."""
     threads = max(1, os.cpu_count() or 1)
@@ -441,7 +454,7 @@ def cpu_baseline(wl: W.Workload, budget_s: float):
     chunk = max(1, threads)
     while done < len(order) and secs < budget_s:
         rows = order[done:done + chunk]
-        u, dt = oracle_sample_run(wl, rows, threads)
+        u, dt = oracle_sample_run(wl, rows, threads, record_format)
         units += u
         secs += dt
         done += len(rows)
@@ -457,9 +470,10 @@ def cpu_baseline(wl: W.Workload, budget_s: float):
 
 # ------------------------------------------------------------------- arms --
 
-def workload_config(wl: W.Workload, world: int):
+def workload_config(wl: W.Workload, world: int, record_format: str = "raw"):
     sp = wl.spec
-    return {"workload": sp.name, "requests": sp.B, "heads": sp.H, "head_dim": sp.D,
+    return {"workload": sp.name, "records": record_format,
+            "requests": sp.B, "heads": sp.H, "head_dim": sp.D,
             "window": sp.Q, "pool_slots": sp.S, "record_slots": sp.record_slots,
             "gate": f"bounded lb={sp.lower_bound}" if sp.bounded else "softplus",
             "decode_steps_per_step": sp.steps, "ranks": world,
@@ -621,10 +635,10 @@ def run_ours(args):
     torch.cuda.set_device(device)
     init_dist(world, "nccl")
     wl = W.generate(args.config, seed=shard_seed(args.seed, rank))
-    eng = Engine(wl, device)
+    eng = Engine(wl, device, args.records)
     names = [n for n, _ in eng.launches()]
     nl = len(names)
-    bytes_per = dict(plan_bytes(wl))
+    bytes_per = dict(plan_bytes(wl, args.records))
 
     clocks = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
@@ -678,7 +692,8 @@ def run_ours(args):
     roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dom["gbs"] / peak,
                 "peak_source": f"{peak_src} ({'of measured' if peak_src == 'measured' else 'of fallback'})",
-                "traffic": profiled_traffic(dom["name"], wl.spec.name),
+                "traffic": profiled_traffic(dom["name"], wl.spec.name if args.records == "raw"
+                                            else f"{wl.spec.name}_{args.records}"),
                 "algorithmic_bytes_per_launch": dom["bytes_per_launch"]}
     step_gbs = step_bytes * args.steps / (ms_total / 1e3) / 1e9
 
@@ -711,12 +726,12 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_budget)
+        cpu = cpu_baseline(wl, args.cpu_budget, args.records)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded)", "config": workload_config(wl, world),
+            "data": "synthetic (seeded)", "config": workload_config(wl, world, args.records),
             "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
             "roofline": roofline, "kernels": kernels, "gpu_launches": nl * args.steps,
             "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
@@ -741,7 +756,7 @@ def run_reference(args):
     times, units = [], 0
     for k in range(args.warmup + args.steps):
         rows = sorted(rng.choice(wl.spec.B, size=rows_per_step, replace=False).tolist())
-        u, dt = oracle_sample_run(wl, rows, threads)
+        u, dt = oracle_sample_run(wl, rows, threads, args.records)
         if k >= args.warmup:
             times.append(dt)
             units += u
@@ -752,7 +767,8 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded)", "config": workload_config(wl, 1),
+            "dtype": "f64", "data": "synthetic (seeded)",
+            "config": workload_config(wl, 1, args.records),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -773,6 +789,8 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the separately timed conv compaction and align commit")
     ap.add_argument("--reference-rows", type=int, default=8)
+    ap.add_argument("--records", choices=["raw", "correction"], default="raw",
+                    help="record format: raw inputs replayed (default) or fp32 deltas folded")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -28,10 +28,12 @@
  *   [T_total][H] with its own token stride.  cu_seqlens is int32 [B + 1]
  *   (row b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1).
  * - Records (the verify -> commit scratch of [GLM] `Records` and [KIMI]
- *   `allocate_records`) hold each token's RAW bf16 k, v, g_raw and beta_raw.
+ *   `allocate_records`) hold each token's RAW bf16 k, v, g_raw and beta_raw
+ *   (or, with cfg->record_format == KDA_RECORDS_CORRECTION, its fp32 delta
+ *   with k and g_raw; see KDA_RECORDS_CORRECTION below).
  *   They are indexed by record slot r in [-1, R): r = -1 is a scratch row
- *   that rows without a record slot write and nothing ever reads.  Layout
- *   (internal, sized by kda_records_bytes): bf16
+ *   that rows without a record slot write and nothing ever reads.  Raw
+ *   layout (internal, sized by kda_records_bytes): bf16
  *   [R + 1][H][Q][KDA_RECORD_STRIDE] with record slot r at row r + 1, and in
  *   each token record k at [0,128), v at [128,256), g_raw at [256,384) and
  *   beta_raw at element 384 (the rest is padding to a 16-byte multiple).
@@ -62,7 +64,7 @@ extern "C" {
 
 typedef enum kda_status {
     KDA_OK = 0,
-    KDA_ERR_INVALID_ARG = 1,  /* a pointer, size, stride or alignment is wrong */
+    KDA_ERR_INVALID_ARG = 1,  /* a pointer, size, stride, alignment or format is wrong */
     KDA_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim != 128, Q > 8, H > 32767 */
     KDA_ERR_CUDA = 3          /* the kernel launch failed */
 } kda_status;
@@ -86,6 +88,23 @@ typedef enum kda_status {
 /* elements (bf16) per token record: k, v, g_raw (3 x 128), beta_raw, padding */
 #define KDA_RECORD_STRIDE 392
 
+/* Record formats (kda_config.record_format).
+ * KDA_RECORDS_RAW: each token's raw bf16 k, v, g_raw and beta_raw; a commit,
+ *   fold or flush replays the recurrence on them ([GLM] `Records`).
+ * KDA_RECORDS_CORRECTION: each token's fp32 delta v' = beta (v - S k^) (the
+ *   "correction" of [KIMI] `allocate_records`, whose fp32 [Q, D] and
+ *   activation-dtype [Q, 2D] tensors these mirror) with its bf16 k and g_raw;
+ *   a commit, fold or flush applies S <- S diag(exp(g)) + v' k^T per token,
+ *   i.e. folds the deltas in closed form, without the prediction S k^.
+ *   Layout (internal, sized by kda_correction_records_bytes): per record slot
+ *   row r + 1, head h and token t, KDA_CORRECTION_RECORD_BYTES bytes: the
+ *   fp32 delta of the 128 rows at byte 0, bf16 k at byte 512, bf16 g_raw at
+ *   byte 768.  The folded state has the bits of the verify's trajectory (the
+ *   same operations in the same order after v'), as in the raw format. */
+#define KDA_RECORDS_RAW 0
+#define KDA_RECORDS_CORRECTION 1
+#define KDA_CORRECTION_RECORD_BYTES 1024
+
 typedef struct kda_config {
     int32_t num_heads;        /* 1 <= H <= KDA_MAX_HEADS */
     int32_t head_dim;         /* must be 128 (K = V) */
@@ -100,11 +119,18 @@ typedef struct kda_config {
     int64_t stride_v_t;
     int64_t stride_g_t;
     int64_t stride_beta_t;    /* any positive stride */
+    int32_t record_format;    /* KDA_RECORDS_RAW or KDA_RECORDS_CORRECTION; every
+                                 call on one records buffer must use the same */
+    int32_t reserved;         /* must be 0 */
 } kda_config;
 
-/* Bytes of the records buffer for H heads, window Q and R record slots:
- * (R + 1) * H * Q * KDA_RECORD_STRIDE * 2.  Returns 0 for invalid sizes. */
+/* Bytes of the raw-format records buffer for H heads, window Q and R record
+ * slots: (R + 1) * H * Q * KDA_RECORD_STRIDE * 2.  0 for invalid sizes. */
 size_t kda_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots);
+
+/* Bytes of a correction-format records buffer:
+ * (R + 1) * H * Q * KDA_CORRECTION_RECORD_BYTES.  0 for invalid sizes. */
+size_t kda_correction_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots);
 
 /*
  * kda_verify -- speculative verify from each row's checkpoint
@@ -118,8 +144,8 @@ size_t kda_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots
  *   or -exp(A_log[h])*softplus(x), beta = sigmoid(beta_raw),
  *   S <- S*diag(exp(g)); v' = beta*(v - S k^); S <- S + v' k^T; o = S q^.
  * Writes o (bf16, round to nearest even) to out[token][h][:], and the
- * token's raw k, v, g_raw, beta_raw to record slot r = record_rows[b] (or b),
- * position t.  The pool is NOT written, except by the deferred fold below.
+ * token's record (raw: k, v, g_raw, beta_raw; correction: v', k, g_raw) to
+ * record slot r = record_rows[b] (or b), position t.  The pool is NOT written, except by the deferred fold below.
  *
  * Deferred fold ([KIMI]: the next verify replays the pending count in the
  * same pass): if pending != NULL, r >= 0 and p = pending[r] > 0, the first p

@@ -21,6 +21,8 @@ _LIBRARY = os.path.join(_PKG, "libkda.so")
 HEAD_DIM = 128
 MAX_WINDOW = 8
 RECORD_STRIDE = 392          # bf16 elements per token record (k, v, g, beta, pad)
+CORRECTION_RECORD_BYTES = 1024  # fp32 delta, bf16 k, bf16 g_raw per token
+RECORD_FORMATS = {"raw": 0, "correction": 1}
 
 KDA_OK = 0
 KDA_ERR_INVALID_ARG = 1
@@ -36,6 +38,7 @@ ROW_BAD_BLOCK = 32
 
 EXPORTED = (
     "kda_records_bytes",
+    "kda_correction_records_bytes",
     "kda_verify",
     "kda_commit",
     "kda_flush",
@@ -70,6 +73,8 @@ class KdaConfig(ctypes.Structure):
         ("stride_v_t", ctypes.c_int64),
         ("stride_g_t", ctypes.c_int64),
         ("stride_beta_t", ctypes.c_int64),
+        ("record_format", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -123,6 +128,8 @@ def load_library():
     cfgp = ctypes.POINTER(KdaConfig)
     lib.kda_records_bytes.restype = ctypes.c_size_t
     lib.kda_records_bytes.argtypes = [i32, i32, i32]
+    lib.kda_correction_records_bytes.restype = ctypes.c_size_t
+    lib.kda_correction_records_bytes.argtypes = [i32, i32, i32]
     lib.kda_verify.restype = ctypes.c_int
     lib.kda_verify.argtypes = [cfgp] + [vp] * 10 + [i32] + [vp] * 7
     lib.kda_commit.restype = ctypes.c_int
@@ -194,9 +201,19 @@ def _opt(t, dtype, name, device):
     return None if t is None else _req(t, dtype, name, device)
 
 
+def _format_code(record_format: str) -> int:
+    try:
+        return RECORD_FORMATS[record_format]
+    except KeyError:
+        raise ValueError(f"record_format must be one of {sorted(RECORD_FORMATS)}") from None
+
+
 def make_config(num_heads, window, num_slots, record_slots, *, lower_bound=None,
-                scale=None, strides=(1, 1, 1, 1, 1), head_dim=HEAD_DIM) -> KdaConfig:
+                scale=None, strides=(1, 1, 1, 1, 1), head_dim=HEAD_DIM,
+                record_format: str = "raw") -> KdaConfig:
     cfg = KdaConfig()
+    cfg.record_format = _format_code(record_format)
+    cfg.reserved = 0
     cfg.num_heads = num_heads
     cfg.head_dim = head_dim
     cfg.window = window
@@ -211,22 +228,46 @@ def make_config(num_heads, window, num_slots, record_slots, *, lower_bound=None,
 
 
 def kda_records_bytes(num_heads: int, window: int, record_slots: int) -> int:
-    """Size in bytes of the records buffer (``kda_records_bytes``)."""
+    """Size in bytes of a raw-format records buffer (``kda_records_bytes``)."""
     return int(load_library().kda_records_bytes(num_heads, window, record_slots))
 
 
-def allocate_records(num_heads: int, window: int, record_slots: int, device) -> torch.Tensor:
-    """A records buffer for ``record_slots`` slots plus the scratch row."""
-    nbytes = kda_records_bytes(num_heads, window, record_slots)
+def kda_correction_records_bytes(num_heads: int, window: int, record_slots: int) -> int:
+    """Size in bytes of a correction-format records buffer
+    (``kda_correction_records_bytes``)."""
+    return int(load_library().kda_correction_records_bytes(num_heads, window, record_slots))
+
+
+def records_bytes(num_heads: int, window: int, record_slots: int, record_format: str) -> int:
+    _format_code(record_format)
+    fn = kda_records_bytes if record_format == "raw" else kda_correction_records_bytes
+    return fn(num_heads, window, record_slots)
+
+
+def allocate_records(num_heads: int, window: int, record_slots: int, device,
+                     record_format: str = "raw") -> torch.Tensor:
+    """A records buffer (raw or correction format) for ``record_slots``
+    slots plus the scratch row, as a flat bf16 tensor."""
+    nbytes = records_bytes(num_heads, window, record_slots, record_format)
     if nbytes == 0:
         raise ValueError("invalid record sizes")
     return torch.empty(nbytes // 2, dtype=torch.bfloat16, device=device)
 
 
+def _check_records(records, H, window, record_slots, record_format):
+    """The records buffer holds the format's size (sizes the library does
+    not support are left for it to report)."""
+    need = records_bytes(H, window, record_slots, record_format)
+    if need > 0 and (records.numel() * records.element_size() < need
+                     or not records.is_contiguous()):
+        raise ValueError(f"records must be a contiguous buffer of at least {need} bytes "
+                         f"for the {record_format} format")
+
+
 def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
                state_indices, records, out, *, window: int, record_slots: int,
                lower_bound=None, scale=None, record_rows=None, pending=None,
-               trajectory_out=None, error_word=None) -> torch.Tensor:
+               trajectory_out=None, error_word=None, record_format: str = "raw") -> torch.Tensor:
     """``kda_verify``: speculative verify from each row's checkpoint.
 
     q, k, v, g_raw: bf16 [T, H, 128] (token stride free, [H, D] packed);
@@ -262,7 +303,8 @@ def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
     strides = (_token_stride(q), _token_stride(k), _token_stride(v), _token_stride(g_raw),
                _token_stride(beta_raw))
     cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound, scale=scale,
-                      strides=strides, head_dim=state_pool.shape[-1])
+                      strides=strides, head_dim=state_pool.shape[-1], record_format=record_format)
+    _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_verify(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                         _ptr(beta_raw), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
@@ -275,7 +317,7 @@ def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
 
 def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepted, records,
                *, window: int, record_slots: int, lower_bound=None, record_rows=None,
-               pending=None, eager=None, error_word=None) -> None:
+               pending=None, eager=None, error_word=None, record_format: str = "raw") -> None:
     """``kda_commit``: fold each row's accepted tokens into its checkpoint
     (eager), or store them as pending replays (deferred, ``pending`` given)."""
     dev = state_pool.device
@@ -297,7 +339,8 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
         raise ValueError("metadata sizes do not match the batch")
     S, H = state_pool.shape[0], state_pool.shape[1]
     cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1])
+                      head_dim=state_pool.shape[-1], record_format=record_format)
+    _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_commit(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
                         _ptr(cu_seqlens), _ptr(state_indices), B, _ptr(num_accepted),
@@ -307,7 +350,8 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
 
 
 def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, window: int,
-              record_slots: int, lower_bound=None, record_rows=None, error_word=None) -> None:
+              record_slots: int, lower_bound=None, record_rows=None, error_word=None,
+              record_format: str = "raw") -> None:
     """``kda_flush``: fold pending replays into the checkpoints in place."""
     dev = state_pool.device
     f32, i32 = torch.float32, torch.int32
@@ -323,7 +367,8 @@ def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, win
     B = state_indices.shape[0]
     S, H = state_pool.shape[0], state_pool.shape[1]
     cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1])
+                      head_dim=state_pool.shape[-1], record_format=record_format)
+    _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_flush(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
                        _ptr(state_indices), B, _ptr(record_rows), _ptr(records), _ptr(pending),
@@ -404,7 +449,7 @@ def _check_align(block_table, num_computed, request_indices, dev):
 def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepted, records,
                      block_table, num_computed, *, block_size: int, window: int,
                      record_slots: int, lower_bound=None, record_rows=None,
-                     request_indices=None, error_word=None) -> None:
+                     request_indices=None, error_word=None, record_format: str = "raw") -> None:
     """``kda_commit_align``: the eager commit writing the final and boundary
     blocks of a paged state cache.  num_accepted, num_computed and the block
     table rows are per request."""
@@ -426,7 +471,8 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
         raise ValueError("metadata sizes do not match the batch")
     S, H = state_pool.shape[0], state_pool.shape[1]
     cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1])
+                      head_dim=state_pool.shape[-1], record_format=record_format)
+    _check_records(records, H, window, record_slots, record_format)
     al = make_align(block_table, num_computed, block_size, request_indices)
     lib = load_library()
     st = lib.kda_commit_align(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),

@@ -9,15 +9,18 @@
 // reduced across those 8 lanes with shuffles only.
 //
 // The per-token vectors that do not depend on the state (k^, q^, exp(g),
-// beta, v) are prepared by producer warps into shared memory; the token loop
-// reads them with conflict-free broadcast loads.
+// beta, v, or a recorded token's delta v') are prepared by producer warps
+// into shared memory; the token loop reads them with conflict-free
+// broadcast loads.
 //
 // Bit-exactness of commit against verify: the verify, the commit replay, the
 // deferred fold and the flush all run the token pieces below with the same
 // thread mapping, the same explicit round-to-nearest intrinsics (no
 // contraction left to the compiler), the same reduction tree and the same
 // token preparation, so the state after a token has the same bits whichever
-// kernel computes it.
+// kernel computes it.  With correction records the replays skip the
+// prediction and apply the v' the verify stored, through the same decay and
+// rank-one pieces, so they reach the same bits too.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -31,6 +34,11 @@ constexpr int kRecStride = 392;     // bf16 elements per token record
 constexpr int kRecV = 128;          // offset of v inside a token record
 constexpr int kRecG = 256;          // offset of g_raw
 constexpr int kRecBeta = 384;       // offset of beta_raw
+// Correction records (the fp32-correction form): per token 1024 bytes, the
+// fp32 delta v' at byte 0, bf16 k at byte 512 and bf16 g_raw at byte 768.
+constexpr int kCorrBytes = 1024;
+constexpr int kCorrK = 512;
+constexpr int kCorrG = 768;
 constexpr unsigned kFull = 0xffffffffu;
 
 // Error-word bits (same values as the public header's macros).
@@ -290,10 +298,8 @@ __device__ __forceinline__ float reduce_rows(const float (&part)[8], int j) {
 // Pieces of one token of the recurrence on the thread's part of the tile:
 //   S <- S diag(e);  u = S k^;  v' = beta (v - u);  S <- S + v' k^T;  o = S q^.
 
-// Decay along K in place, then the partial sums of u = S k^ of the 8 rows.
-__device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int slot, const Lane &L,
-                                               float (&part)[8]) {
-    const float *e = tv.e + slot * kD;
+// Decay along K in place: S <- S diag(e).
+__device__ __forceinline__ void decay(Tile &h, const float *e, const Lane &L) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const float4 ee = ld_cols(e, L, m);
@@ -304,18 +310,11 @@ __device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int s
             h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     }
-    row_partials(h, tv.kh + slot * kD, L, part);
 }
 
-// v' = beta (v - u) for the lane's row, shared with the row group, then the
-// rank-one update S <- S + v' k^T.
-__device__ __forceinline__ void delta_update_vp(Tile &h, const TokView &tv, int slot, float vp,
-                                                const Lane &L) {
-    const int base = L.lane & ~7;
-    float vpi[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) vpi[i] = __shfl_sync(kFull, vp, base + i);
-    const float *kh = tv.kh + slot * kD;
+// Rank-one update S <- S + v' k^T of the thread's 8 rows (vpi: their v').
+__device__ __forceinline__ void rank_one(Tile &h, const float (&vpi)[8], const float *kh,
+                                         const Lane &L) {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         const float4 kk = ld_cols(kh, L, m);
@@ -328,6 +327,24 @@ __device__ __forceinline__ void delta_update_vp(Tile &h, const TokView &tv, int 
             h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
     }
+}
+
+// Decay along K in place, then the partial sums of u = S k^ of the 8 rows.
+__device__ __forceinline__ void decay_partials(Tile &h, const TokView &tv, int slot, const Lane &L,
+                                               float (&part)[8]) {
+    decay(h, tv.e + slot * kD, L);
+    row_partials(h, tv.kh + slot * kD, L, part);
+}
+
+// v' = beta (v - u) for the lane's row, shared with the row group, then the
+// rank-one update S <- S + v' k^T.
+__device__ __forceinline__ void delta_update_vp(Tile &h, const TokView &tv, int slot, float vp,
+                                                const Lane &L) {
+    const int base = L.lane & ~7;
+    float vpi[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vpi[i] = __shfl_sync(kFull, vp, base + i);
+    rank_one(h, vpi, tv.kh + slot * kD, L);
 }
 
 __device__ __forceinline__ void delta_update(Tile &h, const TokView &tv, int slot, float u,
@@ -343,23 +360,27 @@ __device__ __forceinline__ void token_plain(Tile &h, const TokView &tv, int slot
     delta_update(h, tv, slot, reduce_rows(part, L.j), L);
 }
 
+// One token whose delta v' is known (a correction record, in the token
+// vector's v slot): S <- S diag(e) + v' k^T with no prediction S k^.  These
+// are the operations the verify made after it computed v', so the state has
+// the bits of the verify's trajectory.  The thread reads its 8 rows' v'
+// from shared memory (rows 32w + 8g .. +7, two aligned float4).
+__device__ __forceinline__ void token_corr(Tile &h, const TokView &tv, int slot, const Lane &L) {
+    decay(h, tv.e + slot * kD, L);
+    const float4 *d = reinterpret_cast<const float4 *>(tv.v + slot * kD + L.row(0));
+    const float4 d0 = d[0], d1 = d[1];
+    const float vpi[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    rank_one(h, vpi, tv.kh + slot * kD, L);
+}
+
 // One token with its output o = S' q^ (S' the state after the token) to
 // out_row (bf16), from the decayed state D = S diag(e) in one pass:
 // S' q^ = D q^ + v' (k^ . q^), so u = D k^ and D q^ share the pass and the
 // reduction.  The state update is the one token_plain does (same bits).
-__device__ __forceinline__ void token_out(Tile &h, const TokView &tv, int slot, int qslot,
-                                          const Lane &L, __nv_bfloat16 *out_row) {
-    const float *e = tv.e + slot * kD;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const float4 ee = ld_cols(e, L, m);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float2 lo = mul2(h[i][m].x, h[i][m].y, ee.x, ee.y);
-            const float2 hi = mul2(h[i][m].z, h[i][m].w, ee.z, ee.w);
-            h[i][m] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        }
-    }
+// Returns the lane's v' (of row L.row(L.j)).
+__device__ __forceinline__ float token_out(Tile &h, const TokView &tv, int slot, int qslot,
+                                           const Lane &L, __nv_bfloat16 *out_row) {
+    decay(h, tv.e + slot * kD, L);
     float pu[8], po[8];
     row_partials2(h, tv.kh + slot * kD, tv.qh + qslot * kD, L, pu, po);
     const float u = reduce_rows(pu, L.j);
@@ -368,6 +389,7 @@ __device__ __forceinline__ void token_out(Tile &h, const TokView &tv, int slot, 
     const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
     out_row[L.row(L.j)] = __float2bfloat16_rn(__fmaf_rn(vp, tv.kq[qslot], dq));
     delta_update_vp(h, tv, slot, vp, L);
+    return vp;
 }
 
 }  // namespace kda

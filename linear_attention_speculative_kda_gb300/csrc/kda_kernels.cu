@@ -23,6 +23,7 @@
 namespace kda {
 
 static_assert(kRecStride == KDA_RECORD_STRIDE, "record layout mismatch");
+static_assert(kCorrBytes == KDA_CORRECTION_RECORD_BYTES, "correction record layout mismatch");
 static_assert(kD == KDA_HEAD_DIM, "head dim mismatch");
 static_assert(kMaxQ == KDA_MAX_WINDOW, "window mismatch");
 static_assert(kBadLength == KDA_ROW_BAD_LENGTH && kBadSlot == KDA_ROW_BAD_SLOT &&
@@ -54,6 +55,12 @@ __device__ __forceinline__ int read_row(const Params &p, int b, bool need_len, R
 
 __device__ __forceinline__ __nv_bfloat16 *record_base(const Params &p, int r, int head) {
     return p.records + ((size_t)(r + 1) * p.H + head) * (size_t)p.Q * kRecStride;
+}
+
+// Correction records: kCorrBytes per token, same (r + 1, head, token) order.
+__device__ __forceinline__ unsigned char *corr_base(const Params &p, int r, int head) {
+    return reinterpret_cast<unsigned char *>(p.records) +
+           ((size_t)(r + 1) * p.H + head) * (size_t)p.Q * kCorrBytes;
 }
 
 // ------------------------------------------------------------- work items --
@@ -211,7 +218,7 @@ __device__ __forceinline__ void reg_dealloc() {
 
 struct ItemInfo {
     int tile, slot, head, bos, T, p, end;
-    int dst, mid, mid_len, pad0, pad1;
+    int dst, mid, mid_len, r, pad;
 };
 
 struct WorkList {
@@ -240,8 +247,12 @@ struct Sync {
     int pad;
 };
 
-// Raw bf16 inputs and gate parameters of one item, in channel pairs.
+// Raw bf16 inputs and gate parameters of one item, in channel pairs.  With
+// correction records a token's v slot is twice as wide (kD words): a recorded
+// token's fp32 delta, or a new token's bf16 v in its first half.
+template <bool kCorr>
 struct RawView {
+    static constexpr int kVWords = kCorr ? kD : kD / 2;  // 32-bit words per v slot
     uint32_t *k, *v, *g, *q;
     uint2 *tail;                // record tails: beta_raw bits in the low half
     float *bias;                // g_bias of the item's head (128)
@@ -250,7 +261,7 @@ struct RawView {
     __device__ __forceinline__ RawView(unsigned char *base, int slots, int Q) {
         k = reinterpret_cast<uint32_t *>(base);
         v = k + slots * (kD / 2);
-        g = v + slots * (kD / 2);
+        g = v + slots * kVWords;
         q = g + slots * (kD / 2);
         tail = reinterpret_cast<uint2 *>(q + Q * (kD / 2));
         bias = reinterpret_cast<float *>(tail + ((Q + 1) / 2) * 2);
@@ -259,22 +270,23 @@ struct RawView {
     }
 };
 
-__host__ __device__ inline int raw_buffer_bytes(int slots, int Q) {
-    return slots * 3 * (kD * 2) + Q * (kD * 2) + ((Q + 1) / 2) * 16 + kD * 4 + 16 +
+__host__ __device__ inline int raw_buffer_bytes(int slots, int Q, bool corr) {
+    return slots * (corr ? 4 : 3) * (kD * 2) + Q * (kD * 2) + ((Q + 1) / 2) * 16 + kD * 4 + 16 +
            ((Q * 4 + 15) / 16) * 16;
 }
 
-// Shared-memory layout of a launch (window Q, whether the verify folds).
+// Shared-memory layout of a launch (window Q, whether the verify folds, the
+// record format).
 struct Layout {
     int slots, nbuf, tok_bytes, raw_bytes;
     int off_state, off_tok, off_raw, off_list, off_sync, total;
 };
 
-__host__ __device__ inline Layout make_layout(int Q, bool fold) {
+__host__ __device__ inline Layout make_layout(int Q, bool fold, bool corr) {
     Layout l;
     l.slots = fold ? 2 * Q : Q;
     l.tok_bytes = tok_buffer_bytes(l.slots, Q);
-    l.raw_bytes = raw_buffer_bytes(l.slots, Q);
+    l.raw_bytes = raw_buffer_bytes(l.slots, Q, corr);
     l.off_state = 0;                                // 2 x 64 KiB staging
     l.off_tok = 2 * kD * kD * 4;
     const int fixed = l.off_tok + 2 * l.raw_bytes + (int)sizeof(WorkList) + (int)sizeof(Sync);
@@ -389,18 +401,38 @@ __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Curso
 
 // Raw inputs and gate parameters of an item into a raw buffer (cp.async by
 // the producer threads).
-template <Mode kMode>
-__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView rv, int pt) {
+template <Mode kMode, bool kCorr>
+__device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawView<kCorr> rv,
+                                          int pt) {
     const int lane = pt & 31, warp = pt >> 5;
-    const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
-    for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
-        const int u = c / 3;
-        const int part = c - 3 * u;
-        const uint2 *src = reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
-        uint32_t *dst = (part == 0 ? rv.k : (part == 1 ? rv.v : rv.g)) + u * (kD / 2);
-        cp_async8(dst + 2 * lane, src + lane);
+    if constexpr (kCorr) {
+        // recorded tokens: bf16 k and g_raw, fp32 delta (16 bytes per lane)
+        const unsigned char *rec = corr_base(p, w.r, w.head);
+        for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
+            const int u = c / 3;
+            const int part = c - 3 * u;
+            const unsigned char *tok = rec + (size_t)u * kCorrBytes;
+            if (part == 1)
+                cp_async16(rv.v + u * RawView<kCorr>::kVWords + 4 * lane,
+                           reinterpret_cast<const uint4 *>(tok) + lane);
+            else
+                cp_async8((part == 0 ? rv.k : rv.g) + u * (kD / 2) + 2 * lane,
+                          reinterpret_cast<const uint2 *>(tok + (part == 0 ? kCorrK : kCorrG)) +
+                              lane);
+        }
+    } else {
+        const __nv_bfloat16 *rec = record_base(p, w.r, w.head);
+        for (int c = warp; c < 3 * w.p; c += kProducerWarps) {
+            const int u = c / 3;
+            const int part = c - 3 * u;
+            const uint2 *src =
+                reinterpret_cast<const uint2 *>(rec + (size_t)u * kRecStride + part * kD);
+            uint32_t *dst = (part == 0 ? rv.k : (part == 1 ? rv.v : rv.g)) + u * (kD / 2);
+            cp_async8(dst + 2 * lane, src + lane);
+        }
+        if (warp == 0 && lane < w.p)
+            cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
     }
-    if (warp == 0 && lane < w.p) cp_async8(&rv.tail[lane], rec + (size_t)lane * kRecStride + kRecBeta);
     if (warp == kProducerWarps - 2) {
         cp_async16(rv.bias + 4 * lane, p.g_bias + w.head * kD + 4 * lane);
         if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
@@ -417,7 +449,7 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
                 dst = rv.k + (w.p + t) * (kD / 2);
             } else if (part == 1) {
                 src = p.v + tok * p.stride_v;
-                dst = rv.v + (w.p + t) * (kD / 2);
+                dst = rv.v + (w.p + t) * RawView<kCorr>::kVWords;
             } else if (part == 2) {
                 src = p.g + tok * p.stride_g;
                 dst = rv.g + (w.p + t) * (kD / 2);
@@ -434,21 +466,20 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
 // Per-token vectors of an item: token u is prepared by producer warp
 // (u mod 4), four channels per lane, the norms summed across the warp; every
 // token is computed the same way however many tokens the item has.  The
-// verify also writes the new tokens' raw records.
-template <Mode kMode, bool kBounded>
-__device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView rv, TokView tv,
-                                          int pt) {
+// verify also writes the new tokens' records (raw: k, v, g_raw, beta_raw;
+// correction: k and g_raw, the consumer adds the delta).
+template <Mode kMode, bool kBounded, bool kCorr>
+__device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView<kCorr> rv,
+                                          TokView tv, int pt) {
     const int lane = pt & 31, warp = pt >> 5;
     const float a = expf(*rv.a_log);
     const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
-    __nv_bfloat16 *rec = record_base(p, w.r, w.head);
     for (int u = warp; u < w.p + w.T; u += kProducerWarps) {
         const bool is_new = kMode == Mode::kVerify && u >= w.p;
         const int t = u - w.p;
+        const uint32_t *vslot = rv.v + u * RawView<kCorr>::kVWords;
         const uint2 kb = reinterpret_cast<const uint2 *>(rv.k + u * (kD / 2))[lane];
-        const uint2 vb = reinterpret_cast<const uint2 *>(rv.v + u * (kD / 2))[lane];
         const uint2 gb = reinterpret_cast<const uint2 *>(rv.g + u * (kD / 2))[lane];
-        const uint32_t bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
         const float4 k = bf16x4_to_float4(kb);
         float s = __fmul_rn(k.x, k.x);
         s = __fmaf_rn(k.y, k.y, s);
@@ -465,8 +496,18 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
         e.z = decay_factor(__fadd_rn(g.z, bias.z), a, kBounded, p.lower_bound);
         e.w = decay_factor(__fadd_rn(g.w, bias.w), a, kBounded, p.lower_bound);
         *reinterpret_cast<float4 *>(tv.e + u * kD + 4 * lane) = e;
-        *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
-        if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+        uint2 vb = make_uint2(0u, 0u);
+        uint32_t bb = 0u;
+        if (kCorr && !is_new) {
+            // a recorded token's delta, as stored
+            *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) =
+                reinterpret_cast<const float4 *>(vslot)[lane];
+        } else {
+            vb = reinterpret_cast<const uint2 *>(vslot)[lane];
+            bb = is_new ? rv.beta_new[t] : (rv.tail[u].x & 0xffffu);
+            *reinterpret_cast<float4 *>(tv.v + u * kD + 4 * lane) = bf16x4_to_float4(vb);
+            if (lane == 0) tv.beta[u] = sigmoidf_rn(bf16_bits_to_float(bb));
+        }
         if (is_new) {
             const float4 q = bf16x4_to_float4(reinterpret_cast<const uint2 *>(rv.q + t * (kD / 2))[lane]);
             float sq = __fmul_rn(q.x, q.x);
@@ -486,11 +527,20 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
                             __fmul_rn(__fmul_rn(q.w, iq), p.scale));
             // k^ . q^ from the raw dot product and the two norms
             if (lane == 0) tv.kq[t] = __fmul_rn(__fmul_rn(__fmul_rn(dkq, ik), iq), p.scale);
-            uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
-            dst[lane] = kb;
-            dst[kRecV / 4 + lane] = vb;
-            dst[kRecG / 4 + lane] = gb;
-            if (lane == 0) reinterpret_cast<uint16_t *>(rec + (size_t)t * kRecStride)[kRecBeta] = (uint16_t)bb;
+            if constexpr (kCorr) {
+                unsigned char *tok = corr_base(p, w.r, w.head) + (size_t)t * kCorrBytes;
+                reinterpret_cast<uint2 *>(tok + kCorrK)[lane] = kb;
+                reinterpret_cast<uint2 *>(tok + kCorrG)[lane] = gb;
+            } else {
+                __nv_bfloat16 *rec = record_base(p, w.r, w.head);
+                uint2 *dst = reinterpret_cast<uint2 *>(rec + (size_t)t * kRecStride);
+                dst[lane] = kb;
+                dst[kRecV / 4 + lane] = vb;
+                dst[kRecG / 4 + lane] = gb;
+                if (lane == 0)
+                    reinterpret_cast<uint16_t *>(rec + (size_t)t * kRecStride)[kRecBeta] =
+                        (uint16_t)bb;
+            }
         }
     }
 }
@@ -510,9 +560,10 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
 constexpr int kStageThread = kProducerThreads - 32;
 constexpr int kHandoffThread = 32;
 
-template <Mode kMode, bool kBounded>
+template <Mode kMode, bool kBounded, bool kCorr>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
                              int num_tiles, int pt) {
+    using Raw = RawView<kCorr>;
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
     Cursor cursor{0, 0, 0};
@@ -520,7 +571,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     int rb = 0;
     uint32_t beta_next = 0;
     if (cur.tile >= 0) {
-        fetch_raw<kMode>(p, cur, RawView(smem + lay.off_raw, lay.slots, p.Q), pt);
+        fetch_raw<kMode, kCorr>(p, cur, Raw(smem + lay.off_raw, lay.slots, p.Q), pt);
         if (kMode == Mode::kVerify && pt < cur.T)
             beta_next = reinterpret_cast<const uint16_t *>(
                 p.beta)[(size_t)(cur.bos + pt) * p.stride_beta + cur.head];
@@ -538,13 +589,13 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
                             &sy.full_state[c]);
         }
         // raw inputs of `cur` have landed; start those of the next item
-        RawView rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
+        Raw rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
         cp_async_wait_all();
         if (kMode == Mode::kVerify && pt < cur.T) rv.beta_new[pt] = beta_next;
         const Work nxt = next_work<kMode>(p, list, cursor, num_tiles, pt);  // has barriers
         if (nxt.tile >= 0) {
-            fetch_raw<kMode>(p, nxt, RawView(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes,
-                                             lay.slots, p.Q), pt);
+            fetch_raw<kMode, kCorr>(
+                p, nxt, Raw(smem + lay.off_raw + (rb ^ 1) * lay.raw_bytes, lay.slots, p.Q), pt);
             if (kMode == Mode::kVerify && pt < nxt.T)
                 beta_next = reinterpret_cast<const uint16_t *>(
                     p.beta)[(size_t)(nxt.bos + pt) * p.stride_beta + nxt.head];
@@ -560,7 +611,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         producer_sync();
         if (sy.leave[n & 1]) return;
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
-        prep_item<kMode, kBounded>(p, cur, rv, tv, pt);
+        prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt);
         if (pt == kHandoffThread) {
             ItemInfo &it = sy.info[c][b];
             it.head = cur.head;
@@ -571,6 +622,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             it.dst = cur.dst;
             it.mid = cur.mid;
             it.mid_len = cur.mid_len;
+            it.r = cur.r;
         }
         producer_sync();  // all token vectors and the item info written
         if (pt == kHandoffThread) mbar_arrive(&sy.full_tok[c][b]);
@@ -591,7 +643,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-template <Mode kMode>
+template <Mode kMode, bool kCorr>
 __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout &lay, int c,
                              int ct) {
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
@@ -613,7 +665,10 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         mbar_arrive(&sy.empty_state[c]);
         const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         for (int u = 0; u < it.p; ++u) {
-            token_plain(h, tv, u, L);
+            if constexpr (kCorr)
+                token_corr(h, tv, u, L);
+            else
+                token_plain(h, tv, u, L);
             if constexpr (kMode == Mode::kCommit) {
                 if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
                     store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD),
@@ -624,7 +679,10 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         if constexpr (kMode == Mode::kVerify) {
             for (int t = 0; t < it.T; ++t) {
                 const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
-                token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
+                const float vp = token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
+                if constexpr (kCorr)  // the token's delta into its correction record
+                    reinterpret_cast<float *>(corr_base(p, it.r, it.head) +
+                                              (size_t)t * kCorrBytes)[L.row(L.j)] = vp;
                 if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
             }
         }
@@ -632,11 +690,11 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-template <Mode kMode, bool kBounded>
+template <Mode kMode, bool kBounded, bool kCorr>
 __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
                                                                   int fold) {
     extern __shared__ __align__(128) unsigned char smem[];
-    const Layout lay = make_layout(p.Q, fold != 0);
+    const Layout lay = make_layout(p.Q, fold != 0, kCorr);
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -661,10 +719,10 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
     // 2 * 128 * kConsumerRegs + 128 * kProducerRegs == 384 * kLaunchRegs.
     if (tid < 2 * kConsumerThreads) {
         reg_alloc<kConsumerRegs>();
-        run_consumer<kMode>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
+        run_consumer<kMode, kCorr>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
     } else {
         reg_dealloc<kProducerRegs>();
-        run_producer<kMode, kBounded>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
+        run_producer<kMode, kBounded, kCorr>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
     }
 }
 
@@ -692,6 +750,9 @@ kda_status check_config(const kda_config *cfg) {
     if (cfg->use_lower_bound == 1 && !(cfg->lower_bound < 0.0f && isfinite(cfg->lower_bound)))
         return KDA_ERR_INVALID_ARG;
     if (!isfinite(cfg->scale)) return KDA_ERR_INVALID_ARG;
+    if (cfg->record_format != KDA_RECORDS_RAW && cfg->record_format != KDA_RECORDS_CORRECTION)
+        return KDA_ERR_INVALID_ARG;
+    if (cfg->reserved != 0) return KDA_ERR_INVALID_ARG;
     return KDA_OK;
 }
 
@@ -745,14 +806,17 @@ int sm_count() {
 // Launch the warp-specialized step kernel: one CTA per SM (or one per tile
 // when there are fewer tiles), the shared-memory layout sized by the window.
 template <kda::Mode M>
-kda_status launch_step(const Params &p, bool bounded, bool fold, cudaStream_t stream) {
+kda_status launch_step(const Params &p, const kda_config *cfg, bool fold, cudaStream_t stream) {
     const long long tiles = (long long)p.B * p.H;
     const int sms = sm_count();
     if (sms <= 0) return KDA_ERR_CUDA;
     const int grid = (int)(tiles < (long long)sms ? tiles : (long long)sms);
-    const kda::Layout lay = kda::make_layout(p.Q, fold);
+    const bool bounded = cfg->use_lower_bound != 0;
+    const bool corr = cfg->record_format == KDA_RECORDS_CORRECTION;
+    const kda::Layout lay = kda::make_layout(p.Q, fold, corr);
     void (*kern)(const Params, int, int) =
-        bounded ? kda::step_kernel<M, true> : kda::step_kernel<M, false>;
+        corr ? (bounded ? kda::step_kernel<M, true, true> : kda::step_kernel<M, false, true>)
+             : (bounded ? kda::step_kernel<M, true, false> : kda::step_kernel<M, false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -806,6 +870,12 @@ size_t kda_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots
            (size_t)KDA_RECORD_STRIDE * 2u;
 }
 
+size_t kda_correction_records_bytes(int32_t num_heads, int32_t window, int32_t record_slots) {
+    if (num_heads < 1 || window < 1 || window > KDA_MAX_WINDOW || record_slots < 0) return 0;
+    return (size_t)(record_slots + 1) * (size_t)num_heads * (size_t)window *
+           (size_t)KDA_CORRECTION_RECORD_BYTES;
+}
+
 kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const void *v,
                       const void *g_raw, const void *beta_raw, const float *A_log,
                       const float *g_bias, float *state_pool, const int32_t *cu_seqlens,
@@ -847,7 +917,7 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     p.traj = trajectory_out;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kVerify>(p, cfg->use_lower_bound != 0, pending != nullptr,
+    return launch_step<kda::Mode::kVerify>(p, cfg, pending != nullptr,
                                            static_cast<cudaStream_t>(stream));
 }
 
@@ -880,8 +950,7 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     p.eager = eager;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,
-                                           static_cast<cudaStream_t>(stream));
+    return launch_step<kda::Mode::kCommit>(p, cfg, false, static_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const float *g_bias,
@@ -912,8 +981,7 @@ kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const flo
     p.records = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(records));
     p.err = error_word;
 
-    return launch_step<kda::Mode::kCommit>(p, cfg->use_lower_bound != 0, false,
-                                           static_cast<cudaStream_t>(stream));
+    return launch_step<kda::Mode::kCommit>(p, cfg, false, static_cast<cudaStream_t>(stream));
 }
 
 kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_bias,
@@ -938,8 +1006,7 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
     p.pending_in = pending;
     p.err = error_word;
 
-    return launch_step<kda::Mode::kFlush>(p, cfg->use_lower_bound != 0, false,
-                                          static_cast<cudaStream_t>(stream));
+    return launch_step<kda::Mode::kFlush>(p, cfg, false, static_cast<cudaStream_t>(stream));
 }
 
 const char *kda_status_string(kda_status status) {
@@ -952,6 +1019,6 @@ const char *kda_status_string(kda_status status) {
     return "KDA_ERR_UNKNOWN";
 }
 
-int32_t kda_abi_version(void) { return 2; }
+int32_t kda_abi_version(void) { return 3; }
 
 }  // extern "C"

@@ -36,8 +36,8 @@ def oracle_step(wl: W.Workload, step: int = 0, cu_seqlens=None, state_indices=No
                   record_rows=None if rr is None else np.asarray(rr))
 
 
-def oracle_cache(wl: W.Workload) -> O.Cache:
-    return O.Cache(wl.pool.numpy(), wl.spec.record_slots)
+def oracle_cache(wl: W.Workload, record_format: str = "raw") -> O.Cache:
+    return O.Cache(wl.pool.numpy(), wl.spec.record_slots, record_format=record_format)
 
 
 # --------------------------------------------------------------- GPU side --
@@ -45,10 +45,12 @@ def oracle_cache(wl: W.Workload) -> O.Cache:
 class GpuRun:
     """Device copies of a workload plus the buffers the library writes."""
 
-    def __init__(self, wl: W.Workload, device="cuda", with_traj=False, sentinel=True):
+    def __init__(self, wl: W.Workload, device="cuda", with_traj=False, sentinel=True,
+                 record_format="raw"):
         from linear_attention_speculative_kda_gb300 import api
         sp = wl.spec
         self.wl = wl
+        self.record_format = record_format
         self.dev = torch.device(device)
         d = self.dev
         self.A_log = wl.A_log.to(d)
@@ -65,7 +67,8 @@ class GpuRun:
                 num_accepted=st.num_accepted.to(d),
                 eager=None if st.eager is None else st.eager.to(d)))
         T = wl.total_tokens
-        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d)
+        self.records = api.allocate_records(sp.H, sp.Q, sp.record_slots, d,
+                                            record_format=record_format)
         self.out = torch.empty((T, sp.H, sp.D), dtype=torch.bfloat16, device=d)
         if sentinel:
             self.records.fill_(-7.0)
@@ -78,7 +81,8 @@ class GpuRun:
     def kw(self):
         sp = self.wl.spec
         return dict(window=sp.Q, record_slots=sp.record_slots,
-                    lower_bound=sp.lower_bound if sp.bounded else None)
+                    lower_bound=sp.lower_bound if sp.bounded else None,
+                    record_format=self.record_format)
 
     def verify(self, step=0, pending=False, cu=None, slots=None, record_rows="default"):
         from linear_attention_speculative_kda_gb300 import api

@@ -58,14 +58,16 @@ def test_single_rank_reductions_are_identity():
     assert bench.sum_over_ranks(7.0, 1, None) == 7.0
 
 
-def _bytes_by_loops(wl):
+def _bytes_by_loops(wl, tok=2052, rec=770):
     """Per-row loop of the algorithmic byte count: the state tile read once per
-    live row, 2052 bytes per verified token, and 131072 + 770 bytes per
-    replayed token for a commit, counted one row at a time."""
+    live row, `tok` bytes per verified token (raw records: q, k, v, g_raw
+    read, 2 bytes of beta, 256 of output, 770 of record written), and `rec`
+    bytes per replayed record token on top of a commit's state read and
+    write, counted one row at a time."""
     sp = wl.spec
     lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
     slots = wl.state_indices.tolist()
-    state, tok, rec = 65536, 2052, 770
+    state = 65536
 
     def n_of(acc, T):
         return min(max(acc, 0), T, sp.Q)
@@ -112,6 +114,19 @@ def test_plan_bytes_deferred():
     assert names == ["verify", "commit_deferred", "verify_fused", "commit"]
     assert [b for _, b in bench.plan_bytes(wl)] == _bytes_by_loops(wl)
     assert bench.units_per_step(wl) == 2 * 32 * 3
+
+
+def test_plan_bytes_correction_records():
+    # correction records: 1024 bytes per token (fp32 delta, bf16 k and g_raw)
+    # written by the verify and read by a replay; a verified token then moves
+    # 4 * 256 + 2 + 256 + 1024 bytes
+    wl = W.custom(B=32, H=3, Q=4, lens=[4] * 30 + [0, 2], S=40, R=36, deferred=True, steps=2,
+                  seed=5, slots=[0] * 3 + list(range(4, 33)))
+    got = [b for _, b in bench.plan_bytes(wl, "correction")]
+    assert got == _bytes_by_loops(wl, tok=2306, rec=1024)
+    wl1 = W.generate("tiny")
+    assert [b for _, b in bench.plan_bytes(wl1, "correction")] == _bytes_by_loops(
+        wl1, tok=2306, rec=1024)
 
 
 def test_clock_summary_filters_the_timed_window():

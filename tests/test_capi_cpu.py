@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(api.EXPORTED)
     for name in names:
         assert hasattr(lib, name), name
-    assert lib.kda_abi_version() == 2
+    assert lib.kda_abi_version() == 3
     assert lib.kda_status_string(api.KDA_ERR_CUDA) == b"KDA_ERR_CUDA"
 
 
@@ -43,6 +43,39 @@ def test_records_bytes(lib):
     assert api.kda_records_bytes(0, 4, 4) == 0
     assert api.kda_records_bytes(4, 9, 4) == 0
     assert api.kda_records_bytes(4, 4, -1) == 0
+
+
+def test_correction_records_bytes(lib):
+    # fp32 delta + bf16 k + bf16 g_raw = 1024 bytes per token, scratch row included
+    assert api.kda_correction_records_bytes(16, 4, 1024) == 1025 * 16 * 4 * 1024
+    assert api.kda_correction_records_bytes(1, 8, 0) == 8 * 1024
+    assert api.kda_correction_records_bytes(0, 4, 4) == 0
+    assert api.kda_correction_records_bytes(4, 9, 4) == 0
+    assert api.records_bytes(2, 4, 3, "correction") == 4 * 2 * 4 * 1024
+    assert api.records_bytes(2, 4, 3, "raw") == api.kda_records_bytes(2, 4, 3)
+    with pytest.raises(ValueError):
+        api.records_bytes(2, 4, 3, "fp8")
+
+
+def test_record_format_host_checks(lib):
+    cfg = _cfg()
+    cfg.record_format = 2
+    assert _verify(lib, cfg) == api.KDA_ERR_INVALID_ARG
+    cfg = _cfg()
+    cfg.reserved = 1
+    assert _verify(lib, cfg) == api.KDA_ERR_INVALID_ARG
+    cfg = _cfg()
+    cfg.record_format = 1
+    c = ctypes.byref(cfg)
+    assert _verify(lib, cfg, q=None) == api.KDA_ERR_INVALID_ARG   # format fine, pointer not
+    assert lib.kda_flush(c, FAKE, FAKE, FAKE, FAKE, 3, None, FAKE, None, None,
+                         None) == api.KDA_ERR_INVALID_ARG
+    bad = _cfg()
+    bad.record_format = -1
+    assert lib.kda_commit(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, 3, FAKE, None, FAKE,
+                          None, None, None, None) == api.KDA_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        api.make_config(2, 4, 8, 4, record_format="fp16")
 
 
 FAKE = 0x100000  # an aligned address that is never dereferenced
