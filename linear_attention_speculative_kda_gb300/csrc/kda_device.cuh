@@ -165,6 +165,45 @@ __device__ __forceinline__ float2 fma2(float ax, float ay, float bx, float by, f
     return unpack2(d);
 }
 
+__device__ __forceinline__ float4 ld4(const float *ptr) {
+    return *reinterpret_cast<const float4 *>(ptr);
+}
+
+__device__ __forceinline__ float4 mul4(float4 a, float4 b) {
+    return make_float4(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y), __fmul_rn(a.z, b.z),
+                       __fmul_rn(a.w, b.w));
+}
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+    float d = __fmul_rn(a.x, b.x);
+    d = __fmaf_rn(a.y, b.y, d);
+    d = __fmaf_rn(a.z, b.z, d);
+    return __fmaf_rn(a.w, b.w, d);
+}
+
+// Sums 16 values over the 32 lanes of a warp: a reduce-scatter over lane bits
+// 3..0 (each step keeps half of the values and adds the partner's other
+// half), then one exchange across lane bit 4.  Lane l ends with the sum of
+// value (l & 15) over all lanes, in a fixed order.
+__device__ __forceinline__ float reduce16(const float (&x)[16], int lane) {
+    float y8[8], y4[4], y2[2];
+    const bool h8 = (lane & 8) != 0, h4 = (lane & 4) != 0, h2 = (lane & 2) != 0,
+               h1 = (lane & 1) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        y8[i] = __fadd_rn(h8 ? x[i + 8] : x[i], __shfl_xor_sync(kFull, h8 ? x[i] : x[i + 8], 8));
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        y4[i] = __fadd_rn(h4 ? y8[i + 4] : y8[i],
+                          __shfl_xor_sync(kFull, h4 ? y8[i] : y8[i + 4], 4));
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        y2[i] = __fadd_rn(h2 ? y4[i + 2] : y4[i],
+                          __shfl_xor_sync(kFull, h2 ? y4[i] : y4[i + 2], 2));
+    const float y1 = __fadd_rn(h1 ? y2[1] : y2[0], __shfl_xor_sync(kFull, h1 ? y2[0] : y2[1], 1));
+    return __fadd_rn(y1, __shfl_xor_sync(kFull, y1, 16));
+}
+
 __device__ __forceinline__ void flag_error(int *err, int bits) {
     if (err != nullptr) atomicOr(err, bits);
 }
@@ -172,9 +211,12 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 // ------------------------------------------------------- token vectors --
 //
 // One buffer of per-token vectors (fp32): slots [0, p) are folded (recorded)
-// tokens, [p, p + T) the new ones; q^ only for new tokens.
+// tokens, [p, p + T) the new ones; q^ only for new tokens.  In the verify's
+// window form (see token_window) a new token's kh and qh slots hold the
+// decay-weighted G_t * k^_t and G_t * q^_t instead, and pa / pb the pair
+// coefficients of the window (Q x Q each, row t, column s).
 struct TokView {
-    float *kh, *e, *v, *qh, *beta, *kq;
+    float *kh, *e, *v, *qh, *beta, *kq, *pa, *pb;
     __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q) {
         kh = reinterpret_cast<float *>(base);
         e = kh + slots * kD;
@@ -182,11 +224,14 @@ struct TokView {
         qh = v + slots * kD;
         beta = qh + Q * kD;
         kq = beta + ((slots + 3) / 4) * 4;  // k^ . q^ of each new token
+        pa = kq + ((Q + 3) / 4) * 4;
+        pb = pa + Q * Q;
     }
 };
 
 __host__ __device__ inline int tok_buffer_bytes(int slots, int Q) {
-    return (3 * slots + Q) * kD * 4 + ((slots + 3) / 4) * 16 + ((Q + 3) / 4) * 16;
+    return (3 * slots + Q) * kD * 4 + ((slots + 3) / 4) * 16 + ((Q + 3) / 4) * 16 +
+           ((2 * Q * Q + 3) / 4) * 16;
 }
 
 // ------------------------------------------------------------ state tile --
@@ -390,6 +435,136 @@ __device__ __forceinline__ float token_out(Tile &h, const TokView &tv, int slot,
     out_row[L.row(L.j)] = __float2bfloat16_rn(__fmaf_rn(vp, tv.kq[qslot], dq));
     delta_update_vp(h, tv, slot, vp, L);
     return vp;
+}
+
+// ------------------------------------------------------------ window form --
+//
+// A verify never stores the state after its new tokens, so their outputs can
+// be taken from the state S they start from (the checkpoint, or the state
+// after the fold) without updating it.  With G_t = e_1 ... e_t and
+// r_st = e_{s+1} ... e_t per channel (r_tt = 1), the recurrence unrolls to
+//   S_t = S diag(G_t) + sum_{s<=t} v'_s (k^_s * r_st)^T,
+// so token t's prediction is w_t + sum_{s<t} a_ts v'_s and its output
+// o_t = y_t + sum_{s<=t} b_ts v'_s, where
+//   w_t = S (G_t * k^_t),  y_t = S (G_t * q^_t),
+//   a_ts = sum_c k^_s r_st k^_t,  b_ts = sum_c k^_s r_st q^_t.
+// Each consumer prepares, for its own item and before its tile is loaded,
+// G_t * k^_t and G_t * q^_t (into the kh and qh slots) and the pair
+// coefficients (window_prep); it then takes the 2T row dot products with S,
+// which do not depend on one another, and solves each row's deltas
+// v'_t = beta_t (v_t - w_t - sum_{s<t} a_ts v'_s) in token order
+// (window_outputs).  The outputs round differently from the token-by-token
+// form; the states (the commit's, the fold's, the trajectory) are not
+// computed this way.
+
+// One row s of the pair coefficients, this lane's four channels: for
+// t = s .. T-1, x = k^_s * r_st, b_ts = x . q^_t and (t > s) a_ts = x . k^_t,
+// into val[] at slots 2d (b) and 2d - 1 (a) for d = t - s, or mirrored
+// (15 - 2d and 16 - 2d) for a warp's second row.
+template <bool kSecond>
+__device__ __forceinline__ void pair_row(const TokView &tv, int p0, int T, int s, int lane,
+                                         float (&val)[16]) {
+    const float4 ks = ld4(tv.kh + (p0 + s) * kD + 4 * lane);
+    float4 r = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+#pragma unroll
+    for (int d = 0; d < kMaxQ; ++d) {
+        if (s + d < T) {
+            const int t = s + d;
+            if (d > 0) r = mul4(r, ld4(tv.e + (p0 + t) * kD + 4 * lane));
+            const float4 x = mul4(ks, r);
+            val[kSecond ? 15 - 2 * d : 2 * d] = dot4(x, ld4(tv.qh + t * kD + 4 * lane));
+            if (d > 0)
+                val[kSecond ? 16 - 2 * d : 2 * d - 1] =
+                    dot4(x, ld4(tv.kh + (p0 + t) * kD + 4 * lane));
+        }
+    }
+}
+
+// The window's coefficients of tokens p0 .. p0 + T - 1, by the 128 threads of
+// a group (thread ct): warp wi the pair coefficients of rows s = wi and
+// s = T - 1 - wi (2T values, so the warps are balanced), and each thread the
+// decay-weighted G_t * k^_t and G_t * q^_t of channel ct, which replace k^_t
+// and q^_t once every warp has read them.  group_sync() is the group's
+// barrier; false means it gave up (the caller leaves), and so does this.
+template <class GroupSync>
+__device__ __forceinline__ bool window_prep(const TokView &tv, int p0, int T, int Q, int ct,
+                                            GroupSync &&group_sync) {
+    const int lane = ct & 31, warp = ct >> 5;
+    if (warp < (T + 1) / 2) {
+        float val[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) val[i] = 0.0f;
+        const int s0 = warp, s1 = T - 1 - warp;
+        pair_row<false>(tv, p0, T, s0, lane, val);
+        if (s1 != s0) pair_row<true>(tv, p0, T, s1, lane, val);
+        const float sum = reduce16(val, lane);
+        if (lane < 16) {
+            int s = -1, slot = lane;
+            if (slot <= 2 * (T - 1 - s0)) {
+                s = s0;
+            } else if (s1 != s0 && slot >= 15 - 2 * (T - 1 - s1)) {
+                s = s1;
+                slot = 15 - slot;
+            }
+            if (s >= 0) {
+                const int d = (slot + 1) >> 1;
+                float *dst = (slot & 1) ? tv.pa : tv.pb;
+                dst[(s + d) * Q + s] = sum;
+            }
+        }
+    }
+    float gk[kMaxQ], gq[kMaxQ];
+    float G = 1.0f;
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            G = __fmul_rn(G, tv.e[(p0 + t) * kD + ct]);
+            gk[t] = __fmul_rn(G, tv.kh[(p0 + t) * kD + ct]);
+            gq[t] = __fmul_rn(G, tv.qh[t * kD + ct]);
+        }
+    }
+    if (!group_sync()) return false;  // every read of k^ and q^ done
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            tv.kh[(p0 + t) * kD + ct] = gk[t];
+            tv.qh[t * kD + ct] = gq[t];
+        }
+    }
+    return group_sync();  // the coefficients and vectors are in place
+}
+
+// The T new tokens' outputs (row L.row(L.j) per thread) to
+// out0 + t * out_stride.  The new tokens' e and v slots serve as per-row
+// scratch (v - w and y): only this thread reads its row there.
+__device__ __forceinline__ void window_outputs(const Tile &h, const TokView &tv, int p, int T,
+                                               int Q, const Lane &L, __nv_bfloat16 *out0,
+                                               size_t out_stride) {
+    const int row = L.row(L.j);
+    for (int t = 0; t < T; ++t) {
+        float pw[8], py[8];
+        row_partials2(h, tv.kh + (p + t) * kD, tv.qh + t * kD, L, pw, py);
+        const float w = reduce_rows(pw, L.j);
+        const float y = reduce_rows(py, L.j);
+        const int ix = (p + t) * kD + row;
+        tv.e[ix] = __fsub_rn(tv.v[ix], w);
+        tv.v[ix] = y;
+    }
+    float vp[kMaxQ];
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            const int ix = (p + t) * kD + row;
+            float acc = tv.e[ix];
+#pragma unroll
+            for (int s = 0; s < t; ++s) acc = __fmaf_rn(-tv.pa[t * Q + s], vp[s], acc);
+            vp[t] = __fmul_rn(tv.beta[p + t], acc);
+            float o = tv.v[ix];
+#pragma unroll
+            for (int s = 0; s <= t; ++s) o = __fmaf_rn(tv.pb[t * Q + s], vp[s], o);
+            out0[(size_t)t * out_stride + row] = __float2bfloat16_rn(o);
+        }
+    }
 }
 
 }  // namespace kda

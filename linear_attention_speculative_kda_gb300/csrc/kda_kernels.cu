@@ -241,6 +241,7 @@ struct Sync {
     uint64_t empty_state[2];   // the consumer has copied it into registers
     uint64_t full_tok[2][2];   // token vectors of an item are ready
     uint64_t empty_tok[2][2];  // the consumer is done with them
+    uint64_t group[2];         // a consumer's own barrier (window form)
     ItemInfo info[2][2];
     int abort;
     int leave[2];   // per item parity: the producer threads leave (abort seen)
@@ -470,7 +471,7 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
 // correction: k and g_raw, the consumer adds the delta).
 template <Mode kMode, bool kBounded, bool kCorr>
 __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView<kCorr> rv,
-                                          TokView tv, int pt) {
+                                          const TokView &tv, int pt) {
     const int lane = pt & 31, warp = pt >> 5;
     const float a = expf(*rv.a_log);
     const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
@@ -560,7 +561,7 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
 constexpr int kStageThread = kProducerThreads - 32;
 constexpr int kHandoffThread = 32;
 
-template <Mode kMode, bool kBounded, bool kCorr>
+template <Mode kMode, bool kBounded, bool kCorr, bool kWindow>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
                              int num_tiles, int pt) {
     using Raw = RawView<kCorr>;
@@ -643,7 +644,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-template <Mode kMode, bool kCorr>
+template <Mode kMode, bool kCorr, bool kWindow>
 __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout &lay, int c,
                              int ct) {
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
@@ -653,17 +654,27 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     L.g = L.lane >> 3;
     L.j = L.lane & 7;
     const float *staging = reinterpret_cast<const float *>(smem + lay.off_state) + c * kD * kD;
+    // the group's barrier: an mbarrier, so that its wait is bounded like the
+    // others and every thread leaves on an abort
+    uint32_t group_uses = 0;
+    auto group_sync = [&]() -> bool {
+        mbar_arrive(&sy.group[c]);
+        return wait_phase(&sy.group[c], group_uses++ & 1, sy, p);
+    };
     for (int k = 0;; ++k) {
         const int b = k % lay.nbuf;
         const int use_b = k / lay.nbuf;
         if (!wait_phase(&sy.full_tok[c][b], use_b & 1, sy, p)) return;
         const ItemInfo it = sy.info[c][b];
         if (it.end) return;
+        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
+        // the window form's coefficients, before the tile occupies registers
+        if constexpr (kWindow)
+            if (it.T > 0 && !window_prep(tv, it.p, it.T, p.Q, ct, group_sync)) return;
         if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
         Tile h;
         load_tile(h, staging, L);
         mbar_arrive(&sy.empty_state[c]);
-        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         for (int u = 0; u < it.p; ++u) {
             if constexpr (kCorr)
                 token_corr(h, tv, u, L);
@@ -676,7 +687,11 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
             }
         }
         if (it.p > 0) store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
-        if constexpr (kMode == Mode::kVerify) {
+        if constexpr (kWindow) {
+            if (it.T > 0)
+                window_outputs(h, tv, it.p, it.T, p.Q, L,
+                               p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
+        } else if constexpr (kMode == Mode::kVerify) {
             for (int t = 0; t < it.T; ++t) {
                 const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
                 const float vp = token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
@@ -690,9 +705,12 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-template <Mode kMode, bool kBounded, bool kCorr>
+// kWindow: the verify's new tokens in window form (raw records, no
+// trajectory output); otherwise token by token.
+template <Mode kMode, bool kBounded, bool kCorr, bool kWindow>
 __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
                                                                   int fold) {
+    static_assert(!kWindow || (kMode == Mode::kVerify && !kCorr), "window form: raw verify only");
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout lay = make_layout(p.Q, fold != 0, kCorr);
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
@@ -701,6 +719,7 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
         for (int c = 0; c < 2; ++c) {
             mbar_init(&sy.full_state[c], 1);
             mbar_init(&sy.empty_state[c], kConsumerThreads);
+            mbar_init(&sy.group[c], kConsumerThreads);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&sy.full_tok[c][b], 1);
                 mbar_init(&sy.empty_tok[c][b], kConsumerThreads);
@@ -719,10 +738,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
     // 2 * 128 * kConsumerRegs + 128 * kProducerRegs == 384 * kLaunchRegs.
     if (tid < 2 * kConsumerThreads) {
         reg_alloc<kConsumerRegs>();
-        run_consumer<kMode, kCorr>(p, smem, lay, tid / kConsumerThreads, tid % kConsumerThreads);
+        run_consumer<kMode, kCorr, kWindow>(p, smem, lay, tid / kConsumerThreads,
+                                            tid % kConsumerThreads);
     } else {
         reg_dealloc<kProducerRegs>();
-        run_producer<kMode, kBounded, kCorr>(p, smem, lay, num_tiles, tid - 2 * kConsumerThreads);
+        run_producer<kMode, kBounded, kCorr, kWindow>(p, smem, lay, num_tiles,
+                                                      tid - 2 * kConsumerThreads);
     }
 }
 
@@ -803,6 +824,31 @@ int sm_count() {
     return n;
 }
 
+// When a verify runs its new tokens in window form: at most this many tiles
+// per SM, and a window of at least kWindowMinQ tokens.  With few tiles per SM
+// a launch is bound by each item's chain of dependent work, which the window
+// form shortens the more the longer the window; with many it is bound by
+// issue slots and HBM, and the window form's preparation costs more than it
+// saves.  Measured on GB300: 27 tiles per SM with an 8-token window gained
+// 6% of the step; 14 tiles per SM with 4 tokens gained nothing measurable;
+// 108 tiles per SM lost 6% (4 tokens) or broke even (8 tokens).
+constexpr long long kWindowTilesPerSm = 48;
+constexpr int kWindowMinQ = 5;
+
+// The instantiation of a launch: gate, record format, and for a raw-record
+// verify without a trajectory output that qualifies, the window form.
+template <kda::Mode M>
+void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const Params, int,
+                                                                         int) {
+    using kda::step_kernel;
+    if constexpr (M == kda::Mode::kVerify) {
+        if (!corr && !traj && window)
+            return bounded ? step_kernel<M, true, false, true> : step_kernel<M, false, false, true>;
+    }
+    if (corr) return bounded ? step_kernel<M, true, true, false> : step_kernel<M, false, true, false>;
+    return bounded ? step_kernel<M, true, false, false> : step_kernel<M, false, false, false>;
+}
+
 // Launch the warp-specialized step kernel: one CTA per SM (or one per tile
 // when there are fewer tiles), the shared-memory layout sized by the window.
 template <kda::Mode M>
@@ -814,9 +860,9 @@ kda_status launch_step(const Params &p, const kda_config *cfg, bool fold, cudaSt
     const bool bounded = cfg->use_lower_bound != 0;
     const bool corr = cfg->record_format == KDA_RECORDS_CORRECTION;
     const kda::Layout lay = kda::make_layout(p.Q, fold, corr);
+    const bool window = tiles <= kWindowTilesPerSm * sms && p.Q >= kWindowMinQ;
     void (*kern)(const Params, int, int) =
-        corr ? (bounded ? kda::step_kernel<M, true, true> : kda::step_kernel<M, false, true>)
-             : (bounded ? kda::step_kernel<M, true, false> : kda::step_kernel<M, false, false>);
+        step_kernel_for<M>(bounded, corr, p.traj != nullptr, window);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

@@ -9,9 +9,11 @@ Tolerances, as in test_gpu_parity:
 - recorded deltas: per (row, head, token) vector, max |gpu - oracle| <=
   1e-5 * max(1, max |oracle|) (a delta is a difference of O(1) values);
 - recorded k and g_raw: bit-identical copies of the inputs;
-- states and outputs: bit-identical to the raw-record path (the same
-  operations in the same order after v'), and committed states bit-identical
-  to the verify trajectory.
+- states: bit-identical to the raw-record path (the same operations in the
+  same order after v'), and committed states bit-identical to the verify
+  trajectory; outputs: the correction format's verify runs token by token,
+  the raw format's production verify in window form, so they agree to the
+  output tolerance, not bit for bit.
 """
 
 import numpy as np
@@ -59,12 +61,12 @@ def test_verify_records_deltas(name, wl):
     gc.verify()
     torch.cuda.synchronize()
     assert int(gr.err.item()) == 0 and int(gc.err.item()) == 0
-    assert torch.equal(gr.out, gc.out)             # outputs do not depend on the format
     assert torch.equal(gc.pool, gc.pool0)          # a verify without pending stores no state
     layer, step = oracle_layer(wl), oracle_step(wl)
     cache = oracle_cache(wl, "correction")
     res = O.verify(layer, cache, step)
     assert_out_close(gc.out, res.out)
+    assert_out_close(gr.out, res.out)
     delta, k, g_raw = _records(gc)
     cu = wl.cu_seqlens.numpy()
     st = wl.steps[0]
@@ -132,7 +134,7 @@ def test_deferred_fold_and_flush(Q, bounded):
     (gr, fr), (gc, fc) = runs["raw"], runs["correction"]
     for g in (gr, fr, gc, fc):
         assert int(g.err.item()) == 0
-    assert torch.equal(gr.out, gc.out) and torch.equal(gc.out, fc.out)
+    assert torch.equal(gc.out, fc.out) and torch.equal(gr.out, fr.out)
     assert torch.equal(gr.pool, gc.pool) and torch.equal(gc.pool, fc.pool)
     assert torch.equal(fr.pool, fc.pool)
     layer = oracle_layer(wl)
@@ -144,6 +146,7 @@ def test_deferred_fold_and_flush(Q, bounded):
     r2 = O.verify(layer, cache, s2, pending=True)
     O.commit(layer, cache, s2, wl.steps[1].num_accepted.numpy())
     assert_out_close(gc.out, r2.out)
+    assert_out_close(gr.out, r2.out)
     pool = gc.pool.cpu()
     for (slot, h), ref in cache.written.items():
         assert_state_close(pool[slot, h].double().numpy(), ref)
@@ -184,8 +187,8 @@ def test_records_buffer_too_small_is_refused():
 def test_full_size_deferred_two_steps():
     """deferred2 at full size (1024 requests x 16 heads, two steps, the
     benchmark's launch sequence): the correction format gives the raw
-    format's outputs and final states bit for bit, and a sample of tiles
-    matches the oracle."""
+    format's final states bit for bit, and a sample of tiles and outputs
+    matches the oracle in both formats."""
     wl = W.generate("deferred2")
     sp = wl.spec
     ones = torch.ones(sp.B, dtype=torch.uint8, device="cuda")
@@ -201,7 +204,6 @@ def test_full_size_deferred_two_steps():
         outs.append(g.out)
         pools.append(g.pool)
         del g
-    assert torch.equal(outs[0], outs[1])
     assert torch.equal(pools[0], pools[1])
     rng = np.random.default_rng(3)
     rows = sorted(rng.choice(sp.B, size=12, replace=False).tolist())
@@ -215,6 +217,7 @@ def test_full_size_deferred_two_steps():
     r2 = O.verify(layer, cache, s2, pending=True, rows=rows, heads=heads)
     O.commit(layer, cache, s2, wl.steps[1].num_accepted.numpy(), rows=rows, heads=heads)
     assert_out_close(outs[1], r2.out)
+    assert_out_close(outs[0], r2.out)
     assert cache.written
     for (slot, h), ref in cache.written.items():
         assert_state_close(pools[1][slot, h].double().cpu().numpy(), ref)

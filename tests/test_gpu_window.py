@@ -1,0 +1,136 @@
+"""GPU parity of the verify's window form: a raw-record verify without a
+trajectory output, on a grid of at most 48 tiles per SM and with a window of
+at least 5 tokens, computes its new tokens' outputs from the starting state
+in one set of row dot products and a per-row triangular solve, instead of
+token by token (the state is not updated; the commit replays as before).
+The small cases with Q >= 5 here take that form (rows of 1 to Q tokens);
+those with Q <= 4 check that the token-by-token form is kept; the full-size
+ones take whichever form the benchmark runs.
+
+Tolerances, as in test_gpu_parity: bf16 outputs within 2e-3 of the oracle;
+records and every stored state (the fold's, the commit's) bit-identical to
+the token-by-token run, which is itself bit-checked against its trajectory.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from linear_attention_speculative_kda_gb300 import workloads as W
+from oracle import kda_oracle as O
+from tests.helpers import (GpuRun, assert_out_close, assert_state_close, oracle_cache,
+                           oracle_layer, oracle_step)
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases():
+    yield "ragged_q8", W.custom(B=12, H=3, Q=8, lens=[8, 1, 5, 0, 8, 3, 7, 2, 8, 6, 4, 8],
+                                S=16, seed=1)
+    yield "bounded_q8", W.custom(B=10, H=2, Q=8, lens=[8, 8, 2, 7, 5, 8, 1, 3, 8, 6], S=13,
+                                 bounded=True, lower_bound=-5.0, seed=2,
+                                 slots=[3, 0, 5, 7, 0, 1, 9, 11, 2, 12])
+    yield "q1", W.custom(B=6, H=4, Q=1, lens=[1, 1, 0, 1, 1, 1], S=8, seed=3)
+    yield "q2", W.custom(B=7, H=2, Q=2, lens=[2, 1, 2, 2, 0, 2, 1], S=9, seed=5)
+    yield "q3", W.custom(B=7, H=2, Q=3, lens=[3, 1, 2, 3, 3, 0, 2], S=9, seed=6)
+    yield "q5", W.custom(B=6, H=2, Q=5, lens=[5, 4, 5, 1, 3, 5], S=8, seed=7)
+    yield "q7", W.custom(B=8, H=2, Q=7, lens=[7, 6, 1, 7, 2, 7, 5, 3], S=10, seed=8)
+    yield "q4", W.custom(B=9, H=2, Q=4, lens=[4, 4, 2, 4, 0, 3, 4, 1, 4], S=12, seed=4)
+
+
+CASES = list(_cases())
+
+
+@pytest.mark.parametrize("name,wl", CASES, ids=[c[0] for c in CASES])
+def test_window_outputs_records_and_commit(name, wl):
+    gw = GpuRun(wl)                        # window form (no trajectory output)
+    gs = GpuRun(wl, with_traj=True)        # token by token
+    for g in (gw, gs):
+        g.verify()
+        g.commit()
+    torch.cuda.synchronize()
+    assert int(gw.err.item()) == 0 and int(gs.err.item()) == 0
+    assert torch.equal(gw.records, gs.records)
+    assert torch.equal(gw.pool, gs.pool)
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    res = O.verify(layer, oracle_cache(wl), step)
+    assert_out_close(gw.out, res.out)
+    # rows the verify skipped keep the sentinel
+    cu = wl.cu_seqlens.numpy()
+    run = set(res.rows_run)
+    out = gw.out.float().cpu().numpy()
+    for b in range(wl.spec.B):
+        if b not in run:
+            assert (out[cu[b]:cu[b + 1]] == -9.0).all()
+
+
+def test_window_strong_decay_and_large_beta():
+    """Gates near their extremes (decays down to e^-40 per token, so the
+    window's decay products underflow) and beta near 1."""
+    wl = W.custom(B=8, H=2, Q=8, lens=[8] * 8, S=10, seed=12)
+    wl.A_log[:] = torch.tensor([3.2, 0.1])
+    for st in wl.steps:
+        st.g_raw.mul_(3.0)
+        st.beta_buf.add_(4.0)
+    gw = GpuRun(wl)
+    gw.verify()
+    torch.cuda.synchronize()
+    assert int(gw.err.item()) == 0
+    assert torch.isfinite(gw.out.float()).all()
+    res = O.verify(oracle_layer(wl), oracle_cache(wl), oracle_step(wl))
+    assert_out_close(gw.out, res.out)
+
+
+@pytest.mark.parametrize("Q,bounded", [(4, False), (8, True)])
+def test_window_after_fold(Q, bounded):
+    lens = [Q, Q, 2, Q, 1, Q, Q - 1, 0] * 3
+    kw = dict(bounded=True, lower_bound=-5.0) if bounded else {}
+    wl = W.custom(B=len(lens), H=2, Q=Q, lens=lens, S=len(lens) + 6, R=len(lens) + 4,
+                  deferred=True, steps=2, seed=60 + Q, eager_prob=0.25, **kw)
+    gw, gs = GpuRun(wl), GpuRun(wl, with_traj=True)
+    for g in (gw, gs):
+        g.verify(0, pending=True)
+        g.commit(0, deferred=True)
+        g.verify(1, pending=True)
+    torch.cuda.synchronize()
+    assert int(gw.err.item()) == 0 and int(gs.err.item()) == 0
+    assert torch.equal(gw.pool, gs.pool)          # the folded states
+    assert torch.equal(gw.records, gs.records)
+    layer = oracle_layer(wl)
+    cache = oracle_cache(wl)
+    s1, s2 = oracle_step(wl, 0), oracle_step(wl, 1)
+    O.verify(layer, cache, s1, pending=True)
+    O.commit(layer, cache, s1, wl.steps[0].num_accepted.numpy(), deferred=True,
+             eager=wl.steps[0].eager.numpy())
+    r2 = O.verify(layer, cache, s2, pending=True)
+    assert_out_close(gw.out, r2.out)
+    pool = gw.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
+
+
+@pytest.mark.parametrize("name", ["mtp3", "dflash7", "mixed", "deferred2"])
+def test_full_size_window_sampled(name):
+    """The full-size workloads in the benchmark's launch configuration
+    (window form for dflash7, token by token for the others): a sample of
+    (row, head) outputs and committed states against the oracle."""
+    wl = W.generate(name)
+    sp = wl.spec
+    deferred = sp.deferred
+    g = GpuRun(wl, sentinel=False)
+    g.verify(0, pending=deferred)
+    g.commit(0, deferred=deferred)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    rng = np.random.default_rng(1)
+    rows = sorted(rng.choice(sp.B, size=min(sp.B, 24), replace=False).tolist())
+    heads = sorted(rng.choice(sp.H, size=min(sp.H, 3), replace=False).tolist())
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    res = O.verify(layer, cache, step, pending=deferred, rows=rows, heads=heads)
+    acc = wl.steps[0].num_accepted.numpy()
+    eager = None if wl.steps[0].eager is None else wl.steps[0].eager.numpy()
+    O.commit(layer, cache, step, acc, deferred=deferred, eager=eager, rows=rows, heads=heads)
+    assert_out_close(g.out, res.out)
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(g.pool[slot, h].double().cpu().numpy(), ref)
