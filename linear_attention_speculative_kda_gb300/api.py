@@ -11,6 +11,7 @@ raises.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 
 import torch
@@ -165,11 +166,12 @@ def _check(fn: str, status: int) -> None:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes converts it for c_void_p parameters (None is NULL)
+    return None if t is None else t.data_ptr()
 
 
-def _stream_ptr(device) -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+def _stream_ptr(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
 
 
 def _token_stride(t: torch.Tensor) -> int:
@@ -211,6 +213,8 @@ def _format_code(record_format: str) -> int:
 def make_config(num_heads, window, num_slots, record_slots, *, lower_bound=None,
                 scale=None, strides=(1, 1, 1, 1, 1), head_dim=HEAD_DIM,
                 record_format: str = "raw") -> KdaConfig:
+    """A new ``kda_config`` (the entry points below share read-only cached
+    ones, see ``_config``)."""
     cfg = KdaConfig()
     cfg.record_format = _format_code(record_format)
     cfg.reserved = 0
@@ -227,6 +231,16 @@ def make_config(num_heads, window, num_slots, record_slots, *, lower_bound=None,
     return cfg
 
 
+@functools.lru_cache(maxsize=256)
+def _config(num_heads, window, num_slots, record_slots, lower_bound, scale, strides, head_dim,
+            record_format) -> KdaConfig:
+    # the library only reads the config during the call, so one object per
+    # distinct argument set serves every call
+    return make_config(num_heads, window, num_slots, record_slots, lower_bound=lower_bound,
+                       scale=scale, strides=strides, head_dim=head_dim,
+                       record_format=record_format)
+
+
 def kda_records_bytes(num_heads: int, window: int, record_slots: int) -> int:
     """Size in bytes of a raw-format records buffer (``kda_records_bytes``)."""
     return int(load_library().kda_records_bytes(num_heads, window, record_slots))
@@ -238,6 +252,7 @@ def kda_correction_records_bytes(num_heads: int, window: int, record_slots: int)
     return int(load_library().kda_correction_records_bytes(num_heads, window, record_slots))
 
 
+@functools.lru_cache(maxsize=256)
 def records_bytes(num_heads: int, window: int, record_slots: int, record_format: str) -> int:
     _format_code(record_format)
     fn = kda_records_bytes if record_format == "raw" else kda_correction_records_bytes
@@ -302,8 +317,8 @@ def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
         raise ValueError("cu_seqlens must have B + 1 entries")
     strides = (_token_stride(q), _token_stride(k), _token_stride(v), _token_stride(g_raw),
                _token_stride(beta_raw))
-    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound, scale=scale,
-                      strides=strides, head_dim=state_pool.shape[-1], record_format=record_format)
+    cfg = _config(H, window, S, record_slots, lower_bound, scale, strides, state_pool.shape[-1],
+                  record_format)
     _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_verify(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
@@ -338,8 +353,8 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
     if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < B:
         raise ValueError("metadata sizes do not match the batch")
     S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1], record_format=record_format)
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
+                  state_pool.shape[-1], record_format)
     _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_commit(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
@@ -366,8 +381,8 @@ def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, win
         raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
     B = state_indices.shape[0]
     S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1], record_format=record_format)
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
+                  state_pool.shape[-1], record_format)
     _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_flush(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
@@ -470,8 +485,8 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
     if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < block_table.shape[0]:
         raise ValueError("metadata sizes do not match the batch")
     S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = make_config(H, window, S, record_slots, lower_bound=lower_bound,
-                      head_dim=state_pool.shape[-1], record_format=record_format)
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
+                  state_pool.shape[-1], record_format)
     _check_records(records, H, window, record_slots, record_format)
     al = make_align(block_table, num_computed, block_size, request_indices)
     lib = load_library()
