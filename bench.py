@@ -113,18 +113,28 @@ def hbm_peak():
 STEP_SOURCES = ("kda_align.cuh", "kda_async.cuh", "kda_device.cuh", "kda_kernels.cu")
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_text(source: str) -> str:
+    """C/CUDA source without its comments and with its whitespace collapsed
+    (the step sources hold no string literal with comment markers), so that
+    a comment edit does not change the hash below."""
+    return " ".join(_COMMENT.sub(" ", source).split())
+
+
 def kernel_source_hash() -> str:
-    """Hash of the verify / commit kernel's sources: a profile taken on other
-    sources no longer describes the kernel."""
+    """Hash of the verify / commit kernel's code (comments and layout
+    aside): a profile taken on other code no longer describes the kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_speculative_kda_gb300", "csrc")
     for name in STEP_SOURCES:
         path = os.path.join(csrc, name)
         if not os.path.exists(path):
             continue
-        with open(path, "rb") as fh:
+        with open(path, encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

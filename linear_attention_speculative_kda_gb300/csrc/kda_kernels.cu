@@ -9,8 +9,13 @@
 //    the replay of `Glm5NextRecoverSSMCommitContext.commit`, restricted to
 //    the accepted tokens, with the deferred variant of
 //    `KDADeferredCommitContext.commit` (pending / eager);
-//  - flush: `KDADeferredCommitContext.flush`.
-// The public contract is in include/kda.h.
+//  - flush: `KDADeferredCommitContext.flush`;
+//  - with correction records (the Kimi-K3 context page's fp32 corrections),
+//    the verify also records each token's delta, and the commit, the fold
+//    and the flush apply the deltas without the prediction S k^.
+// A verify on a small grid with a long window may compute its outputs in
+// the window form (kda_device.cuh); every stored state is computed token by
+// token.  The public contract is in include/kda.h.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>

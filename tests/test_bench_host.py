@@ -161,8 +161,15 @@ def test_profiled_traffic_requires_current_sources(tmp_path, monkeypatch):
     assert bench.profiled_traffic("commit", "w") is None
     (csrc / "kda_conv.cu").write_text("conv v2")   # not the step kernel's source
     assert bench.profiled_traffic("verify", "w") == 1234.0
+    (csrc / "kda_kernels.cu").write_text("kernel  v1 // a comment\n/* another */")
+    assert bench.profiled_traffic("verify", "w") == 1234.0   # comments and layout only
     (csrc / "kda_kernels.cu").write_text("kernel v2")
     assert bench.profiled_traffic("verify", "w") is None
+
+
+def test_code_text_strips_comments():
+    src = "a = 1; // one\n/* two\n lines */ b  =\t2;"
+    assert bench.code_text(src) == "a = 1; b = 2;"
 
 
 def test_conv_compact_bytes_counts_committed_rows():
