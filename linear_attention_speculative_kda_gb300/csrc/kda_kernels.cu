@@ -13,8 +13,8 @@
 //  - with correction records (the Kimi-K3 context page's fp32 corrections),
 //    the verify also records each token's delta, and the commit, the fold
 //    and the flush apply the deltas without the prediction S k^.
-// A verify on a small grid with a long window may compute its outputs in
-// the window form (kda_device.cuh); every stored state is computed token by
+// A verify item with 5 or more new tokens computes its outputs in the
+// window form (kda_device.cuh); every stored state is computed token by
 // token.  The public contract is in include/kda.h.
 #include <cuda_runtime.h>
 #include <math.h>
@@ -201,6 +201,12 @@ constexpr int kProducerWarps = 4;
 constexpr int kProducerThreads = 32 * kProducerWarps;
 constexpr int kBlockThreads = 2 * kConsumerThreads + kProducerThreads;
 constexpr int kProducerBarrier = 1;  // named barrier of the producer warps
+// A verify item with at least this many new tokens runs them in window form
+// (kWindow kernels).  Measured on GB300: items of 8 tokens gain (dflash7's
+// verify 115 -> 103 us), mixed lengths gain when only their longer items
+// take it (mixed's verify 297 -> 288 us; all items: no gain), and windows of
+// 4 tokens lose (deferred2's verify 245 -> 272 us).
+constexpr int kWindowMinT = 5;
 constexpr int kPlanSize = kProducerThreads;
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 constexpr int kSmemBudget = 227 * 1024;
@@ -674,8 +680,9 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         if (it.end) return;
         const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
         // the window form's coefficients, before the tile occupies registers
+        const bool window = kWindow && it.T >= kWindowMinT;
         if constexpr (kWindow)
-            if (it.T > 0 && !window_prep(tv, it.p, it.T, p.Q, ct, group_sync)) return;
+            if (window && !window_prep(tv, it.p, it.T, p.Q, ct, group_sync)) return;
         if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
         Tile h;
         load_tile(h, staging, L);
@@ -692,10 +699,9 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
             }
         }
         if (it.p > 0) store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
-        if constexpr (kWindow) {
-            if (it.T > 0)
-                window_outputs(h, tv, it.p, it.T, p.Q, L,
-                               p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
+        if (kWindow && window) {
+            window_outputs(h, tv, it.p, it.T, p.Q, L,
+                           p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
         } else if constexpr (kMode == Mode::kVerify) {
             for (int t = 0; t < it.T; ++t) {
                 const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
@@ -710,8 +716,9 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     }
 }
 
-// kWindow: the verify's new tokens in window form (raw records, no
-// trajectory output); otherwise token by token.
+// kWindow: items of the verify with at least kWindowMinT new tokens run them
+// in window form (raw records, no trajectory output); the others, and every
+// other kernel, token by token.
 template <Mode kMode, bool kBounded, bool kCorr, bool kWindow>
 __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
                                                                   int fold) {
@@ -829,19 +836,9 @@ int sm_count() {
     return n;
 }
 
-// When a verify runs its new tokens in window form: at most this many tiles
-// per SM, and a window of at least kWindowMinQ tokens.  With few tiles per SM
-// a launch is bound by each item's chain of dependent work, which the window
-// form shortens the more the longer the window; with many it is bound by
-// issue slots and HBM, and the window form's preparation costs more than it
-// saves.  Measured on GB300: 27 tiles per SM with an 8-token window gained
-// 6% of the step; 14 tiles per SM with 4 tokens gained nothing measurable;
-// 108 tiles per SM lost 6% (4 tokens) or broke even (8 tokens).
-constexpr long long kWindowTilesPerSm = 48;
-constexpr int kWindowMinQ = 5;
-
 // The instantiation of a launch: gate, record format, and for a raw-record
-// verify without a trajectory output that qualifies, the window form.
+// verify without a trajectory output whose window can hold kWindowMinT
+// tokens, the kernel that runs such items in window form.
 template <kda::Mode M>
 void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const Params, int,
                                                                          int) {
@@ -865,9 +862,8 @@ kda_status launch_step(const Params &p, const kda_config *cfg, bool fold, cudaSt
     const bool bounded = cfg->use_lower_bound != 0;
     const bool corr = cfg->record_format == KDA_RECORDS_CORRECTION;
     const kda::Layout lay = kda::make_layout(p.Q, fold, corr);
-    const bool window = tiles <= kWindowTilesPerSm * sms && p.Q >= kWindowMinQ;
     void (*kern)(const Params, int, int) =
-        step_kernel_for<M>(bounded, corr, p.traj != nullptr, window);
+        step_kernel_for<M>(bounded, corr, p.traj != nullptr, p.Q >= kda::kWindowMinT);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,

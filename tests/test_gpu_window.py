@@ -1,11 +1,11 @@
-"""GPU parity of the verify's window form: a raw-record verify without a
-trajectory output, on a grid of at most 48 tiles per SM and with a window of
-at least 5 tokens, computes its new tokens' outputs from the starting state
-in one set of row dot products and a per-row triangular solve, instead of
-token by token (the state is not updated; the commit replays as before).
-The small cases with Q >= 5 here take that form (rows of 1 to Q tokens);
-those with Q <= 4 check that the token-by-token form is kept; the full-size
-ones take whichever form the benchmark runs.
+"""GPU parity of the verify's window form: in a raw-record verify without a
+trajectory output, each item with at least 5 new tokens computes their
+outputs from the starting state in one set of row dot products and a
+per-row triangular solve, instead of token by token (the state is not
+updated; the commit replays as before); shorter items stay token by token.
+The small cases with Q >= 5 here mix both kinds of items in one launch
+(rows of 1 to Q tokens); those with Q <= 4 check that nothing changes for
+them; the full-size ones run as the benchmark runs them.
 
 Tolerances, as in test_gpu_parity: bf16 outputs within 2e-3 of the oracle;
 records and every stored state (the fold's, the commit's) bit-identical to
@@ -112,8 +112,9 @@ def test_window_after_fold(Q, bounded):
 @pytest.mark.parametrize("name", ["mtp3", "dflash7", "mixed", "deferred2"])
 def test_full_size_window_sampled(name):
     """The full-size workloads in the benchmark's launch configuration
-    (window form for dflash7, token by token for the others): a sample of
-    (row, head) outputs and committed states against the oracle."""
+    (window form for dflash7's items and mixed's longer ones, token by token
+    otherwise): a sample of (row, head) outputs and committed states
+    against the oracle."""
     wl = W.generate(name)
     sp = wl.spec
     deferred = sp.deferred
