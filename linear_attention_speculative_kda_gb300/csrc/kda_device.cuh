@@ -212,7 +212,7 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 //
 // One buffer of per-token vectors (fp32): slots [0, p) are folded (recorded)
 // tokens, [p, p + T) the new ones; q^ only for new tokens.  In the verify's
-// window form (see token_window) a new token's kh and qh slots hold the
+// window form (see window_outputs) a new token's kh and qh slots hold the
 // decay-weighted G_t * k^_t and G_t * q^_t instead, and pa / pb the pair
 // coefficients of the window (Q x Q each, row t, column s).
 struct TokView {
