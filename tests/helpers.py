@@ -42,7 +42,7 @@ def oracle_cache(wl: W.Workload, record_format: str = "raw") -> O.Cache:
 
 # --------------------------------------------------------------- GPU side --
 
-class GpuRun:
+class DeviceRun:
     """Device copies of a workload plus the buffers the library writes."""
 
     def __init__(self, wl: W.Workload, device="cuda", with_traj=False, sentinel=True,

@@ -11,7 +11,7 @@ import torch
 from linear_attention_speculative_kda_gb300 import api
 from linear_attention_speculative_kda_gb300 import workloads as W
 from oracle import kda_oracle as O
-from tests.helpers import GpuRun, assert_state_close, oracle_cache, oracle_layer, oracle_step
+from tests.helpers import DeviceRun, assert_state_close, oracle_cache, oracle_layer, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def _run_align(g, wl, table, nc, bs, request_indices=None, acc=None):
 @pytest.mark.parametrize("Q,bounded", [(4, False), (8, False), (8, True), (1, False)])
 def test_commit_align_against_oracle_and_trajectory(Q, bounded):
     wl, table, nc, bs = _case(Q, bounded, seed=40 + Q)
-    g = GpuRun(wl, with_traj=True)
+    g = DeviceRun(wl, with_traj=True)
     g.verify()
     torch.cuda.synchronize()
     traj = g.traj.clone()
@@ -88,7 +88,7 @@ def test_commit_align_against_oracle_and_trajectory(Q, bounded):
 def test_blocks_at_source_equal_the_plain_commit():
     wl, _, nc, bs = _case(4, seed=50)
     table = np.repeat(wl.state_indices.numpy()[:, None], WIDTH, axis=1).astype(np.int32)
-    a, p = GpuRun(wl), GpuRun(wl)
+    a, p = DeviceRun(wl), DeviceRun(wl)
     a.verify()
     p.verify()
     _run_align(a, wl, table, nc, bs)
@@ -110,7 +110,7 @@ def test_request_indices_permute_the_tables():
     table_p[perm] = table
     nc_p[perm] = nc
     acc_p[perm] = acc
-    a, p = GpuRun(wl), GpuRun(wl)
+    a, p = DeviceRun(wl), DeviceRun(wl)
     a.verify()
     p.verify()
     _run_align(a, wl, table, nc, bs)
@@ -126,7 +126,7 @@ def test_bad_blocks_are_flagged_and_skipped():
     S = wl.spec.S
     table[0, :] = S + 5                      # final block past the pool
     nc[1] = bs * WIDTH + bs - 1              # boundary block past the table
-    g = GpuRun(wl)
+    g = DeviceRun(wl)
     g.verify()
     acc = np.full(wl.spec.B, 2, dtype=np.int32)
     _run_align(g, wl, table, nc, bs, acc=acc.tolist())
@@ -194,7 +194,7 @@ def test_full_size_align_commit():
     wl.spec = W.Spec(**{**sp.__dict__, "S": S})
     table = (1 + B + np.arange(B * width)).reshape(B, width).astype(np.int32)
     nc = torch.randint(0, bs, (B,), generator=gen, dtype=torch.int32).numpy()
-    g = GpuRun(wl, with_traj=True, sentinel=False)
+    g = DeviceRun(wl, with_traj=True, sentinel=False)
     g.verify()
     torch.cuda.synchronize()
     _run_align(g, wl, table, nc, bs)

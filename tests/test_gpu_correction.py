@@ -23,7 +23,7 @@ import torch
 from linear_attention_speculative_kda_gb300 import api
 from linear_attention_speculative_kda_gb300 import workloads as W
 from oracle import kda_oracle as O
-from tests.helpers import (GpuRun, assert_out_close, assert_state_close, oracle_cache,
+from tests.helpers import (DeviceRun, assert_out_close, assert_state_close, oracle_cache,
                            oracle_layer, oracle_step)
 
 pytestmark = pytest.mark.gpu
@@ -56,7 +56,7 @@ CASES = list(_cases())
 
 @pytest.mark.parametrize("name,wl", CASES, ids=[c[0] for c in CASES])
 def test_verify_records_deltas(name, wl):
-    gr, gc = GpuRun(wl), GpuRun(wl, record_format="correction")
+    gr, gc = DeviceRun(wl), DeviceRun(wl, record_format="correction")
     gr.verify()
     gc.verify()
     torch.cuda.synchronize()
@@ -83,8 +83,8 @@ def test_verify_records_deltas(name, wl):
 
 @pytest.mark.parametrize("name,wl", CASES, ids=[c[0] for c in CASES])
 def test_commit_bit_equal_to_raw_and_trajectory(name, wl):
-    gr = GpuRun(wl)
-    gc = GpuRun(wl, record_format="correction", with_traj=True)
+    gr = DeviceRun(wl)
+    gc = DeviceRun(wl, record_format="correction", with_traj=True)
     for g in (gr, gc):
         g.verify()
         g.commit()
@@ -118,12 +118,12 @@ def test_deferred_fold_and_flush(Q, bounded):
     ones = torch.ones_like(wl.steps[1].eager).cuda()
     runs = {}
     for fmt in ("raw", "correction"):
-        g = GpuRun(wl, record_format=fmt)
+        g = DeviceRun(wl, record_format=fmt)
         g.verify(0, pending=True)
         g.commit(0, deferred=True)
         g.verify(1, pending=True)                   # folds the pending deltas
         g.commit(1, deferred=True, eager=ones)
-        f = GpuRun(wl, record_format=fmt)           # the same with a flush instead of a fold
+        f = DeviceRun(wl, record_format=fmt)           # the same with a flush instead of a fold
         f.verify(0, pending=True)
         f.commit(0, deferred=True)
         f.flush()
@@ -162,7 +162,7 @@ def test_align_commit_bit_equal_to_raw():
                       dtype=torch.int32, device="cuda")
     pools = []
     for fmt in ("raw", "correction"):
-        g = GpuRun(wl, record_format=fmt)
+        g = DeviceRun(wl, record_format=fmt)
         g.verify()
         api.kda_commit_align(g.A_log, g.g_bias, g.pool, g.cu, g.slots,
                              g.steps[0]["num_accepted"], g.records, table, nc, block_size=bs,
@@ -175,7 +175,7 @@ def test_align_commit_bit_equal_to_raw():
 
 def test_records_buffer_too_small_is_refused():
     wl = W.custom(B=2, H=1, Q=4, lens=[4, 4], S=4, seed=1)
-    g = GpuRun(wl)                                  # a raw-sized buffer
+    g = DeviceRun(wl)                                  # a raw-sized buffer
     with pytest.raises(ValueError):
         api.kda_verify(g.steps[0]["qkv"][:, 0], g.steps[0]["qkv"][:, 1],
                        g.steps[0]["qkv"][:, 2], g.steps[0]["g_raw"],
@@ -194,7 +194,7 @@ def test_full_size_deferred_two_steps():
     ones = torch.ones(sp.B, dtype=torch.uint8, device="cuda")
     outs, pools = [], []
     for fmt in ("raw", "correction"):
-        g = GpuRun(wl, sentinel=False, record_format=fmt)
+        g = DeviceRun(wl, sentinel=False, record_format=fmt)
         g.verify(0, pending=True)
         g.commit(0, deferred=True)
         g.verify(1, pending=True)

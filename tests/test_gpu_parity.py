@@ -16,7 +16,7 @@ import torch
 from linear_attention_speculative_kda_gb300 import api
 from linear_attention_speculative_kda_gb300 import workloads as W
 from oracle import kda_oracle as O
-from tests.helpers import (GpuRun, assert_out_close, assert_state_close, f64, oracle_cache,
+from tests.helpers import (DeviceRun, assert_out_close, assert_state_close, f64, oracle_cache,
                            oracle_layer, oracle_step)
 
 pytestmark = pytest.mark.gpu
@@ -37,7 +37,7 @@ def _small_cases():
 
 @pytest.mark.parametrize("name,wl", list(_small_cases()), ids=lambda x: x if isinstance(x, str) else "")
 def test_verify_outputs_records_trajectory(name, wl):
-    g = GpuRun(wl, with_traj=True)
+    g = DeviceRun(wl, with_traj=True)
     g.verify()
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
@@ -75,7 +75,7 @@ def test_verify_outputs_records_trajectory(name, wl):
 
 @pytest.mark.parametrize("name,wl", list(_small_cases()), ids=lambda x: x if isinstance(x, str) else "")
 def test_commit_matches_oracle_and_trajectory_bits(name, wl):
-    g = GpuRun(wl, with_traj=True)
+    g = DeviceRun(wl, with_traj=True)
     g.verify()
     g.commit()
     torch.cuda.synchronize()
@@ -113,14 +113,14 @@ def test_deferred_two_steps_bit_exact_and_oracle():
     acc1 = wl.steps[0].num_accepted
     acc2 = wl.steps[1].num_accepted
     # eager two steps on the GPU
-    ge = GpuRun(wl)
+    ge = DeviceRun(wl)
     ge.verify(0)
     ge.commit(0)
     oe1 = ge.out.clone()
     ge.verify(1)
     ge.commit(1)
     # deferred: verify1, deferred commit1, fused verify2, eager commit2
-    gd = GpuRun(wl)
+    gd = DeviceRun(wl)
     gd.verify(0, pending=True)
     gd.commit(0, deferred=True)
     od1 = gd.out.clone()
@@ -160,11 +160,11 @@ def test_deferred_two_steps_bit_exact_and_oracle():
 def test_flush_then_plain_verify_equals_fused_verify():
     wl = W.custom(B=8, H=2, Q=4, lens=[4, 4, 3, 4, 2, 4, 4, 1], S=12, R=10, deferred=True,
                   steps=2, seed=9)
-    ga = GpuRun(wl)
+    ga = DeviceRun(wl)
     ga.verify(0, pending=True)
     ga.commit(0, deferred=True)
     ga.verify(1, pending=True)
-    gb = GpuRun(wl)
+    gb = DeviceRun(wl)
     gb.verify(0, pending=True)
     gb.commit(0, deferred=True)
     pend = gb.pending.clone()
@@ -179,7 +179,7 @@ def test_flush_then_plain_verify_equals_fused_verify():
 def test_error_word_and_skips():
     wl = W.custom(B=5, H=2, Q=4, lens=[4, 4, 4, 4, 4], S=8, R=6, seed=13,
                   slots=[1, 2, 3, 4, 5], record_rows=[0, 1, 2, 3, 4])
-    g = GpuRun(wl)
+    g = DeviceRun(wl)
     cu = torch.tensor([0, 4, 9, 12, 16, 20], dtype=torch.int32, device="cuda")   # row 1: T = 5
     slots = torch.tensor([1, 2, 11, 4, 5], dtype=torch.int32, device="cuda")     # row 2: 11 >= S
     rr = torch.tensor([0, 1, 2, 9, 4], dtype=torch.int32, device="cuda")         # row 3: 9 >= R
@@ -200,7 +200,7 @@ def test_error_word_and_skips():
 
 def test_zero_rows_and_host_errors():
     wl = W.custom(B=2, H=1, Q=4, lens=[4, 4], S=4, seed=1)
-    g = GpuRun(wl)
+    g = DeviceRun(wl)
     empty = torch.zeros(0, dtype=torch.int32, device="cuda")
     st = g.steps[0]
     api.kda_verify(st["qkv"][:, 0], st["qkv"][:, 1], st["qkv"][:, 2], st["g_raw"],
@@ -223,7 +223,7 @@ def test_full_size_sampled(name):
     sample of (row, head) tiles is checked against the oracle."""
     wl = W.generate(name)
     sp = wl.spec
-    g = GpuRun(wl, with_traj=True, sentinel=False)
+    g = DeviceRun(wl, with_traj=True, sentinel=False)
     deferred = sp.deferred
     g.verify(0, pending=deferred)
     g.commit(0, deferred=deferred)
@@ -269,7 +269,7 @@ def test_all_rows_idle_and_more_ctas_than_work():
     # every row null or empty: the persistent CTAs find no work and write nothing
     wl = W.custom(B=40, H=16, Q=4, lens=[0, 4] * 20, S=48, seed=17,
                   slots=[0 if i % 2 else i + 1 for i in range(40)])
-    g = GpuRun(wl)
+    g = DeviceRun(wl)
     g.verify()
     g.commit()
     torch.cuda.synchronize()
@@ -283,10 +283,10 @@ def test_strided_activations_eight_byte_aligned():
     8, starting 8 bytes past a 16-byte boundary, give the same bits as the
     packed layout."""
     wl = W.custom(B=9, H=3, Q=8, lens=[8, 3, 0, 8, 5, 1, 8, 7, 2], S=12, seed=23)
-    ref = GpuRun(wl, with_traj=True)
+    ref = DeviceRun(wl, with_traj=True)
     ref.verify()
     ref.commit()
-    g = GpuRun(wl, with_traj=True)
+    g = DeviceRun(wl, with_traj=True)
     st = g.steps[0]
     T, H, D = st["qkv"].shape[0], wl.spec.H, wl.spec.D
     width = 3 * H * D + 4
@@ -315,12 +315,12 @@ def test_deferred_window8_bounded_with_folds():
     wl = W.custom(B=24, H=2, Q=8, lens=[8, 7, 1, 8, 3, 8, 8, 5, 0, 8, 2, 8] * 2, S=30, R=28,
                   deferred=True, steps=2, seed=29, bounded=True, lower_bound=-5.0,
                   eager_prob=0.2)
-    ge = GpuRun(wl)
+    ge = DeviceRun(wl)
     ge.verify(0)
     ge.commit(0)
     ge.verify(1)
     ge.commit(1)
-    gd = GpuRun(wl)
+    gd = DeviceRun(wl)
     gd.verify(0, pending=True)
     gd.commit(0, deferred=True)
     gd.verify(1, pending=True)
@@ -348,7 +348,7 @@ def test_record_slot_minus_one_rows():
     are never committed, and leave pending alone."""
     wl = W.custom(B=6, H=2, Q=4, lens=[4, 4, 4, 4, 4, 4], S=10, R=6, deferred=True, seed=31,
                   record_rows=[0, -1, 2, -1, 4, 5])
-    g = GpuRun(wl)
+    g = DeviceRun(wl)
     g.pending.fill_(0)
     g.verify(pending=True)
     g.commit(deferred=True, eager=torch.ones(6, dtype=torch.uint8, device="cuda"))

@@ -18,7 +18,7 @@ import torch
 
 from linear_attention_speculative_kda_gb300 import workloads as W
 from oracle import kda_oracle as O
-from tests.helpers import (GpuRun, assert_out_close, assert_state_close, oracle_cache,
+from tests.helpers import (DeviceRun, assert_out_close, assert_state_close, oracle_cache,
                            oracle_layer, oracle_step)
 
 pytestmark = pytest.mark.gpu
@@ -43,8 +43,8 @@ CASES = list(_cases())
 
 @pytest.mark.parametrize("name,wl", CASES, ids=[c[0] for c in CASES])
 def test_window_outputs_records_and_commit(name, wl):
-    gw = GpuRun(wl)                        # window form (no trajectory output)
-    gs = GpuRun(wl, with_traj=True)        # token by token
+    gw = DeviceRun(wl)                        # window form (no trajectory output)
+    gs = DeviceRun(wl, with_traj=True)        # token by token
     for g in (gw, gs):
         g.verify()
         g.commit()
@@ -72,7 +72,7 @@ def test_window_strong_decay_and_large_beta():
     for st in wl.steps:
         st.g_raw.mul_(3.0)
         st.beta_buf.add_(4.0)
-    gw = GpuRun(wl)
+    gw = DeviceRun(wl)
     gw.verify()
     torch.cuda.synchronize()
     assert int(gw.err.item()) == 0
@@ -87,7 +87,7 @@ def test_window_after_fold(Q, bounded):
     kw = dict(bounded=True, lower_bound=-5.0) if bounded else {}
     wl = W.custom(B=len(lens), H=2, Q=Q, lens=lens, S=len(lens) + 6, R=len(lens) + 4,
                   deferred=True, steps=2, seed=60 + Q, eager_prob=0.25, **kw)
-    gw, gs = GpuRun(wl), GpuRun(wl, with_traj=True)
+    gw, gs = DeviceRun(wl), DeviceRun(wl, with_traj=True)
     for g in (gw, gs):
         g.verify(0, pending=True)
         g.commit(0, deferred=True)
@@ -118,7 +118,7 @@ def test_full_size_window_sampled(name):
     wl = W.generate(name)
     sp = wl.spec
     deferred = sp.deferred
-    g = GpuRun(wl, sentinel=False)
+    g = DeviceRun(wl, sentinel=False)
     g.verify(0, pending=deferred)
     g.commit(0, deferred=deferred)
     torch.cuda.synchronize()
