@@ -299,7 +299,13 @@ class Engine:
         self.dev = d
         self.A_log = wl.A_log.to(d)
         self.g_bias = wl.g_bias.to(d)
-        self.pool = wl.pool.to(d)
+        # consecutive steps run on different copies of the state pool, enough
+        # of them that a step finds none of its checkpoints in L2
+        self.pools = [wl.pool.to(d)]
+        for _ in range(pool_copies(wl.pool.numel() * 4) - 1):
+            self.pools.append(self.pools[0].clone())
+        self.pool = self.pools[0]
+        self.turn = 0
         self.cu = wl.cu_seqlens.to(d)
         self.slots = wl.state_indices.to(d)
         self.rr = None if wl.record_rows is None else wl.record_rows.to(d)
@@ -326,35 +332,41 @@ class Engine:
                 out=torch.empty((T, sp.H, sp.D), dtype=torch.bfloat16, device=d)))
         return steps
 
-    def _verify(self, s, pending):
+    def _verify(self, s, pending, pool):
         H = self.wl.spec.H
         self.api.kda_verify(s["qkv"][:, 0], s["qkv"][:, 1], s["qkv"][:, 2], s["g_raw"],
-                            s["beta_buf"][:, :H], self.A_log, self.g_bias, self.pool, self.cu,
+                            s["beta_buf"][:, :H], self.A_log, self.g_bias, pool, self.cu,
                             self.slots, self.records, s["out"], record_rows=self.rr,
                             pending=self.pending if pending else None, error_word=self.err,
                             **self.kw)
 
-    def _commit(self, s, deferred, eager):
-        self.api.kda_commit(self.A_log, self.g_bias, self.pool, self.cu, self.slots,
+    def _commit(self, s, deferred, eager, pool):
+        self.api.kda_commit(self.A_log, self.g_bias, pool, self.cu, self.slots,
                             s["num_accepted"], self.records, record_rows=self.rr,
                             pending=self.pending if deferred else None,
                             eager=eager if deferred else None, error_word=self.err, **self.kw)
 
-    def launches(self, steps=None):
-        """The step as a list of (name, callable), on input set `steps`."""
+    def launches(self, steps=None, pool=None):
+        """The step as a list of (name, callable), on input set `steps` and
+        state pool `pool` (by default the first copy)."""
         steps = self.steps if steps is None else steps
+        pool = self.pool if pool is None else pool
         if not self.wl.spec.deferred:
             s = steps[0]
-            return [("verify", lambda: self._verify(s, False)),
-                    ("commit", lambda: self._commit(s, False, None))]
+            return [("verify", lambda: self._verify(s, False, pool)),
+                    ("commit", lambda: self._commit(s, False, None, pool))]
         s1, s2 = steps
-        return [("verify", lambda: self._verify(s1, True)),
-                ("commit_deferred", lambda: self._commit(s1, True, s1["eager"])),
-                ("verify_fused", lambda: self._verify(s2, True)),
-                ("commit", lambda: self._commit(s2, True, self.all_eager))]
+        # the step ends with every row committed (pending all 0), so the next
+        # step may run on another copy of the pool
+        return [("verify", lambda: self._verify(s1, True, pool)),
+                ("commit_deferred", lambda: self._commit(s1, True, s1["eager"], pool)),
+                ("verify_fused", lambda: self._verify(s2, True, pool)),
+                ("commit", lambda: self._commit(s2, True, self.all_eager, pool))]
 
     def run_step(self, events=None, steps=None):
-        for i, (_, fn) in enumerate(self.launches(steps)):
+        pool = self.pools[self.turn % len(self.pools)]
+        self.turn += 1
+        for i, (_, fn) in enumerate(self.launches(steps, pool)):
             if events is not None:
                 events[i][0].record()
             fn()
@@ -493,13 +505,24 @@ def workload_config(wl: W.Workload, world: int, record_format: str = "raw"):
 
 
 L2_BYTES = 129 * 10**6   # GB300 L2
+POOL_ROTATION_BYTES = 4 * L2_BYTES
+
+
+def pool_copies(pool_bytes: int) -> int:
+    """Copies of the state pool that consecutive steps rotate over: enough to
+    hold 4x the L2 in all, so that a step's checkpoints (written by the step
+    that used the same copy, several steps before) have left L2."""
+    if pool_bytes <= 0:
+        return 1
+    return max(1, -(-POOL_ROTATION_BYTES // pool_bytes))
 
 
 def l2_note(pool_bytes: int) -> str:
-    if pool_bytes > L2_BYTES:
+    n = pool_copies(pool_bytes)
+    if n == 1:
         return "inputs larger than L2 (state pool %.2f GB)" % (pool_bytes / 1e9)
-    return "state pool %.3f GB fits in L2 and is not flushed (latency-bound small case)" % (
-        pool_bytes / 1e9)
+    return ("inputs larger than L2: steps rotate over %d copies of the %.3f GB state pool "
+            "(%.2f GB in all)" % (n, pool_bytes / 1e9, n * pool_bytes / 1e9))
 
 
 def conv_compact_bytes(wl: W.Workload, conv_dim: int, hist: int, elem_bytes: int, acc) -> int:

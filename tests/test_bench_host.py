@@ -188,8 +188,17 @@ def test_align_commit_bytes_by_rows():
 
 
 def test_l2_note_is_truthful():
-    assert bench.l2_note(2 * 10**9).startswith("inputs larger than L2")
-    assert "fits in L2" in bench.l2_note(2 * 2**20)
+    assert bench.l2_note(2 * 10**9).startswith("inputs larger than L2 (state pool")
+    note = bench.l2_note(2 * 2**20)
+    assert note.startswith("inputs larger than L2: steps rotate over 247 copies")
+
+
+def test_pool_copies_exceed_four_l2():
+    for pool in (2 * 2**20, 201 * 10**6, 335 * 10**6, 600 * 10**6, 2 * 10**9):
+        n = bench.pool_copies(pool)
+        assert n * pool >= 4 * bench.L2_BYTES
+        assert n == 1 or (n - 1) * pool < 4 * bench.L2_BYTES   # no more than needed
+    assert bench.pool_copies(201 * 10**6) == 3 and bench.pool_copies(2 * 10**9) == 1
 
 
 def test_reference_arm_prints_the_contract_line():
