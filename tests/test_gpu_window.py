@@ -135,3 +135,32 @@ def test_full_size_window_sampled(name):
     assert_out_close(g.out, res.out)
     for (slot, h), ref in cache.written.items():
         assert_state_close(g.pool[slot, h].double().cpu().numpy(), ref)
+
+
+def test_window_strided_activations_eight_byte_aligned():
+    """Window form with activation rows whose token stride is a multiple of
+    4 elements but not of 8, starting 8 bytes past a 16-byte boundary: the
+    same bits as the packed layout."""
+    from linear_attention_speculative_kda_gb300 import api
+    wl = W.custom(B=9, H=3, Q=8, lens=[8, 3, 0, 8, 5, 1, 8, 7, 6], S=12, seed=23)
+    ref = DeviceRun(wl)
+    ref.verify()
+    g = DeviceRun(wl)
+    st = g.steps[0]
+    T, H, D = st["qkv"].shape[0], wl.spec.H, wl.spec.D
+    width = 3 * H * D + 4
+    flat = torch.zeros(T * width + 4, dtype=torch.bfloat16, device="cuda")
+    view = flat[4:].view(T, width)
+    view[:, : 3 * H * D] = st["qkv"].reshape(T, -1)
+    q = view[:, 0 * H * D:1 * H * D].view(T, H, D)
+    k = view[:, 1 * H * D:2 * H * D].view(T, H, D)
+    v = view[:, 2 * H * D:3 * H * D].view(T, H, D)
+    assert q.stride(0) % 8 == 4 and q.data_ptr() % 16 == 8
+    api.kda_verify(q, k, v, st["g_raw"], st["beta_buf"][:, :H], g.A_log, g.g_bias, g.pool, g.cu,
+                   g.slots, g.records, g.out, error_word=g.err, **g.kw())
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0 and int(ref.err.item()) == 0
+    assert torch.equal(g.out, ref.out)
+    assert torch.equal(g.records, ref.records)
+    res = O.verify(oracle_layer(wl), oracle_cache(wl), oracle_step(wl))
+    assert_out_close(g.out, res.out)
