@@ -164,3 +164,47 @@ def test_window_strided_activations_eight_byte_aligned():
     assert torch.equal(g.records, ref.records)
     res = O.verify(oracle_layer(wl), oracle_cache(wl), oracle_step(wl))
     assert_out_close(g.out, res.out)
+
+
+def test_window_kernel_error_word_and_skips():
+    """Bad metadata in a launch of the window kernel (window 8): the bad rows
+    are flagged and skipped, the others run in window form."""
+    from linear_attention_speculative_kda_gb300 import api
+    wl = W.custom(B=5, H=2, Q=8, lens=[8, 8, 8, 8, 8], S=8, R=6, seed=13,
+                  slots=[1, 2, 3, 4, 5], record_rows=[0, 1, 2, 3, 4])
+    g = DeviceRun(wl)
+    cu = torch.tensor([0, 8, 17, 24, 32, 40], dtype=torch.int32, device="cuda")  # row 1: T = 9
+    slots = torch.tensor([1, 2, 11, 4, 5], dtype=torch.int32, device="cuda")     # row 2: 11 >= S
+    rr = torch.tensor([0, 1, 2, 9, 4], dtype=torch.int32, device="cuda")         # row 3: 9 >= R
+    g.verify(cu=cu, slots=slots, record_rows=rr)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == api.ROW_BAD_LENGTH | api.ROW_BAD_SLOT | api.ROW_BAD_RECORD
+    out = g.out.float().cpu().numpy()
+    assert (out[8:32] == -9.0).all()            # rows 1..3 skipped
+    assert not (out[0:8] == -9.0).any()         # rows 0 and 4 ran
+    assert not (out[32:40] == -9.0).any()
+    assert torch.equal(g.pool, g.pool0)
+
+
+def test_window_rows_without_record_slot():
+    """Rows whose record slot is -1 verify in window form into the scratch
+    row and are never committed."""
+    wl = W.custom(B=6, H=2, Q=8, lens=[8, 8, 6, 8, 5, 8], S=10, R=6, deferred=True, seed=31,
+                  record_rows=[0, -1, 2, -1, 4, 5])
+    g = DeviceRun(wl)
+    g.verify(pending=True)
+    g.commit(deferred=True, eager=torch.ones(6, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    res = O.verify(layer, cache, step, pending=True)
+    O.commit(layer, cache, step, wl.steps[0].num_accepted.numpy(), deferred=True,
+             eager=np.ones(6, np.uint8))
+    assert_out_close(g.out, res.out)
+    slots = wl.state_indices.numpy()
+    for b in (1, 3):
+        assert torch.equal(g.pool[int(slots[b])], g.pool0[int(slots[b])])
+    pool = g.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
