@@ -288,7 +288,9 @@ def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
     q, k, v, g_raw: bf16 [T, H, 128] (token stride free, [H, D] packed);
     beta_raw: bf16 [T, H]; A_log fp32 [H]; g_bias fp32 [H*128];
     state_pool fp32 [S, H, 128, 128]; cu_seqlens int32 [B+1];
-    state_indices int32 [B]; records: buffer from ``allocate_records``;
+    state_indices int32 [B]; records: buffer from ``allocate_records``
+    for the same ``record_format`` ("raw": k, v, g_raw and beta_raw per
+    token; "correction": each token's fp32 delta with k and g_raw);
     out: bf16 [T, H, 128] contiguous.  Returns ``out``.
     """
     dev = state_pool.device
@@ -334,7 +336,8 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
                *, window: int, record_slots: int, lower_bound=None, record_rows=None,
                pending=None, eager=None, error_word=None, record_format: str = "raw") -> None:
     """``kda_commit``: fold each row's accepted tokens into its checkpoint
-    (eager), or store them as pending replays (deferred, ``pending`` given)."""
+    (eager), or store them as pending replays (deferred, ``pending`` given).
+    ``record_format`` must be the one the verify wrote ``records`` with."""
     dev = state_pool.device
     f32, i32 = torch.float32, torch.int32
     for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
@@ -367,7 +370,8 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
 def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, window: int,
               record_slots: int, lower_bound=None, record_rows=None, error_word=None,
               record_format: str = "raw") -> None:
-    """``kda_flush``: fold pending replays into the checkpoints in place."""
+    """``kda_flush``: fold pending replays into the checkpoints in place
+    (``record_format`` as for ``kda_commit``)."""
     dev = state_pool.device
     f32, i32 = torch.float32, torch.int32
     for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
@@ -467,7 +471,7 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
                      request_indices=None, error_word=None, record_format: str = "raw") -> None:
     """``kda_commit_align``: the eager commit writing the final and boundary
     blocks of a paged state cache.  num_accepted, num_computed and the block
-    table rows are per request."""
+    table rows are per request; ``record_format`` as for ``kda_commit``."""
     dev = state_pool.device
     f32, i32 = torch.float32, torch.int32
     for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
