@@ -220,3 +220,26 @@ def test_conv_compact_align_host_checks(lib):
     assert call(_align(num_computed=None)) == api.KDA_ERR_INVALID_ARG
     assert call(_align(), B=-1) == api.KDA_ERR_INVALID_ARG
     assert call(None, B=0) == api.KDA_OK
+
+
+def test_binding_refuses_small_records_buffer(lib):
+    # the size check runs before any device call, so CPU tensors suffice
+    import torch
+    T, H = 4, 2
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    act = torch.zeros((T, H, 128), dtype=bf)
+    pool = torch.zeros((3, H, 128, 128), dtype=f32)
+    raw = torch.zeros(api.kda_records_bytes(H, 4, 1) // 2, dtype=bf)
+    args = (act, act, act, act, torch.zeros((T, H), dtype=bf), torch.zeros(H, dtype=f32),
+            torch.zeros(H * 128, dtype=f32), pool, torch.tensor([0, 4], dtype=i32),
+            torch.tensor([1], dtype=i32))
+    with pytest.raises(ValueError, match="correction"):
+        api.kda_verify(*args, raw, torch.zeros_like(act), window=4, record_slots=1,
+                       record_format="correction")
+    with pytest.raises(ValueError, match="raw"):
+        api.kda_verify(*args, raw[:-1], torch.zeros_like(act), window=4, record_slots=1)
+    with pytest.raises(ValueError):
+        api.kda_commit(torch.zeros(H, dtype=f32), torch.zeros(H * 128, dtype=f32), pool,
+                       torch.tensor([0, 4], dtype=i32), torch.tensor([1], dtype=i32),
+                       torch.tensor([2], dtype=i32), raw, window=4, record_slots=1,
+                       record_format="correction")
