@@ -112,7 +112,15 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
     Row row;
     const int bad = read_row(p, b, kMode != Mode::kFlush, row);
     if (bad) {
-        if (head == 0) flag_error(p.err, bad);
+        if (head == 0) {
+            flag_error(p.err, bad);
+            // a deferred commit clears the pending count of a skipped row
+            // whose record slot is usable: its records are this step's, so
+            // the previous step's count no longer describes them
+            if (kMode == Mode::kCommit && p.pending_out != nullptr && !(bad & kBadRecord) &&
+                row.r >= 0)
+                p.pending_out[row.r] = 0;
+        }
         return false;
     }
     int fold = 0, T = 0;
@@ -134,7 +142,10 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (p.block_table != nullptr) {
             if (p.request_indices != nullptr) req = p.request_indices[b];
             if (req < 0 || req >= p.num_requests) {
-                if (head == 0) flag_error(p.err, kBadBlock);
+                if (head == 0) {
+                    flag_error(p.err, kBadBlock);
+                    if (p.pending_out != nullptr && row.r >= 0) p.pending_out[row.r] = 0;
+                }
                 return false;
             }
         }
@@ -146,7 +157,10 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (p.block_table != nullptr && valid) {
             const int bad_align = align_targets(p, req, n, w);
             if (bad_align) {
-                if (head == 0) flag_error(p.err, bad_align);
+                if (head == 0) {
+                    flag_error(p.err, bad_align);
+                    if (p.pending_out != nullptr && row.r >= 0) p.pending_out[row.r] = 0;
+                }
                 return false;
             }
             valid = w.dst > 0;
@@ -809,11 +823,14 @@ Params base_params(const kda_config *cfg, int32_t B) {
 
 kda_status check_common(const kda_config *cfg, const float *A_log, const float *g_bias,
                         const float *pool, const int32_t *state_indices, int32_t B,
-                        const int32_t *record_rows, const void *records) {
+                        const int32_t *record_rows, const void *records,
+                        const int32_t *error_word) {
     if (!A_log || !g_bias || !pool || !state_indices || !records) return KDA_ERR_INVALID_ARG;
     if (!aligned(g_bias, 16) || !aligned(pool, 16) || !aligned(A_log, 4) ||
         !aligned(state_indices, 4) || !aligned(records, 16))
         return KDA_ERR_INVALID_ARG;
+    // the kernels OR bits into the error word with a 32-bit atomic
+    if (error_word != nullptr && !aligned(error_word, 4)) return KDA_ERR_INVALID_ARG;
     if (record_rows == nullptr && B > cfg->record_slots) return KDA_ERR_INVALID_ARG;
     if (record_rows != nullptr && !aligned(record_rows, 4)) return KDA_ERR_INVALID_ARG;
     if ((long long)B * cfg->num_heads > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
@@ -933,7 +950,8 @@ kda_status kda_verify(const kda_config *cfg, const void *q, const void *k, const
     if (st != KDA_OK) return st;
     if (B < 0) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
-    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
+    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records,
+                      error_word);
     if (st != KDA_OK) return st;
     if (!q || !k || !v || !g_raw || !beta_raw || !cu_seqlens || !out) return KDA_ERR_INVALID_ARG;
     if (!aligned(q, 8) || !aligned(k, 8) || !aligned(v, 8) || !aligned(g_raw, 8) ||
@@ -977,7 +995,8 @@ kda_status kda_commit(const kda_config *cfg, const float *A_log, const float *g_
     if (st != KDA_OK) return st;
     if (B < 0) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
-    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
+    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records,
+                      error_word);
     if (st != KDA_OK) return st;
     if (!cu_seqlens || !num_accepted) return KDA_ERR_INVALID_ARG;
     if (!aligned(cu_seqlens, 4) || !aligned(num_accepted, 4)) return KDA_ERR_INVALID_ARG;
@@ -1010,7 +1029,8 @@ kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const flo
     if (st != KDA_OK) return st;
     if (B < 0) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
-    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
+    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records,
+                      error_word);
     if (st != KDA_OK) return st;
     if (!cu_seqlens || !num_accepted) return KDA_ERR_INVALID_ARG;
     if (!aligned(cu_seqlens, 4) || !aligned(num_accepted, 4)) return KDA_ERR_INVALID_ARG;
@@ -1039,7 +1059,8 @@ kda_status kda_flush(const kda_config *cfg, const float *A_log, const float *g_b
     if (st != KDA_OK) return st;
     if (B < 0) return KDA_ERR_INVALID_ARG;
     if (B == 0) return KDA_OK;  // nothing to do; no pointer is inspected
-    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records);
+    st = check_common(cfg, A_log, g_bias, state_pool, state_indices, B, record_rows, records,
+                      error_word);
     if (st != KDA_OK) return st;
     if (!pending || !aligned(pending, 4)) return KDA_ERR_INVALID_ARG;
 

@@ -403,6 +403,11 @@ def commit(layer: Layer, cache: Cache, step: Step, num_accepted, *,
         r = _record_slot(step.record_rows, b)
         bad = _row_checks(layer, cache, T, slot, r)
         if bad:
+            # a deferred commit rewrites the pending count of every row whose
+            # record slot is usable, a skipped row's to 0: its records now
+            # hold this step's tokens, not the ones the old count replays
+            if deferred and bad != "record" and r >= 0:
+                cache.pending[r] = 0
             return RowIssue(b, bad)
         n = commit_len(num_accepted[b], T, layer.window)
         valid = slot > 0 and n > 0 and r >= 0

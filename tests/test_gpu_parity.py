@@ -366,3 +366,30 @@ def test_record_slot_minus_one_rows():
     pool = g.pool.cpu()
     for (slot, h), ref in cache.written.items():
         assert_state_close(pool[slot, h].double().numpy(), ref)
+
+
+def test_deferred_commit_clears_pending_of_skipped_rows():
+    """A deferred commit that skips rows for bad metadata still rewrites
+    their pending counts (to 0) when the record slot is usable, as the
+    oracle does; a row with a bad record slot leaves pending alone."""
+    wl = W.custom(B=4, H=2, Q=4, lens=[4, 4, 4, 4], S=6, R=6, deferred=True,
+                  record_rows=[1, 2, 3, 4], slots=[1, 2, 3, 4], seed=9)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, 4, 9, 12, 16], **i32)        # row 1: T = 5 > Q
+    slots = torch.tensor([1, 2, 9, 3], **i32)           # row 2: slot 9 >= S
+    rr = torch.tensor([1, 2, 3, 8], **i32)              # row 3: record slot 8 >= R
+    acc = torch.tensor([2, 2, 2, 2], **i32)
+    g = DeviceRun(wl)
+    g.pending.fill_(3)
+    g.commit(deferred=True, eager=torch.zeros(4, dtype=torch.uint8, device="cuda"),
+             num_accepted=acc, cu=cu, slots=slots, record_rows=rr)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == api.ROW_BAD_LENGTH | api.ROW_BAD_SLOT | api.ROW_BAD_RECORD
+    layer = oracle_layer(wl)
+    step = oracle_step(wl, cu_seqlens=cu.cpu(), state_indices=slots.cpu(),
+                       record_rows=rr.cpu().numpy())
+    cache = oracle_cache(wl)
+    cache.pending[:] = 3
+    O.commit(layer, cache, step, acc.cpu().numpy(), deferred=True, eager=np.zeros(4, np.uint8))
+    assert g.pending.cpu().tolist() == cache.pending.tolist() == [3, 2, 0, 0, 3, 3]
+    assert torch.equal(g.pool, g.pool0)

@@ -144,3 +144,22 @@ def test_invalid_rows_are_reported():
     cache.pending[0] = 5                       # > Q: invalid pending count
     res = O.verify(layer, cache, step, pending=True, rows=[0])
     assert [(i.row, i.reason) for i in res.issues] == [(0, "pending")]
+
+
+def test_deferred_commit_clears_pending_of_skipped_rows():
+    # rows skipped for bad metadata still have their pending count rewritten
+    # (to 0) when their record slot is usable: the slot's records were just
+    # overwritten by this step's verify, so an old count would replay them
+    wl = W.custom(B=4, H=1, Q=4, lens=[4, 4, 4, 4], S=6, R=6, deferred=True,
+                  record_rows=[1, 2, 3, 4], slots=[1, 2, 3, 4], seed=9)
+    layer = oracle_layer(wl)
+    step = oracle_step(wl, cu_seqlens=torch.tensor([0, 4, 9, 12, 16], dtype=torch.int32),
+                       state_indices=torch.tensor([1, 2, 9, 3], dtype=torch.int32),
+                       record_rows=np.array([1, 2, 3, 8]))
+    cache = oracle_cache(wl)
+    cache.pending[:] = 3                      # stale counts of the previous step
+    issues = O.commit(layer, cache, step, np.array([2, 2, 2, 2]), deferred=True,
+                      eager=np.zeros(4, np.uint8))
+    # row 1: T = 5 > Q; row 2: slot 9 >= S; row 3: record slot 8 >= R (not written)
+    assert {i.row: i.reason for i in issues} == {1: "length", 2: "slot", 3: "record"}
+    assert cache.pending.tolist() == [3, 2, 0, 0, 3, 3]
