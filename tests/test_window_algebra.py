@@ -26,7 +26,10 @@ def _np_gate(x, a_log, bounded, lb):
     return -a * np.logaddexp(0.0, x)
 
 
-def _window_form(S, q, k, v, g_raw, beta_raw, a_log, g_bias, bounded, lb, scale):
+def _window_form(S, q, k, v, g_raw, beta_raw, a_log, g_bias, bounded, lb, scale,
+                 perturb_b=None):
+    # perturb_b = (t, s, factor): multiplies b_ts by factor (a planted
+    # mistake, for the tests of the output checker)
     T = k.shape[0]
     kh = k / np.sqrt((k * k).sum(axis=1, keepdims=True) + 1e-6)
     qh = q / np.sqrt((q * q).sum(axis=1, keepdims=True) + 1e-6) * scale
@@ -44,6 +47,8 @@ def _window_form(S, q, k, v, g_raw, beta_raw, a_log, g_bias, bounded, lb, scale)
                 r = r * e[t]
                 a[t, s] = np.sum(kh[s] * r * kh[t])
             b[t, s] = np.sum(kh[s] * r * qh[t])
+    if perturb_b is not None:
+        b[perturb_b[0], perturb_b[1]] *= perturb_b[2]
     vp = np.zeros_like(v)
     out = np.zeros_like(v)
     for t in range(T):
