@@ -203,6 +203,56 @@ def _opt(t, dtype, name, device):
     return None if t is None else _req(t, dtype, name, device)
 
 
+# Shape and size checks.  The C ABI takes bare pointers and cannot see how
+# large a buffer is, so the binding checks every tensor the kernels index
+# against the sizes the call implies, before anything is launched.
+
+def _tokens(t, name, H, D):
+    """Token count of a [T, H, D] (or [1, T, H, D]) activation, or of a
+    [T, H] (or [1, T, H]) one when D is None."""
+    lead = 4 if D is not None else 3
+    if t.dim() == lead:
+        if t.shape[0] != 1:
+            raise ValueError(f"{name}: a leading batch dimension must be 1")
+        t = t[0]
+    want = (H, D) if D is not None else (H,)
+    if t.dim() != len(want) + 1 or tuple(t.shape[1:]) != want:
+        shape = "[T, H, D]" if D is not None else "[T, H]"
+        raise ValueError(f"{name} must be {shape} with H={H}" +
+                         (f", D={D}" if D is not None else "") + f", got {tuple(t.shape)}")
+    return t.shape[0]
+
+
+def _at_least(t, n, name):
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{name} needs at least {n} elements, has {t.numel()}")
+
+
+def _check_pool(state_pool):
+    if (state_pool.dim() != 4 or not state_pool.is_contiguous()
+            or state_pool.shape[2] != state_pool.shape[3]):
+        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor with V == K")
+    return state_pool.shape[0], state_pool.shape[1], state_pool.shape[3]
+
+
+def _check_gate(A_log, g_bias, H, D):
+    if not A_log.is_contiguous() or not g_bias.is_contiguous():
+        raise ValueError("A_log and g_bias must be contiguous")
+    _at_least(A_log, H, "A_log")
+    _at_least(g_bias, H * D, "g_bias")
+
+
+def _check_rows(B, record_slots, record_rows=None, pending=None, eager=None, error_word=None):
+    for name, t in (("record_rows", record_rows), ("pending", pending), ("eager", eager),
+                    ("error_word", error_word)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _at_least(record_rows, B, "record_rows")
+    _at_least(pending, record_slots, "pending")
+    _at_least(eager, B, "eager")
+    _at_least(error_word, 1, "error_word")
+
+
 def _format_code(record_format: str) -> int:
     try:
         return RECORD_FORMATS[record_format]
@@ -306,17 +356,27 @@ def kda_verify(q, k, v, g_raw, beta_raw, A_log, g_bias, state_pool, cu_seqlens,
     _opt(pending, i32, "pending", dev)
     _opt(trajectory_out, f32, "trajectory_out", dev)
     _opt(error_word, i32, "error_word", dev)
-    if state_pool.dim() != 4 or not state_pool.is_contiguous():
-        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
-    S, H = state_pool.shape[0], state_pool.shape[1]
-    if not out.is_contiguous() or not A_log.is_contiguous() or not g_bias.is_contiguous():
-        raise ValueError("out, A_log and g_bias must be contiguous")
-    for t in (cu_seqlens, state_indices, record_rows, pending):
-        if t is not None and not t.is_contiguous():
+    S, H, D = _check_pool(state_pool)
+    _check_gate(A_log, g_bias, H, D)
+    for t in (cu_seqlens, state_indices):
+        if not t.is_contiguous():
             raise ValueError("metadata tensors must be contiguous")
     B = state_indices.shape[0]
     if cu_seqlens.shape[0] != B + 1:
         raise ValueError("cu_seqlens must have B + 1 entries")
+    _check_rows(B, record_slots, record_rows, pending, None, error_word)
+    T = _tokens(q, "q", H, D)
+    for name, t in (("k", k), ("v", v), ("g_raw", g_raw), ("out", out)):
+        if _tokens(t, name, H, D) != T:
+            raise ValueError(f"{name} has a different token count from q")
+    if _tokens(beta_raw, "beta_raw", H, None) != T:
+        raise ValueError("beta_raw has a different token count from q")
+    if not out.is_contiguous():
+        raise ValueError("out must be contiguous")
+    if trajectory_out is not None:
+        if not trajectory_out.is_contiguous():
+            raise ValueError("trajectory_out must be contiguous")
+        _at_least(trajectory_out, T * H * D * D, "trajectory_out")
     strides = (_token_stride(q), _token_stride(k), _token_stride(v), _token_stride(g_raw),
                _token_stride(beta_raw))
     cfg = _config(H, window, S, record_slots, lower_bound, scale, strides, state_pool.shape[-1],
@@ -350,14 +410,17 @@ def kda_commit(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepte
     _opt(pending, i32, "pending", dev)
     _opt(eager, torch.uint8, "eager", dev)
     _opt(error_word, i32, "error_word", dev)
-    if state_pool.dim() != 4 or not state_pool.is_contiguous():
-        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    S, H, D = _check_pool(state_pool)
+    _check_gate(A_log, g_bias, H, D)
     B = state_indices.shape[0]
+    for t in (cu_seqlens, state_indices, num_accepted):
+        if not t.is_contiguous():
+            raise ValueError("metadata tensors must be contiguous")
     if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < B:
         raise ValueError("metadata sizes do not match the batch")
-    S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
-                  state_pool.shape[-1], record_format)
+    _check_rows(B, record_slots, record_rows, pending, eager, error_word)
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1), D,
+                  record_format)
     _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_commit(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
@@ -381,12 +444,14 @@ def kda_flush(A_log, g_bias, state_pool, state_indices, records, pending, *, win
     _req(pending, i32, "pending", dev)
     _opt(record_rows, i32, "record_rows", dev)
     _opt(error_word, i32, "error_word", dev)
-    if state_pool.dim() != 4 or not state_pool.is_contiguous():
-        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    S, H, D = _check_pool(state_pool)
+    _check_gate(A_log, g_bias, H, D)
     B = state_indices.shape[0]
-    S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
-                  state_pool.shape[-1], record_format)
+    if not state_indices.is_contiguous():
+        raise ValueError("metadata tensors must be contiguous")
+    _check_rows(B, record_slots, record_rows, pending, None, error_word)
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1), D,
+                  record_format)
     _check_records(records, H, window, record_slots, record_format)
     lib = load_library()
     st = lib.kda_flush(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
@@ -483,14 +548,19 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
     _opt(record_rows, i32, "record_rows", dev)
     _opt(error_word, i32, "error_word", dev)
     _check_align(block_table, num_computed, request_indices, dev)
-    if state_pool.dim() != 4 or not state_pool.is_contiguous():
-        raise ValueError("state_pool must be a contiguous [S, H, V, K] tensor")
+    S, H, D = _check_pool(state_pool)
+    _check_gate(A_log, g_bias, H, D)
     B = state_indices.shape[0]
+    for t in (cu_seqlens, state_indices, num_accepted):
+        if not t.is_contiguous():
+            raise ValueError("metadata tensors must be contiguous")
     if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < block_table.shape[0]:
         raise ValueError("metadata sizes do not match the batch")
-    S, H = state_pool.shape[0], state_pool.shape[1]
-    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1),
-                  state_pool.shape[-1], record_format)
+    _check_rows(B, record_slots, record_rows, None, None, error_word)
+    if request_indices is not None:
+        _at_least(request_indices, B, "request_indices")
+    cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1), D,
+                  record_format)
     _check_records(records, H, window, record_slots, record_format)
     al = make_align(block_table, num_computed, block_size, request_indices)
     lib = load_library()

@@ -243,3 +243,72 @@ def test_binding_refuses_small_records_buffer(lib):
                        torch.tensor([0, 4], dtype=i32), torch.tensor([1], dtype=i32),
                        torch.tensor([2], dtype=i32), raw, window=4, record_slots=1,
                        record_format="correction")
+
+
+def test_error_word_alignment(lib):
+    # the kernels OR bits into the error word with a 32-bit atomic: a pointer
+    # off a 4-byte boundary is refused before anything is launched
+    c = ctypes.byref(_cfg())
+    assert _verify(lib, _cfg(), err=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+    assert lib.kda_commit(c, FAKE, FAKE, FAKE, FAKE, FAKE, 3, FAKE, None, FAKE, None, None,
+                          FAKE + 1, None) == api.KDA_ERR_INVALID_ARG
+    assert lib.kda_flush(c, FAKE, FAKE, FAKE, FAKE, 3, None, FAKE, FAKE, FAKE + 2,
+                         None) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(), err=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+    assert _conv(lib, err=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+
+
+def _host_args(T=4, H=2, S=3, B=1, R=1):
+    """Consistent CPU tensors for the binding's checks (never launched: each
+    test below breaks one of them, and the check raises first)."""
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    return dict(
+        q=torch.zeros((T, H, 128), dtype=bf), k=torch.zeros((T, H, 128), dtype=bf),
+        v=torch.zeros((T, H, 128), dtype=bf), g_raw=torch.zeros((T, H, 128), dtype=bf),
+        beta_raw=torch.zeros((T, H), dtype=bf), A_log=torch.zeros(H, dtype=f32),
+        g_bias=torch.zeros(H * 128, dtype=f32), state_pool=torch.zeros((S, H, 128, 128), dtype=f32),
+        cu_seqlens=torch.tensor([0, T], dtype=i32), state_indices=torch.tensor([1], dtype=i32),
+        records=torch.zeros(api.kda_records_bytes(H, 4, R) // 2, dtype=bf),
+        out=torch.zeros((T, H, 128), dtype=bf))
+
+
+def _bad_verify(**change):
+    a = _host_args()
+    kw = dict(window=4, record_slots=1)
+    for name, val in change.items():
+        (a if name in a else kw)[name] = val
+    with pytest.raises(ValueError):
+        api.kda_verify(a["q"], a["k"], a["v"], a["g_raw"], a["beta_raw"], a["A_log"], a["g_bias"],
+                       a["state_pool"], a["cu_seqlens"], a["state_indices"], a["records"],
+                       a["out"], **kw)
+
+
+def test_binding_checks_shapes_before_any_launch(lib):
+    import torch
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    _bad_verify(k=torch.zeros((4, 1, 128), dtype=bf))            # fewer heads than the pool
+    _bad_verify(v=torch.zeros((4, 2, 64), dtype=bf))             # not 128 channels
+    _bad_verify(g_raw=torch.zeros((3, 2, 128), dtype=bf))        # another token count
+    _bad_verify(beta_raw=torch.zeros((4, 1), dtype=bf))          # beta needs H columns
+    _bad_verify(out=torch.zeros((2, 2, 128), dtype=bf))          # out shorter than q
+    _bad_verify(q=torch.zeros((2, 4, 2, 128), dtype=bf))         # a batch dimension > 1
+    _bad_verify(A_log=torch.zeros(1, dtype=f32))                 # fewer than H entries
+    _bad_verify(g_bias=torch.zeros(128, dtype=f32))              # fewer than H * 128
+    _bad_verify(state_pool=torch.zeros((3, 2, 128, 64), dtype=f32))
+    _bad_verify(pending=torch.zeros(0, dtype=i32))               # fewer than record_slots
+    _bad_verify(record_rows=torch.zeros(0, dtype=i32))           # fewer than B
+    _bad_verify(error_word=torch.zeros(0, dtype=i32))
+    _bad_verify(trajectory_out=torch.zeros(4 * 2 * 128 * 127, dtype=f32))
+    a = _host_args()
+    common = (a["A_log"], a["g_bias"], a["state_pool"], a["cu_seqlens"], a["state_indices"])
+    with pytest.raises(ValueError):   # eager mask shorter than the batch
+        api.kda_commit(*common, torch.tensor([2], dtype=i32), a["records"], window=4,
+                       record_slots=1, pending=torch.zeros(1, dtype=i32),
+                       eager=torch.zeros(0, dtype=torch.uint8))
+    with pytest.raises(ValueError):   # g_bias of one head for a two-head pool
+        api.kda_commit(a["A_log"], torch.zeros(128, dtype=f32), *common[2:],
+                       torch.tensor([2], dtype=i32), a["records"], window=4, record_slots=1)
+    with pytest.raises(ValueError):   # pending shorter than the record slots
+        api.kda_flush(a["A_log"], a["g_bias"], a["state_pool"], a["state_indices"], a["records"],
+                      torch.zeros(0, dtype=i32), window=4, record_slots=1)
