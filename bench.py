@@ -138,20 +138,86 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_path(workload: str) -> str:
+    return os.path.join(ROOT, "profiles", f"ncu_{workload}.json")
+
+
 def profiled_traffic(launch: str, workload: str):
-    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
-    recorded from an ncu capture in profiles/ncu_<workload>.md, if that
-    capture was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"ncu_{workload}.md")
+    """(DRAM bytes of one launch, where they came from): the ncu counters
+    dram__bytes_read.sum + dram__bytes_write.sum that ``--ncu-traffic``
+    wrote to profiles/ncu_<workload>.json from a capture of the same
+    launch, if that capture was taken on the current kernel sources; else
+    (None, why not)."""
+    path = traffic_path(workload)
+    rel = os.path.relpath(path, ROOT)
     try:
-        text = open(path).read()
-    except OSError:
-        return None
-    s = re.search(r"source_hash:\s*([0-9a-f]+)", text)
-    m = re.search(r"traffic\[" + re.escape(launch) + r"\]:\s*([0-9.eE+]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
-        return None
-    return float(m.group(1))
+        with open(path) as fh:
+            data = json.load(fh)
+    except (OSError, ValueError):
+        return None, f"no capture ({rel} missing)"
+    if data.get("source_hash") != kernel_source_hash():
+        return None, f"{rel} was captured on other kernel sources"
+    entry = data.get("launches", {}).get(launch)
+    if not entry:
+        return None, f"{rel} holds no launch named {launch}"
+    return (float(entry["traffic"]),
+            f"{rel}: ncu dram__bytes_read.sum + dram__bytes_write.sum of launch {launch}")
+
+
+def _ncu_value(value: str, unit: str) -> float:
+    scale = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+             "nsecond": 1.0, "usecond": 1e3, "msecond": 1e6, "second": 1e9}
+    factor = scale.get(unit.strip().lower())
+    if factor is None:
+        raise ValueError(f"unexpected ncu unit {unit!r}")
+    return float(value.replace(",", "")) * factor
+
+
+def read_ncu_csv(path: str):
+    """Launches of an ncu ``--csv`` metrics log, in capture order: a list of
+    (kernel name, {metric: value in bytes or nanoseconds})."""
+    import csv
+    with open(path, newline="") as fh:
+        lines = fh.read().splitlines()
+    start = next(i for i, ln in enumerate(lines) if ln.startswith('"ID"'))
+    launches = {}
+    for row in csv.DictReader(lines[start:]):
+        if not row.get("ID"):
+            continue
+        name, metrics = launches.setdefault(row["ID"], (row["Kernel Name"], {}))
+        metrics[row["Metric Name"]] = _ncu_value(row["Metric Value"], row["Metric Unit"])
+    return [launches[k] for k in sorted(launches, key=int)]
+
+
+def write_traffic(csv_path: str, workload: str, names, command: str) -> str:
+    """Write profiles/ncu_<workload>.json from an ncu capture of exactly the
+    launches of one step (``names``, in launch order)."""
+    launches = read_ncu_csv(csv_path)
+    if len(launches) != len(names):
+        raise ValueError(f"the capture holds {len(launches)} launches, one step has "
+                         f"{len(names)} ({', '.join(names)})")
+    out = {"workload": workload, "source_hash": kernel_source_hash(), "command": command,
+           "metric": "dram__bytes_read.sum + dram__bytes_write.sum (bytes per launch)",
+           "launches": {}}
+    for name, (kernel, m) in zip(names, launches):
+        if "step_kernel" not in kernel:
+            raise ValueError(f"launch {name} is {kernel}, not the step kernel")
+        rd, wr = m["dram__bytes_read.sum"], m["dram__bytes_write.sum"]
+        out["launches"][name] = {"kernel": kernel, "dram_bytes_read": rd,
+                                 "dram_bytes_write": wr, "traffic": rd + wr,
+                                 "duration_ns": m.get("gpu__time_duration.sum")}
+    path = traffic_path(workload)
+    with open(path, "w") as fh:
+        json.dump(out, fh, indent=1)
+        fh.write("\n")
+    return path
+
+
+def launch_names(wl: W.Workload):
+    """Names of one step's launches (the capture order of a step)."""
+    if wl.spec.deferred:
+        return ["verify", "commit_deferred", "verify_fused", "commit"]
+    return ["verify", "commit"]
 
 
 class ClockSampler:
@@ -464,30 +530,49 @@ def oracle_sample_run(wl: W.Workload, rows, threads: int, record_format: str = "
     return len(rows) * sp.H * sp.steps, dt
 
 
-def cpu_baseline(wl: W.Workload, budget_s: float, record_format: str = "raw"):
-    """Time the oracle on growing samples of rows until ``budget_s`` seconds
-    of CPU work have been measured (or the whole batch is done)."""
-    threads = max(1, os.cpu_count() or 1)
+def time_oracle(wl: W.Workload, budget_s: float, threads: int, record_format: str = "raw",
+                arithmetic: str = "fp64"):
+    """Time the oracle (or its float build) on growing samples of rows until
+    ``budget_s`` seconds of CPU work have been measured (or the whole batch
+    is done).  Returns (units per second, rows done, seconds)."""
+    from oracle import kda_oracle as O
     rng = np.random.default_rng(123)
     order = rng.permutation(wl.spec.B).tolist()
     units = 0
     secs = 0.0
     done = 0
     chunk = max(1, threads)
-    while done < len(order) and secs < budget_s:
-        rows = order[done:done + chunk]
-        u, dt = oracle_sample_run(wl, rows, threads, record_format)
-        units += u
-        secs += dt
-        done += len(rows)
-        chunk = min(len(order) - done, chunk * 2) if done < len(order) else 0
-        if chunk <= 0:
-            break
-    return {"value": units / secs if secs > 0 else None, "unit": UNIT, "cores": threads,
-            "kind": "oracle",
-            "sample": f"{done} of {wl.spec.B} rows x {wl.spec.H} heads x {wl.spec.steps} "
-                      f"decode step(s) of workload {wl.spec.name}, fp64 C oracle, "
-                      f"{threads} threads, {secs:.1f} s"}
+    with O.arithmetic(arithmetic):
+        while done < len(order) and secs < budget_s:
+            rows = order[done:done + chunk]
+            u, dt = oracle_sample_run(wl, rows, threads, record_format)
+            units += u
+            secs += dt
+            done += len(rows)
+            chunk = min(len(order) - done, chunk * 2) if done < len(order) else 0
+            if chunk <= 0:
+                break
+    return (units / secs if secs > 0 else None), done, secs
+
+
+def cpu_baseline(wl: W.Workload, budget_s: float, record_format: str = "raw"):
+    """The CPU baseline: the fp64 oracle on all host cores (the reported
+    value), beside the float build of the same C code on all cores and the
+    fp64 oracle on one core, each on a bounded sample of the workload."""
+    threads = max(1, os.cpu_count() or 1)
+    legs = []
+    for arith, nthreads, budget in (("fp64", threads, budget_s),
+                                    ("fp32", threads, budget_s / 2),
+                                    ("fp64", 1, budget_s / 2)):
+        value, done, secs = time_oracle(wl, budget, nthreads, record_format, arith)
+        legs.append({"arithmetic": arith, "cores": nthreads, "value": value,
+                     "sample": f"{done} of {wl.spec.B} rows x {wl.spec.H} heads x "
+                               f"{wl.spec.steps} decode step(s), {secs:.1f} s"})
+    main = legs[0]
+    return {"value": main["value"], "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{main['sample']} of workload {wl.spec.name}, fp64 C oracle, "
+                      f"{threads} threads",
+            "legs": legs}
 
 
 # ------------------------------------------------------------------- arms --
@@ -727,12 +812,13 @@ def run_ours(args):
                         "share": sum(per_kernel[n]) / max(1e-9, sum(sum(v) for v in
                                                                   per_kernel.values()))})
     dom = max(kernels, key=lambda x: x["share"])
+    traffic, traffic_src = profiled_traffic(
+        dom["name"], wl.spec.name if args.records == "raw" else f"{wl.spec.name}_{args.records}")
     step_bytes = sum(bytes_per.values())
     roofline = {"bound": "hbm", "kernel": dom["name"], "achieved": dom["gbs"], "peak": peak,
                 "unit": "GB/s", "frac": dom["gbs"] / peak,
                 "peak_source": f"{peak_src} ({'of measured' if peak_src == 'measured' else 'of fallback'})",
-                "traffic": profiled_traffic(dom["name"], wl.spec.name if args.records == "raw"
-                                            else f"{wl.spec.name}_{args.records}"),
+                "traffic": traffic, "traffic_source": traffic_src,
                 "algorithmic_bytes_per_launch": dom["bytes_per_launch"]}
     step_gbs = step_bytes * args.steps / (ms_total / 1e3) / 1e9
 
@@ -832,7 +918,18 @@ def main(argv=None):
     ap.add_argument("--reference-rows", type=int, default=8)
     ap.add_argument("--records", choices=["raw", "correction"], default="raw",
                     help="record format: raw inputs replayed (default) or fp32 deltas folded")
+    ap.add_argument("--ncu-traffic", metavar="CSV",
+                    help="write profiles/ncu_<config>.json from an ncu --csv log of one "
+                         "step's launches (dram__bytes_read.sum, dram__bytes_write.sum, "
+                         "--print-units base) and exit")
+    ap.add_argument("--ncu-command", default="",
+                    help="the ncu command line that made --ncu-traffic's log")
     args = ap.parse_args(argv)
+    if args.ncu_traffic:
+        wl = W.generate(args.config, seed=args.seed, pool=False)
+        name = args.config if args.records == "raw" else f"{args.config}_{args.records}"
+        print(write_traffic(args.ncu_traffic, name, launch_names(wl), args.ncu_command))
+        return
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)

@@ -52,6 +52,7 @@ invariants).
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from concurrent.futures import ThreadPoolExecutor
@@ -63,13 +64,29 @@ from . import build as _build
 
 _dbl_p = ctypes.POINTER(ctypes.c_double)
 
-_LIB = None
+_LIBS = {}
+_ARITHMETIC = "fp64"
+
+
+@contextlib.contextmanager
+def arithmetic(kind: str):
+    """Within the block, run the window loops in ``kind``: "fp64" (the
+    oracle) or "fp32" (a float build of the same C file).  Only the
+    benchmark's CPU baseline times the float build; the tests never use it."""
+    global _ARITHMETIC
+    if kind not in ("fp64", "fp32"):
+        raise ValueError("arithmetic must be 'fp64' or 'fp32'")
+    prev, _ARITHMETIC = _ARITHMETIC, kind
+    try:
+        yield
+    finally:
+        _ARITHMETIC = prev
 
 
 def _lib():
-    global _LIB
-    if _LIB is None:
-        path = _build.build()
+    lib = _LIBS.get(_ARITHMETIC)
+    if lib is None:
+        path = _build.library(_ARITHMETIC)
         lib = ctypes.CDLL(path)
         lib.kda_oracle_window.restype = ctypes.c_int
         lib.kda_oracle_window.argtypes = [
@@ -94,8 +111,8 @@ def _lib():
                                         ctypes.c_int, ctypes.c_double]
         lib.kda_oracle_round_bf16.restype = ctypes.c_double
         lib.kda_oracle_round_bf16.argtypes = [ctypes.c_double]
-        _LIB = lib
-    return _LIB
+        _LIBS[_ARITHMETIC] = lib
+    return lib
 
 
 def _ptr(a):

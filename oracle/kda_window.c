@@ -37,16 +37,39 @@
 #include <stdlib.h>
 #include <string.h>
 
-static double oracle_softplus(double x)
+/* Arithmetic type of the window loops.  The oracle is the double build.  The
+ * benchmark's CPU baseline also times a float build of this same file
+ * (-DKDA_ORACLE_FP32, libkda_oracle_fp32.so); no test uses that build. */
+#ifdef KDA_ORACLE_FP32
+typedef float real;
+#define R_EXP expf
+#define R_LOG1P log1pf
+#define R_SQRT sqrtf
+#else
+typedef double real;
+#define R_EXP exp
+#define R_LOG1P log1p
+#define R_SQRT sqrt
+#endif
+
+static real oracle_softplus(real x)
 {
-    if (x > 20.0)
+    if (x > (real)20.0)
         return x;
-    return log1p(exp(x));
+    return R_LOG1P(R_EXP(x));
 }
 
-static double oracle_sigmoid(double x)
+static real oracle_sigmoid(real x)
 {
-    return 1.0 / (1.0 + exp(-x));
+    return (real)1.0 / ((real)1.0 + R_EXP(-x));
+}
+
+static real oracle_gate(real x, real a_log, int bounded, real lower_bound)
+{
+    real a = R_EXP(a_log);
+    if (bounded)
+        return lower_bound * oracle_sigmoid(a * x);
+    return -a * oracle_softplus(x);
 }
 
 /* Gate of one channel: x = g_raw + g_bias.  The bounded form is the one
@@ -56,10 +79,7 @@ static double oracle_sigmoid(double x)
  * gate that kda.py names as the layer's default. */
 double kda_oracle_gate(double x, double a_log, int bounded, double lower_bound)
 {
-    double a = exp(a_log);
-    if (bounded)
-        return lower_bound * oracle_sigmoid(a * x);
-    return -a * oracle_softplus(x);
+    return (double)oracle_gate((real)x, (real)a_log, bounded, (real)lower_bound);
 }
 
 /* One window of T tokens from the state h0 (V x K, row-major, k fastest).
@@ -86,18 +106,20 @@ int kda_oracle_window(int K, int V, int T,
     if (q == NULL && out != NULL)
         return -1;
 
-    double *H = h_final;
-    memmove(H, h0, sizeof(double) * (size_t)V * (size_t)K);
-
-    double *kh = (double *)malloc(sizeof(double) * (size_t)K);
-    double *qh = (double *)malloc(sizeof(double) * (size_t)K);
-    double *decay = (double *)malloc(sizeof(double) * (size_t)K);
-    if (kh == NULL || qh == NULL || decay == NULL) {
+    size_t nvk = (size_t)V * (size_t)K;
+    real *H = (real *)malloc(sizeof(real) * nvk);
+    real *kh = (real *)malloc(sizeof(real) * (size_t)K);
+    real *qh = (real *)malloc(sizeof(real) * (size_t)K);
+    real *decay = (real *)malloc(sizeof(real) * (size_t)K);
+    if (H == NULL || kh == NULL || qh == NULL || decay == NULL) {
+        free(H);
         free(kh);
         free(qh);
         free(decay);
         return -1;
     }
+    for (size_t i = 0; i < nvk; ++i)
+        H[i] = (real)h0[i];
 
     for (int t = 0; t < T; ++t) {
         const double *kt = k + (size_t)t * K;
@@ -105,30 +127,30 @@ int kda_oracle_window(int K, int V, int T,
         const double *gt = g_raw + (size_t)t * K;
 
         /* L2 norm of k, eps inside the square root. */
-        double sk = 0.0;
+        real sk = 0;
         for (int c = 0; c < K; ++c)
-            sk += kt[c] * kt[c];
-        double nk = sqrt(sk + 1e-6);
+            sk += (real)kt[c] * (real)kt[c];
+        real nk = R_SQRT(sk + (real)1e-6);
         for (int c = 0; c < K; ++c)
-            kh[c] = kt[c] / nk;
+            kh[c] = (real)kt[c] / nk;
 
         /* L2 norm of q, then the scale. */
         if (q != NULL) {
             const double *qt = q + (size_t)t * K;
-            double sq = 0.0;
+            real sq = 0;
             for (int c = 0; c < K; ++c)
-                sq += qt[c] * qt[c];
-            double nq = sqrt(sq + 1e-6);
+                sq += (real)qt[c] * (real)qt[c];
+            real nq = R_SQRT(sq + (real)1e-6);
             for (int c = 0; c < K; ++c)
-                qh[c] = qt[c] / nq * scale;
+                qh[c] = (real)qt[c] / nq * (real)scale;
         }
 
         /* Per-channel decay factor exp(g). */
         for (int c = 0; c < K; ++c)
-            decay[c] = exp(kda_oracle_gate(gt[c] + g_bias[c], a_log, bounded,
-                                           lower_bound));
+            decay[c] = R_EXP(oracle_gate((real)gt[c] + (real)g_bias[c], (real)a_log, bounded,
+                                         (real)lower_bound));
 
-        double beta = oracle_sigmoid(beta_raw[t]);
+        real beta = oracle_sigmoid((real)beta_raw[t]);
 
         /* Decay: every row scales column c by the same factor. */
         for (int r = 0; r < V; ++r)
@@ -138,32 +160,36 @@ int kda_oracle_window(int K, int V, int T,
         /* Delta and rank-one update, one row at a time: the row's own
          * prediction H[r,:] . k^ only involves that row. */
         for (int r = 0; r < V; ++r) {
-            double *row = H + (size_t)r * K;
-            double u = 0.0;
+            real *row = H + (size_t)r * K;
+            real u = 0;
             for (int c = 0; c < K; ++c)
                 u += row[c] * kh[c];
-            double vp = beta * (vt[r] - u);
+            real vp = beta * ((real)vt[r] - u);
             for (int c = 0; c < K; ++c)
                 row[c] += vp * kh[c];
             if (delta != NULL)
-                delta[(size_t)t * V + r] = vp;
+                delta[(size_t)t * V + r] = (double)vp;
         }
 
         /* Output after the update. */
         if (out != NULL) {
             for (int r = 0; r < V; ++r) {
-                const double *row = H + (size_t)r * K;
-                double o = 0.0;
+                const real *row = H + (size_t)r * K;
+                real o = 0;
                 for (int c = 0; c < K; ++c)
                     o += row[c] * qh[c];
-                out[(size_t)t * V + r] = o;
+                out[(size_t)t * V + r] = (double)o;
             }
         }
 
         if (traj != NULL)
-            memcpy(traj + (size_t)t * V * K, H, sizeof(double) * (size_t)V * K);
+            for (size_t i = 0; i < nvk; ++i)
+                traj[(size_t)t * nvk + i] = (double)H[i];
     }
 
+    for (size_t i = 0; i < nvk; ++i)
+        h_final[i] = (double)H[i];
+    free(H);
     free(kh);
     free(qh);
     free(decay);
@@ -195,11 +221,11 @@ int kda_oracle_fold_deltas(int K, int V, int n,
     if (K <= 0 || V <= 0 || n < 0)
         return -1;
     size_t nk = (size_t)(n > 0 ? n : 1) * (size_t)K;
-    double *kh = (double *)malloc(sizeof(double) * nk);
-    double *e = (double *)malloc(sizeof(double) * nk);
-    double *coef = (double *)malloc(sizeof(double) * nk);
-    double *P = (double *)malloc(sizeof(double) * (size_t)K);
-    double *acc = (double *)malloc(sizeof(double) * (size_t)V * (size_t)K);
+    real *kh = (real *)malloc(sizeof(real) * nk);
+    real *e = (real *)malloc(sizeof(real) * nk);
+    real *coef = (real *)malloc(sizeof(real) * nk);
+    real *P = (real *)malloc(sizeof(real) * (size_t)K);
+    real *acc = (real *)malloc(sizeof(real) * (size_t)V * (size_t)K);
     if (kh == NULL || e == NULL || coef == NULL || P == NULL || acc == NULL) {
         free(kh);
         free(e);
@@ -211,19 +237,19 @@ int kda_oracle_fold_deltas(int K, int V, int n,
     for (int t = 0; t < n; ++t) {
         const double *kt = k + (size_t)t * K;
         const double *gt = g_raw + (size_t)t * K;
-        double sk = 0.0;
+        real sk = 0;
         for (int c = 0; c < K; ++c)
-            sk += kt[c] * kt[c];
-        double nrm = sqrt(sk + 1e-6);
+            sk += (real)kt[c] * (real)kt[c];
+        real nrm = R_SQRT(sk + (real)1e-6);
         for (int c = 0; c < K; ++c) {
-            kh[(size_t)t * K + c] = kt[c] / nrm;
-            e[(size_t)t * K + c] = exp(kda_oracle_gate(gt[c] + g_bias[c], a_log, bounded,
-                                                       lower_bound));
+            kh[(size_t)t * K + c] = (real)kt[c] / nrm;
+            e[(size_t)t * K + c] = R_EXP(oracle_gate((real)gt[c] + (real)g_bias[c], (real)a_log,
+                                                     bounded, (real)lower_bound));
         }
     }
     /* P runs from P_n = 1 down to P_0; coef_t = k^_t * P_t. */
     for (int c = 0; c < K; ++c)
-        P[c] = 1.0;
+        P[c] = 1;
     for (int t = n - 1; t >= 0; --t) {
         for (int c = 0; c < K; ++c) {
             coef[(size_t)t * K + c] = kh[(size_t)t * K + c] * P[c];
@@ -232,12 +258,13 @@ int kda_oracle_fold_deltas(int K, int V, int n,
     }
     for (int r = 0; r < V; ++r)
         for (int c = 0; c < K; ++c) {
-            double s = h0[(size_t)r * K + c] * P[c];
+            real s = (real)h0[(size_t)r * K + c] * P[c];
             for (int t = 0; t < n; ++t)
-                s += delta[(size_t)t * V + r] * coef[(size_t)t * K + c];
+                s += (real)delta[(size_t)t * V + r] * coef[(size_t)t * K + c];
             acc[(size_t)r * K + c] = s;
         }
-    memcpy(h_final, acc, sizeof(double) * (size_t)V * (size_t)K);
+    for (size_t i = 0; i < (size_t)V * (size_t)K; ++i)
+        h_final[i] = (double)acc[i];
     free(kh);
     free(e);
     free(coef);

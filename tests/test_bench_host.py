@@ -2,6 +2,7 @@
 over gloo), the per-rank seeds of weak scaling, the algorithmic byte count,
 the clock-sample summary and the profile lookup."""
 
+import json
 import os
 import socket
 import sys
@@ -147,24 +148,76 @@ def test_clock_summary_filters_the_timed_window():
     assert s["samples"] == 1 and s["sm_mhz"] == 1900
 
 
-def test_profiled_traffic_requires_current_sources(tmp_path, monkeypatch):
+_NCU_HEADER = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+               '"Block Size","Grid Size","Device","CC","Section Name","Metric Name",'
+               '"Metric Unit","Metric Value"')
+
+
+def _ncu_csv(path, launches):
+    """An ncu --csv metrics log (one row per launch and metric)."""
+    rows = ["==PROF== Connected to process 1 (python3)", _NCU_HEADER]
+    for i, (kernel, metrics) in enumerate(launches):
+        for name, unit, value in metrics:
+            rows.append(f'"{i}","1","python3","host","{kernel}","1","7","(384, 1, 1)",'
+                        f'"(152, 1, 1)","0","10.3","Command line profiler metrics","{name}",'
+                        f'"{unit}","{value}"')
+    path.write_text("\n".join(rows) + "\n")
+
+
+def _fake_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "profiles").mkdir()
     csrc = tmp_path / "linear_attention_speculative_kda_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (csrc / "kda_kernels.cu").write_text("kernel v1")
     (csrc / "kda_conv.cu").write_text("conv v1")
-    h = bench.kernel_source_hash()
-    (tmp_path / "profiles" / "ncu_w.md").write_text(
-        f"source_hash: {h}\ntraffic[verify]: 1234\n")
-    assert bench.profiled_traffic("verify", "w") == 1234.0
-    assert bench.profiled_traffic("commit", "w") is None
+    return csrc
+
+
+def test_traffic_is_written_from_ncu_and_read_back(tmp_path, monkeypatch):
+    csrc = _fake_sources(tmp_path, monkeypatch)
+    kern = "void kda::step_kernel<(kda::Mode)0, false, false, false>(kda::Params, int, int)"
+    csv_path = tmp_path / "dram.csv"
+    _ncu_csv(csv_path, [
+        (kern, [("dram__bytes_read.sum", "byte", "1,143,000,000"),
+                ("dram__bytes_write.sum", "byte", "66,100,000"),
+                ("gpu__time_duration.sum", "nsecond", "245,000")]),
+        (kern.replace(")0", ")1"), [("dram__bytes_read.sum", "Mbyte", "898.6"),
+                                     ("dram__bytes_write.sum", "Gbyte", "0.8098"),
+                                     ("gpu__time_duration.sum", "usecond", "296.9")])])
+    wl = W.generate("tiny", pool=False)
+    assert bench.launch_names(wl) == ["verify", "commit"]
+    path = bench.write_traffic(str(csv_path), "w", bench.launch_names(wl), "ncu ... bench.py")
+    data = json.loads(open(path).read())
+    assert data["command"] == "ncu ... bench.py"
+    assert data["launches"]["verify"]["traffic"] == 1143000000 + 66100000
+    assert data["launches"]["commit"]["traffic"] == 898.6e6 + 0.8098e9
+    assert data["launches"]["commit"]["duration_ns"] == 296900.0
+    traffic, src = bench.profiled_traffic("verify", "w")
+    assert traffic == 1209100000.0 and "profiles/ncu_w.json" in src
+    assert bench.profiled_traffic("flush", "w")[0] is None
     (csrc / "kda_conv.cu").write_text("conv v2")   # not the step kernel's source
-    assert bench.profiled_traffic("verify", "w") == 1234.0
+    assert bench.profiled_traffic("verify", "w")[0] == 1209100000.0
     (csrc / "kda_kernels.cu").write_text("kernel  v1 // a comment\n/* another */")
-    assert bench.profiled_traffic("verify", "w") == 1234.0   # comments and layout only
+    assert bench.profiled_traffic("verify", "w")[0] == 1209100000.0   # comments and layout only
     (csrc / "kda_kernels.cu").write_text("kernel v2")
-    assert bench.profiled_traffic("verify", "w") is None
+    traffic, src = bench.profiled_traffic("verify", "w")
+    assert traffic is None and "other kernel sources" in src
+
+
+def test_traffic_writer_refuses_a_partial_step(tmp_path, monkeypatch):
+    _fake_sources(tmp_path, monkeypatch)
+    csv_path = tmp_path / "dram.csv"
+    _ncu_csv(csv_path, [("void kda::step_kernel<>(kda::Params, int, int)",
+                         [("dram__bytes_read.sum", "byte", "1"),
+                          ("dram__bytes_write.sum", "byte", "2")])])
+    with pytest.raises(ValueError, match="one step has 4"):
+        bench.write_traffic(str(csv_path), "d", bench.launch_names(W.generate(
+            "deferred2", pool=False)), "")
+    _ncu_csv(csv_path, [("at::FillFunctor", [("dram__bytes_read.sum", "byte", "1"),
+                                             ("dram__bytes_write.sum", "byte", "2")])] * 2)
+    with pytest.raises(ValueError, match="not the step kernel"):
+        bench.write_traffic(str(csv_path), "t", ["verify", "commit"], "")
 
 
 def test_code_text_strips_comments():
@@ -219,3 +272,14 @@ def test_reference_arm_prints_the_contract_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["config"]["workload"] == "tiny"
+
+
+def test_cpu_baseline_reports_three_legs():
+    """The CPU baseline times the fp64 oracle on all cores (its value), the
+    float build of the same C code on all cores and the oracle on one core."""
+    line = bench.cpu_baseline(W.generate("tiny"), 0.2)
+    legs = line["legs"]
+    assert [(leg["arithmetic"], leg["cores"]) for leg in legs] == [
+        ("fp64", line["cores"]), ("fp32", line["cores"]), ("fp64", 1)]
+    assert line["kind"] == "oracle" and line["value"] == legs[0]["value"]
+    assert all(leg["value"] > 0 for leg in legs)
