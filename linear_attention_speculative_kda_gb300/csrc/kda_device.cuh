@@ -102,6 +102,13 @@ __device__ __forceinline__ float inv_l2(float sum) {
     return rsqrtf(__fadd_rn(sum, 1e-6f));
 }
 
+// The gate's exponentials use CUDA's __expf intrinsic and its divisions the
+// __fdividef intrinsic: their documented error bounds (2 + floor(|1.16 x|)
+// ulp for __expf, 2 ulp for __fdividef in this range) cost the state a few
+// ulp per token, far inside the state tolerance, and they take half the
+// instructions of the accurate forms on the producer's path.  Verify and
+// commit call the same functions, so their states stay bit-identical.
+//
 // softplus(x) = log(1 + e^x), taken as x itself for x > 20, evaluated as
 // max(x, 0) + log1p(z) with z = e^{-|x|} in (0, 1] (an identity) and
 // log1p(z) = z * P(z): P is a degree-9 least-squares fit of log1p(z) / z on
@@ -111,7 +118,7 @@ __device__ __forceinline__ float softplus(float x) {
     constexpr float c[10] = {0x1p+0f,        -0x1.ffffcp-2f,  0x1.554c9cp-2f, -0x1.ff11c2p-3f,
                              0x1.930202p-3f, -0x1.399642p-3f, 0x1.b2c2a2p-4f, -0x1.d3784ep-5f,
                              0x1.4628bp-6f,  -0x1.aad1eep-9f};
-    const float z = expf(-fabsf(x));
+    const float z = __expf(-fabsf(x));
     float r = c[9];
 #pragma unroll
     for (int i = 8; i >= 0; --i) r = __fmaf_rn(r, z, c[i]);
@@ -126,14 +133,14 @@ __device__ __forceinline__ float softplus(float x) {
 __device__ __forceinline__ float decay_factor(float x, float a, bool bounded, float lb) {
     float g;
     if (bounded)
-        g = __fdiv_rn(lb, __fadd_rn(1.0f, expf(-__fmul_rn(a, x))));
+        g = __fdividef(lb, __fadd_rn(1.0f, __expf(-__fmul_rn(a, x))));
     else
         g = -__fmul_rn(a, softplus(x));
-    return expf(g);
+    return __expf(g);
 }
 
 __device__ __forceinline__ float sigmoidf_rn(float x) {
-    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
+    return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-x)));
 }
 
 // Packed pairs of fp32 operations (Blackwell's f32x2 forms): each lane does

@@ -464,27 +464,27 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
         if (lane == 0) cp_async4(rv.a_log, p.A_log + w.head);
     }
     if constexpr (kMode == Mode::kVerify) {
-        for (int c = warp; c < 4 * w.T; c += kProducerWarps) {
-            const int t = c >> 2;
-            const int part = c & 3;
-            const size_t tok = (size_t)(w.bos + t);
-            const __nv_bfloat16 *src;
-            uint32_t *dst;
-            if (part == 0) {
-                src = p.k + tok * p.stride_k;
-                dst = rv.k + (w.p + t) * (kD / 2);
-            } else if (part == 1) {
-                src = p.v + tok * p.stride_v;
-                dst = rv.v + (w.p + t) * RawView<kCorr>::kVWords;
-            } else if (part == 2) {
-                src = p.g + tok * p.stride_g;
-                dst = rv.g + (w.p + t) * (kD / 2);
-            } else {
-                src = p.q + tok * p.stride_q;
-                dst = rv.q + t * (kD / 2);
-            }
-            cp_async8(dst + 2 * lane, reinterpret_cast<const uint2 *>(src + w.head * kD) + lane);
+        // producer warp w copies part w (k, v, g_raw, q) of every new token:
+        // one source row and one destination slot per token
+        static_assert(kProducerWarps == 4, "one activation part per producer warp");
+        const __nv_bfloat16 *src;
+        long long stride;
+        uint32_t *dst;
+        int dstep;
+        if (warp == 0) {
+            src = p.k, stride = p.stride_k, dst = rv.k + w.p * (kD / 2), dstep = kD / 2;
+        } else if (warp == 1) {
+            src = p.v, stride = p.stride_v, dst = rv.v + w.p * RawView<kCorr>::kVWords,
+            dstep = RawView<kCorr>::kVWords;
+        } else if (warp == 2) {
+            src = p.g, stride = p.stride_g, dst = rv.g + w.p * (kD / 2), dstep = kD / 2;
+        } else {
+            src = p.q, stride = p.stride_q, dst = rv.q, dstep = kD / 2;
         }
+        const uint2 *row = reinterpret_cast<const uint2 *>(src + (size_t)w.bos * stride +
+                                                           w.head * kD) + lane;
+        const long long rstep = stride / 4;  // uint2 per token (the stride is a multiple of 4)
+        for (int t = 0; t < w.T; ++t) cp_async8(dst + t * dstep + 2 * lane, row + t * rstep);
     }
     cp_async_commit();
 }
