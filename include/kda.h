@@ -293,12 +293,25 @@ typedef struct kda_align {
 } kda_align;
 
 /*
- * kda_commit_align -- the eager commit in align mode: as kda_commit with
- * pending == NULL, but the replayed states go to the final and boundary
- * blocks above.  Rows with a request index outside [0, num_requests), a
- * negative num_computed or a boundary block past the table are skipped and
- * flagged KDA_ROW_BAD_BLOCK; a block >= num_slots flags KDA_ROW_BAD_SLOT.
- * num_accepted: int32 [num_requests].
+ * kda_commit_align -- the commit in align mode: as kda_commit, but the
+ * replayed states go to the final and boundary blocks above.  Rows with a
+ * request index outside [0, num_requests), a negative num_computed or a
+ * boundary block past the table are skipped and flagged KDA_ROW_BAD_BLOCK; a
+ * block >= num_slots flags KDA_ROW_BAD_SLOT.  num_accepted: int32
+ * [num_requests].
+ *
+ * pending == NULL: every valid row is committed now (eager).
+ * pending != NULL (the deferred commit of [KIMI] `KDADeferredCommitContext.commit`
+ * with a block table): a valid row is committed now when eager[b] != 0
+ * (eager may be NULL: no row), when its final block is not its own state
+ * slot state_indices[b], or when it owes a boundary block (boundary_len <
+ * n); its pending[r] is set to 0.  Any other valid row only sets pending[r]
+ * = n: its final block is its own slot and no boundary state is due, so the
+ * next verify's fold (or kda_flush), which stores to the row's slot, leaves
+ * exactly what this commit would have written.  Rows that commit nothing,
+ * and rows skipped for bad metadata whose record slot is in range, get
+ * pending[r] = 0.  The pages leave the fold's target in align mode open;
+ * this rule is the reading that keeps every block right.
  */
 kda_status kda_commit_align(const kda_config *cfg,
                             const float *A_log, const float *g_bias,
@@ -308,6 +321,7 @@ kda_status kda_commit_align(const kda_config *cfg,
                             const int32_t *num_accepted,
                             const int32_t *record_rows, const void *records,
                             const kda_align *align,
+                            int32_t *pending, const uint8_t *eager,
                             int32_t *error_word, void *stream);
 
 /*

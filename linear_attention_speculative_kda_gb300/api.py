@@ -141,7 +141,7 @@ def load_library():
     lib.kda_conv_compact.argtypes = [ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] + [vp] * 3
     alp = ctypes.POINTER(KdaAlign)
     lib.kda_commit_align.restype = ctypes.c_int
-    lib.kda_commit_align.argtypes = [cfgp] + [vp] * 5 + [i32] + [vp] * 3 + [alp, vp, vp]
+    lib.kda_commit_align.argtypes = [cfgp] + [vp] * 5 + [i32] + [vp] * 3 + [alp, vp, vp, vp, vp]
     lib.kda_conv_compact_align.restype = ctypes.c_int
     lib.kda_conv_compact_align.argtypes = ([ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] +
                                            [vp, alp, vp, vp])
@@ -533,10 +533,14 @@ def _check_align(block_table, num_computed, request_indices, dev):
 def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_accepted, records,
                      block_table, num_computed, *, block_size: int, window: int,
                      record_slots: int, lower_bound=None, record_rows=None,
-                     request_indices=None, error_word=None, record_format: str = "raw") -> None:
-    """``kda_commit_align``: the eager commit writing the final and boundary
-    blocks of a paged state cache.  num_accepted, num_computed and the block
-    table rows are per request; ``record_format`` as for ``kda_commit``."""
+                     request_indices=None, pending=None, eager=None, error_word=None,
+                     record_format: str = "raw") -> None:
+    """``kda_commit_align``: the commit writing the final and boundary blocks
+    of a paged state cache.  num_accepted, num_computed and the block table
+    rows are per request; ``record_format`` as for ``kda_commit``.  With
+    ``pending`` (and optionally ``eager``), the deferred form: rows that stay
+    in their own slot and owe no boundary block only record their pending
+    replay."""
     dev = state_pool.device
     f32, i32 = torch.float32, torch.int32
     for name, t in (("A_log", A_log), ("g_bias", g_bias), ("state_pool", state_pool)):
@@ -546,6 +550,8 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
     _req(state_indices, i32, "state_indices", dev)
     _req(num_accepted, i32, "num_accepted", dev)
     _opt(record_rows, i32, "record_rows", dev)
+    _opt(pending, i32, "pending", dev)
+    _opt(eager, torch.uint8, "eager", dev)
     _opt(error_word, i32, "error_word", dev)
     _check_align(block_table, num_computed, request_indices, dev)
     S, H, D = _check_pool(state_pool)
@@ -556,7 +562,7 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
             raise ValueError("metadata tensors must be contiguous")
     if cu_seqlens.shape[0] != B + 1 or num_accepted.shape[0] < block_table.shape[0]:
         raise ValueError("metadata sizes do not match the batch")
-    _check_rows(B, record_slots, record_rows, None, None, error_word)
+    _check_rows(B, record_slots, record_rows, pending, eager, error_word)
     if request_indices is not None:
         _at_least(request_indices, B, "request_indices")
     cfg = _config(H, window, S, record_slots, lower_bound, None, (1, 1, 1, 1, 1), D,
@@ -567,7 +573,7 @@ def kda_commit_align(A_log, g_bias, state_pool, cu_seqlens, state_indices, num_a
     st = lib.kda_commit_align(ctypes.byref(cfg), _ptr(A_log), _ptr(g_bias), _ptr(state_pool),
                               _ptr(cu_seqlens), _ptr(state_indices), B, _ptr(num_accepted),
                               _ptr(record_rows), _ptr(records), ctypes.byref(al),
-                              _ptr(error_word), _stream_ptr(dev))
+                              _ptr(pending), _ptr(eager), _ptr(error_word), _stream_ptr(dev))
     _check("kda_commit_align", st)
 
 

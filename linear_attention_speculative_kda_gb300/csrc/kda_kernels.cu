@@ -166,7 +166,11 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
             valid = w.dst > 0;
         }
         if (p.pending_out != nullptr) {
-            const bool now = p.eager != nullptr && p.eager[b] != 0;
+            // deferred: eager rows commit now; in align mode so does a row
+            // whose final block is not its own slot or that owes a boundary
+            // block (the later fold stores to the row's slot only)
+            bool now = p.eager != nullptr && p.eager[b] != 0;
+            if (p.block_table != nullptr && valid) now = now || w.dst != row.slot || w.mid > 0;
             if (head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
             if (!now) return false;
         }
@@ -1023,8 +1027,8 @@ kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const flo
                             float *state_pool, const int32_t *cu_seqlens,
                             const int32_t *state_indices, int32_t B,
                             const int32_t *num_accepted, const int32_t *record_rows,
-                            const void *records, const kda_align *align,
-                            int32_t *error_word, void *stream) {
+                            const void *records, const kda_align *align, int32_t *pending,
+                            const uint8_t *eager, int32_t *error_word, void *stream) {
     kda_status st = check_config(cfg);
     if (st != KDA_OK) return st;
     if (B < 0) return KDA_ERR_INVALID_ARG;
@@ -1034,6 +1038,8 @@ kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const flo
     if (st != KDA_OK) return st;
     if (!cu_seqlens || !num_accepted) return KDA_ERR_INVALID_ARG;
     if (!aligned(cu_seqlens, 4) || !aligned(num_accepted, 4)) return KDA_ERR_INVALID_ARG;
+    if (pending != nullptr && !aligned(pending, 4)) return KDA_ERR_INVALID_ARG;
+    if (pending == nullptr && eager != nullptr) return KDA_ERR_INVALID_ARG;
 
     Params p = base_params(cfg, B);
     st = set_align(align, cfg->window, p);
@@ -1046,6 +1052,8 @@ kda_status kda_commit_align(const kda_config *cfg, const float *A_log, const flo
     p.record_rows = record_rows;
     p.num_accepted = num_accepted;
     p.records = const_cast<__nv_bfloat16 *>(static_cast<const __nv_bfloat16 *>(records));
+    p.pending_out = pending;
+    p.eager = eager;
     p.err = error_word;
 
     return launch_step<kda::Mode::kCommit>(p, cfg, false, static_cast<cudaStream_t>(stream));
@@ -1087,6 +1095,6 @@ const char *kda_status_string(kda_status status) {
     return "KDA_ERR_UNKNOWN";
 }
 
-int32_t kda_abi_version(void) { return 3; }
+int32_t kda_abi_version(void) { return 4; }
 
 }  // extern "C"

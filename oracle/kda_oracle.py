@@ -569,8 +569,8 @@ def _align_row(layer, cache_slots, T, slot, num_accepted, num_computed, block_ro
 
 
 def commit_align(layer: Layer, cache: Cache, step: Step, num_accepted, block_table,
-                 num_computed, block_size: int, *, request_indices=None, rows=None,
-                 heads=None, threads: int = 1) -> list:
+                 num_computed, block_size: int, *, request_indices=None, deferred: bool = False,
+                 eager=None, rows=None, heads=None, threads: int = 1) -> list:
     """Align-mode commit (recoverssm.py commit context with a block table;
     ``_replay_indices_kernel``): each valid row replays its first n records
     from the checkpoint of ``state_indices[b]`` and writes the state after
@@ -578,12 +578,25 @@ def commit_align(layer: Layer, cache: Cache, step: Step, num_accepted, block_tab
     token (boundary_len < n), the state after boundary_len tokens to the
     boundary block.  The source slot itself is not written unless it is one
     of those blocks.  ``num_accepted``, ``num_computed`` and the block-table
-    rows are indexed by request (``request_indices[b]``, or b).  Returns the
-    list of invalid rows."""
+    rows are indexed by request (``request_indices[b]``, or b).
+
+    ``deferred`` (the Kimi-K3 context page's commit with a block table and
+    pending / eager): a valid row whose final block is its own state slot
+    and that owes no boundary block only records n as the pending replay of
+    its record slot; the next verify's fold, which stores to the row's slot,
+    then leaves the state after n tokens in that final block.  Every other
+    valid row (an ``eager`` row, a row whose accepted tokens end in another
+    block, or one that crosses a boundary before its last token) is
+    committed now, and its pending count, like that of every row that
+    commits nothing, is set to 0.  Returns the list of invalid rows."""
     B = len(step.state_indices)
     H = layer.num_heads
     rows = range(B) if rows is None else rows
     heads = range(H) if heads is None else heads
+
+    def clear(r):
+        if deferred and r >= 0:
+            cache.pending[r] = 0
 
     def run(b):
         T = _row_len(step.cu_seqlens, b)
@@ -591,22 +604,33 @@ def commit_align(layer: Layer, cache: Cache, step: Step, num_accepted, block_tab
         r = _record_slot(step.record_rows, b)
         bad = _row_checks(layer, cache, T, slot, r)
         if bad:
+            if bad != "record":
+                clear(r)
             return RowIssue(b, bad)
         req = b if request_indices is None else int(request_indices[b])
         if req < 0 or req >= len(block_table):
+            clear(r)
             return RowIssue(b, "block")
         if r < 0:  # no records: nothing to replay
             return None
         plan, bad = _align_row(layer, cache.num_slots, T, slot, num_accepted[req],
                                num_computed[req], block_table[req], block_size)
         if bad:
+            clear(r)
             return RowIssue(b, bad)
         if plan is None:
+            clear(r)
             return None
+        mid_due = plan.boundary > 0 and plan.boundary_len < plan.n
+        if deferred:
+            now = (eager is not None and bool(eager[b])) or plan.final != slot or mid_due
+            cache.pending[r] = 0 if now else plan.n
+            if not now:
+                return None
         for h in heads:
             # both replays start from the checkpoint as it was before the commit
             mid = None
-            if plan.boundary > 0 and plan.boundary_len < plan.n:
+            if mid_due:
                 mid = _replay_records(layer, cache, slot, h, r, plan.boundary_len)
             end = _replay_records(layer, cache, slot, h, r, plan.n)
             if mid is not None:

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(api.EXPORTED)
     for name in names:
         assert hasattr(lib, name), name
-    assert lib.kda_abi_version() == 3
+    assert lib.kda_abi_version() == 4
     assert lib.kda_status_string(api.KDA_ERR_CUDA) == b"KDA_ERR_CUDA"
 
 
@@ -180,13 +180,13 @@ def _align(**kw):
 
 def _commit_align(lib, al, cfg=None, B=3, **ptrs):
     p = dict(a_log=FAKE, g_bias=FAKE, pool=FAKE, cu=FAKE, slots=FAKE, acc=FAKE, rr=None,
-             records=FAKE, err=None)
+             records=FAKE, pending=None, eager=None, err=None)
     p.update(ptrs)
     cfg = _cfg() if cfg is None else cfg
     alp = None if al is None else ctypes.byref(al)
     return lib.kda_commit_align(ctypes.byref(cfg), p["a_log"], p["g_bias"], p["pool"], p["cu"],
-                                p["slots"], B, p["acc"], p["rr"], p["records"], alp, p["err"],
-                                None)
+                                p["slots"], B, p["acc"], p["rr"], p["records"], alp,
+                                p["pending"], p["eager"], p["err"], None)
 
 
 def test_commit_align_host_checks(lib):
@@ -204,6 +204,9 @@ def test_commit_align_host_checks(lib):
     assert _commit_align(lib, _align(), cfg=_cfg(window=9)) == api.KDA_ERR_UNSUPPORTED
     assert _commit_align(lib, _align(), B=-1) == api.KDA_ERR_INVALID_ARG
     assert _commit_align(lib, None, B=0) == api.KDA_OK
+    # the deferred form: an eager mask needs pending; pending needs 4-byte alignment
+    assert _commit_align(lib, _align(), eager=FAKE) == api.KDA_ERR_INVALID_ARG
+    assert _commit_align(lib, _align(), pending=FAKE + 2) == api.KDA_ERR_INVALID_ARG
 
 
 def test_conv_compact_align_host_checks(lib):

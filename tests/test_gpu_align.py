@@ -227,3 +227,67 @@ def test_full_size_align_commit():
     assert cache.written
     for (slot, h), ref in cache.written.items():
         assert_state_close(g.pool[slot, h].double().cpu().numpy(), ref)
+
+
+def _deferred_align_case(Q, bounded, seed):
+    """Rows whose state slot is the block of their last computed token (the
+    table column (c - 1) // bs, as a runner keeps it), so that the deferred
+    form defers the rows that stay in their block."""
+    B = 12
+    lens = [Q, Q, max(1, Q - 1), Q, min(2, Q), Q, Q, 1, Q, Q, max(1, Q - 2), Q]
+    kw = dict(bounded=True, lower_bound=-5.0) if bounded else {}
+    wl = W.custom(B=B, H=2, Q=Q, lens=lens, S=1 + B + B * WIDTH, seed=seed,
+                  slots=list(range(1, B + 1)), **kw)
+    rng = np.random.default_rng(seed)
+    bs = max(Q, 4) * 2
+    nc = rng.integers(1, bs * (WIDTH - 1), size=B).astype(np.int32)
+    table = (1 + B + np.arange(B * WIDTH)).reshape(B, WIDTH).astype(np.int32)
+    for b in range(B):
+        table[b, (nc[b] - 1) // bs] = int(wl.state_indices[b])
+    eager = (rng.random(B) < 0.25).astype(np.uint8)
+    return wl, table, nc, bs, eager
+
+
+@pytest.mark.parametrize("Q,bounded", [(4, False), (8, True)])
+def test_deferred_align_commit_against_oracle_and_eager(Q, bounded):
+    """The deferred align commit: pending counts equal the oracle's, the rows
+    committed now match the oracle and the eager align commit bit for bit, and
+    after a flush the whole pool equals the eager align commit's."""
+    wl, table, nc, bs, eager = _deferred_align_case(Q, bounded, seed=60 + Q)
+    d = torch.device("cuda")
+    i32 = dict(dtype=torch.int32, device=d)
+    acc = wl.steps[0].num_accepted.numpy()
+    e, g = DeviceRun(wl), DeviceRun(wl)
+    for run in (e, g):
+        run.verify()
+    _run_align(e, wl, table, nc, bs)
+    g.pending.fill_(7)
+    api.kda_commit_align(g.A_log, g.g_bias, g.pool, g.cu, g.slots, g.steps[0]["num_accepted"],
+                         g.records, torch.tensor(table, **i32), torch.tensor(nc, **i32),
+                         block_size=bs, record_rows=g.record_rows, pending=g.pending,
+                         eager=torch.tensor(eager, dtype=torch.uint8, device=d),
+                         error_word=g.err, **g.kw())
+    torch.cuda.synchronize()
+    assert int(e.err.item()) == 0 and int(g.err.item()) == 0
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)
+    cache.pending[:] = 7
+    cache.written.clear()
+    assert O.commit_align(layer, cache, step, acc, table, nc, bs, deferred=True,
+                          eager=eager) == []
+    assert g.pending.cpu().tolist() == cache.pending.tolist()
+    deferred = [b for b in range(wl.spec.B) if cache.pending[b] > 0]
+    assert deferred and len(deferred) < wl.spec.B     # both kinds occur
+    pool = g.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
+        assert torch.equal(pool[slot, h], e.pool[slot, h].cpu())
+    # the deferred rows' slots still hold the checkpoint until the fold
+    for b in deferred:
+        s = int(wl.state_indices[b])
+        assert torch.equal(g.pool[s], g.pool0[s])
+    g.flush()
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    assert torch.equal(g.pool, e.pool)

@@ -171,3 +171,54 @@ def test_invalid_blocks_are_reported():
     nc[1] = bs * 6 + bs - 1                    # boundary block beyond the table
     issues = O.commit_align(layer, cache, step, acc, table, nc, bs)
     assert [(i.row, i.reason) for i in issues][:2] == [(0, "slot"), (1, "block")]
+
+
+def _deferred_case():
+    """Six rows whose state slot is the block of their last computed token
+    (column (c - 1) // bs of their table row, as a runner keeps it): row 0
+    stays in that block, row 1 starts the next block, row 2 crosses a
+    boundary before its last token, row 3 is eager, row 4 accepts nothing,
+    row 5 reaches the boundary exactly at its last token."""
+    wl = W.custom(B=6, H=2, Q=4, lens=[4] * 6, S=60, seed=33, slots=[1, 2, 3, 4, 5, 6])
+    bs, width = 8, 4
+    nc = np.array([10, 16, 13, 10, 10, 12])
+    table = np.arange(20, 20 + 6 * width).reshape(6, width)
+    for b in range(6):
+        table[b, (nc[b] - 1) // bs] = int(wl.state_indices[b])
+    acc = np.array([3, 4, 4, 2, 0, 4])
+    eager = np.array([0, 0, 0, 1, 0, 0], np.uint8)
+    return wl, table, nc, bs, acc, eager
+
+
+def test_deferred_align_commits_only_rows_that_leave_their_block():
+    wl, table, nc, bs, acc, eager = _deferred_case()
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    cache = oracle_cache(wl)
+    O.verify(layer, cache, step)
+    cache.pending[:] = 7                              # stale counts
+    cache.written.clear()
+    assert O.commit_align(layer, cache, step, acc, table, nc, bs, deferred=True,
+                          eager=eager) == []
+    # rows 0 and 5 keep their state in their own slot: pending replays
+    assert cache.pending.tolist() == [3, 0, 0, 0, 0, 4]
+    # rows 1, 2 (final and boundary block) and 3 are committed now
+    final = {b: O.align_plan(int(acc[b]), int(nc[b]), table[b], bs) for b in (1, 2, 3)}
+    want = {(final[b].final, h) for b in (1, 2, 3) for h in range(2)}
+    want |= {(final[2].boundary, h) for h in range(2)}
+    assert final[2].boundary_len == 3 and final[3].final == int(wl.state_indices[3])
+    assert set(cache.written) == want
+
+
+def test_deferred_align_then_flush_equals_the_eager_align_commit():
+    wl, table, nc, bs, acc, eager = _deferred_case()
+    layer, step = oracle_layer(wl), oracle_step(wl)
+    eager_cache, deferred_cache = oracle_cache(wl), oracle_cache(wl)
+    for c in (eager_cache, deferred_cache):
+        O.verify(layer, c, step)
+    assert O.commit_align(layer, eager_cache, step, acc, table, nc, bs) == []
+    assert O.commit_align(layer, deferred_cache, step, acc, table, nc, bs, deferred=True,
+                          eager=eager) == []
+    assert O.flush(layer, deferred_cache, step) == []
+    for s in range(wl.spec.S):
+        for h in range(wl.spec.H):
+            assert np.array_equal(eager_cache.state(s, h), deferred_cache.state(s, h)), (s, h)
