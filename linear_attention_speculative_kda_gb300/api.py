@@ -124,7 +124,15 @@ def load_library():
         raise RuntimeError(
             f"libkda.so not found at {_LIBRARY}; build it first "
             "(python -c 'import __graft_entry__ as g; g.build()')")
-    lib = ctypes.CDLL(_LIBRARY)
+    _lib_handle = bind_library(_LIBRARY)
+    return _lib_handle
+
+
+def bind_library(path: str):
+    """A ctypes handle of a build of the library at ``path`` (libkda.so, or a
+    test variant from build.build_variant) with every entry point's argument
+    types declared."""
+    lib = ctypes.CDLL(path)
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     cfgp = ctypes.POINTER(KdaConfig)
     lib.kda_records_bytes.restype = ctypes.c_size_t
@@ -149,7 +157,6 @@ def load_library():
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_abi_version.restype = i32
     lib.kda_abi_version.argtypes = []
-    _lib_handle = lib
     return lib
 
 

@@ -41,7 +41,7 @@ def _stale() -> bool:
     return any(os.path.getmtime(src) > built for src in DEPENDS)
 
 
-def compile_command(output: str, extra=()) -> list[str]:
+def compile_command(output: str, extra=(), sources=None) -> list[str]:
     return [
         nvcc_path(),
         *ARCH_FLAGS,
@@ -58,7 +58,7 @@ def compile_command(output: str, extra=()) -> list[str]:
         *extra,
         "-o",
         output,
-        *SOURCES,
+        *(SOURCES if sources is None else sources),
     ]
 
 
@@ -71,6 +71,30 @@ def build(force: bool = False, verbose: bool = False) -> str:
     subprocess.run(compile_command(tmp, extra), check=True)
     os.replace(tmp, LIBRARY)
     return LIBRARY
+
+
+VARIANT_DIR = os.path.join(PKG, "_variants")
+
+
+def build_variant(name: str, defines, force: bool = False) -> str:
+    """Build a test variant of the library with extra preprocessor
+    definitions, into _variants/libkda_<name>.so; never the product library.
+    The tests use it for paths no input of the C ABI can reach (a wait that
+    runs out)."""
+    os.makedirs(VARIANT_DIR, exist_ok=True)
+    out = os.path.join(VARIANT_DIR, f"libkda_{name}.so")
+    if not force and os.path.exists(out) and not _stale_against(out):
+        return out
+    tmp = out + f".tmp{os.getpid()}"
+    extra = [f"-D{d}" for d in defines]
+    subprocess.run(compile_command(tmp, extra), check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _stale_against(path: str) -> bool:
+    built = os.path.getmtime(path)
+    return any(os.path.getmtime(src) > built for src in DEPENDS)
 
 
 if __name__ == "__main__":

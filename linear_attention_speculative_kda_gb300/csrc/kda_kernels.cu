@@ -226,7 +226,12 @@ constexpr int kProducerBarrier = 1;  // named barrier of the producer warps
 // 4 tokens lose (deferred2's verify 245 -> 272 us).
 constexpr int kWindowMinT = 5;
 constexpr int kPlanSize = kProducerThreads;
+#ifdef KDA_TEST_WAIT_BUDGET
+// a test build: a short budget, so that a wait the test starves runs out fast
+constexpr long long kWaitBudget = KDA_TEST_WAIT_BUDGET;
+#else
 constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
+#endif
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kLaunchRegs = 168;     // 65536 / 384, rounded down to a multiple of 8
 constexpr int kConsumerRegs = 208;
@@ -667,6 +672,14 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             const int b = use_c % lay.nbuf;
             const int use_b = use_c / lay.nbuf;
             if (use_b > 0 && !wait_phase(&sy.empty_tok[c][b], (use_b - 1) & 1, sy, p)) return;
+#ifdef KDA_TEST_WITHHOLD_END_MARKER
+            // a test build of the timeout path: consumer 0 of CTA 0 is never
+            // told that its work is done, so its wait for a next item runs
+            // out.  Every copy into this CTA's shared memory has landed by
+            // then: the consumer waited for each checkpoint it loaded, and
+            // the producer for each item's raw inputs.
+            if (c == 0 && blockIdx.x == 0) continue;
+#endif
             sy.info[c][b].end = 1;
             mbar_arrive(&sy.full_tok[c][b]);
         }
