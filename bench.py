@@ -166,7 +166,8 @@ def profiled_traffic(launch: str, workload: str):
 
 def _ncu_value(value: str, unit: str) -> float:
     scale = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
-             "nsecond": 1.0, "usecond": 1e3, "msecond": 1e6, "second": 1e9}
+             "nsecond": 1.0, "usecond": 1e3, "msecond": 1e6, "second": 1e9,
+             "ns": 1.0, "us": 1e3, "ms": 1e6, "s": 1e9}
     factor = scale.get(unit.strip().lower())
     if factor is None:
         raise ValueError(f"unexpected ncu unit {unit!r}")

@@ -181,7 +181,7 @@ def test_traffic_is_written_from_ncu_and_read_back(tmp_path, monkeypatch):
     _ncu_csv(csv_path, [
         (kern, [("dram__bytes_read.sum", "byte", "1,143,000,000"),
                 ("dram__bytes_write.sum", "byte", "66,100,000"),
-                ("gpu__time_duration.sum", "nsecond", "245,000")]),
+                ("gpu__time_duration.sum", "ns", "245000")]),
         (kern.replace(")0", ")1"), [("dram__bytes_read.sum", "Mbyte", "898.6"),
                                      ("dram__bytes_write.sum", "Gbyte", "0.8098"),
                                      ("gpu__time_duration.sum", "usecond", "296.9")])])
