@@ -101,18 +101,18 @@ __device__ __forceinline__ int align_targets(const Params &p, int req, int n, Wo
     return 0;
 }
 
-// Plan one tile: row checks, the commit plan (n = clamp(accepted, 0,
-// min(T, Q)), valid iff slot > 0, n > 0, r >= 0), the deferred commit's
-// pending write.  Side effects (error bits, pending writes) are made by the
-// one thread that plans the tile.
+// Plan row b for head `head`: row checks, the commit plan (n = clamp(accepted,
+// 0, min(T, Q)), valid iff slot > 0, n > 0, r >= 0), the deferred commit's
+// pending write.  Every head of a row has the same plan.  The row's side
+// effects (error bits, pending writes) are made only when `side_effects` is
+// set, by the one thread of the grid that plans the row for that purpose.
 template <Mode kMode>
-__device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
-    const int b = tile / p.H;
-    const int head = tile - b * p.H;
+__device__ __forceinline__ bool plan_row(const Params &p, int b, int head, bool side_effects,
+                                         Work &w) {
     Row row;
     const int bad = read_row(p, b, kMode != Mode::kFlush, row);
     if (bad) {
-        if (head == 0) {
+        if (side_effects) {
             flag_error(p.err, bad);
             // a deferred commit clears the pending count of a skipped row
             // whose record slot is usable: its records are this step's, so
@@ -129,7 +129,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (p.pending_in != nullptr && row.r >= 0) {
             fold = p.pending_in[row.r];
             if (fold < 0 || fold > p.Q) {
-                if (head == 0) flag_error(p.err, kBadPending);
+                if (side_effects) flag_error(p.err, kBadPending);
                 return false;
             }
         }
@@ -142,7 +142,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (p.block_table != nullptr) {
             if (p.request_indices != nullptr) req = p.request_indices[b];
             if (req < 0 || req >= p.num_requests) {
-                if (head == 0) {
+                if (side_effects) {
                     flag_error(p.err, kBadBlock);
                     if (p.pending_out != nullptr && row.r >= 0) p.pending_out[row.r] = 0;
                 }
@@ -157,7 +157,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (p.block_table != nullptr && valid) {
             const int bad_align = align_targets(p, req, n, w);
             if (bad_align) {
-                if (head == 0) {
+                if (side_effects) {
                     flag_error(p.err, bad_align);
                     if (p.pending_out != nullptr && row.r >= 0) p.pending_out[row.r] = 0;
                 }
@@ -171,7 +171,7 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
             // block (the later fold stores to the row's slot only)
             bool now = p.eager != nullptr && p.eager[b] != 0;
             if (p.block_table != nullptr && valid) now = now || w.dst != row.slot || w.mid > 0;
-            if (head == 0 && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
+            if (side_effects && row.r >= 0) p.pending_out[row.r] = (valid && !now) ? n : 0;
             if (!now) return false;
         }
         if (!valid) return false;
@@ -180,13 +180,13 @@ __device__ __forceinline__ bool plan_tile(const Params &p, int tile, Work &w) {
         if (row.slot <= 0 || row.r < 0) return false;
         const int n = p.pending_in[row.r];
         if (n < 0 || n > p.Q) {
-            if (head == 0) flag_error(p.err, kBadPending);
+            if (side_effects) flag_error(p.err, kBadPending);
             return false;
         }
         if (n == 0) return false;
         fold = n;
     }
-    w.tile = tile;
+    w.tile = b * p.H + head;
     w.head = head;
     w.slot = row.slot;
     w.r = row.r;
@@ -266,7 +266,18 @@ struct WorkList {
     int mid_len[kPlanSize];
     int warp_count[kProducerWarps];
     int count;
-    int pad;
+    int rows_per_thread;  // balanced plan: rows each producer thread scans (0: strided plan)
+    // balanced plan (when shared memory has room for it): mask[t] bit i
+    // marks row t * rows_per_thread + i as having work; prefix[t] counts the
+    // work rows of the threads before t
+    unsigned *mask;
+    int *prefix;
+};
+
+struct Balance {
+    unsigned mask[kPlanSize];
+    int prefix[kPlanSize + 1];
+    int pad[3];
 };
 
 // Hand-off barriers and the abort flag.
@@ -314,7 +325,7 @@ __host__ __device__ inline int raw_buffer_bytes(int slots, int Q, bool corr) {
 // record format).
 struct Layout {
     int slots, nbuf, tok_bytes, raw_bytes;
-    int off_state, off_tok, off_raw, off_list, off_sync, total;
+    int off_state, off_tok, off_raw, off_list, off_sync, off_bal, total;
 };
 
 __host__ __device__ inline Layout make_layout(int Q, bool fold, bool corr) {
@@ -330,6 +341,9 @@ __host__ __device__ inline Layout make_layout(int Q, bool fold, bool corr) {
     l.off_list = l.off_raw + 2 * l.raw_bytes;
     l.off_sync = l.off_list + (int)sizeof(WorkList);
     l.total = l.off_sync + (int)sizeof(Sync);
+    // the balanced plan's arrays, where they fit (else the strided plan)
+    l.off_bal = l.total + (int)sizeof(Balance) <= kSmemBudget ? l.total : -1;
+    if (l.off_bal >= 0) l.total += (int)sizeof(Balance);
     return l;
 }
 
@@ -354,20 +368,111 @@ __device__ __forceinline__ void producer_sync() {
     asm volatile("bar.sync %0, %1;" ::"n"(kProducerBarrier), "n"(kProducerThreads) : "memory");
 }
 
-__device__ __forceinline__ int num_candidates(int num_tiles) {
+// Candidate tiles of this CTA: of the balanced plan's work tiles, or of all
+// tiles (the strided plan), every gridDim.x-th from blockIdx.x.
+__device__ __forceinline__ int num_candidates(const WorkList &list, int num_tiles, int H) {
+    const int total = list.rows_per_thread > 0 ? list.prefix[kPlanSize] * H : num_tiles;
     const int first = (int)blockIdx.x;
-    return first < num_tiles ? (num_tiles - first + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    return first < total ? (total - first + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
+// Balanced plan, for batches of at most kBalanceRows rows.  With the
+// strided plan every CTA takes every gridDim.x-th tile, and rows without
+// work (null rows, nothing accepted, deferred rows) leave some CTAs with
+// far more work than others.  Here every CTA first scans all rows: producer
+// thread t checks rows t R .. t R + R - 1 (R = ceil(B / kPlanSize)) and marks
+// those with work; the work rows, in row order, times the heads are the work
+// tiles, and every CTA takes every gridDim.x-th of them.  A row's side
+// effects (error bits, pending writes) are made by one CTA, row b's by CTA
+// b mod gridDim.x, during this scan.
+constexpr int kBalanceRowsPerThread = 32;
+constexpr int kBalanceRows = kPlanSize * kBalanceRowsPerThread;
+
+template <Mode kMode>
+__device__ void balance_scan(const Params &p, WorkList &list, Balance *bal, int pt) {
+    // Commits and flushes only: their rows without work (nothing accepted,
+    // deferred, no pending replay) are what unbalances the strided plan.  A
+    // verify has work in almost every row, and there the scan measured
+    // slower than the strided plan (mixed verify 266 -> 273 us, deferred2
+    // fused verify 344 -> 349 us; commits 1 to 8 us faster).
+    const int R = (kMode != Mode::kVerify && bal != nullptr && p.B <= kBalanceRows)
+                      ? (p.B + kPlanSize - 1) / kPlanSize
+                      : 0;
+    if (pt == 0) {
+        list.rows_per_thread = R;
+        list.mask = bal != nullptr ? bal->mask : nullptr;
+        list.prefix = bal != nullptr ? bal->prefix : nullptr;
+    }
+    if (R == 0) {
+        producer_sync();
+        return;
+    }
+    unsigned m = 0u;
+#pragma unroll 4
+    for (int i = 0; i < kBalanceRowsPerThread; ++i) {
+        const int b = pt * R + i;
+        if (i < R && b < p.B) {
+            Work w;
+            if (plan_row<kMode>(p, b, 0, b % (int)gridDim.x == (int)blockIdx.x, w)) m |= 1u << i;
+        }
+    }
+    // exclusive prefix of the per-thread counts: a warp scan, then the warps'
+    // totals
+    const int lane = pt & 31, warp = pt >> 5;
+    const int cnt = __popc(m);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) list.warp_count[warp] = incl;
+    bal->mask[pt] = m;
+    producer_sync();
+    int before = 0;
+#pragma unroll
+    for (int i = 0; i < kProducerWarps; ++i)
+        if (i < warp) before += list.warp_count[i];
+    bal->prefix[pt] = before + incl - cnt;
+    if (pt == kPlanSize - 1) bal->prefix[kPlanSize] = before + incl;
+    producer_sync();
+}
+
+// Row of the rank-th work row of the balanced plan.
+__device__ __forceinline__ int balanced_row(const WorkList &list, int rank) {
+    int lo = 0, hi = kPlanSize;  // prefix[lo] <= rank < prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (list.prefix[mid] <= rank)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    unsigned m = list.mask[lo];
+    for (int j = rank - list.prefix[lo]; j > 0; --j) m &= m - 1u;  // drop the lowest j bits
+    return lo * list.rows_per_thread + (__ffs(m) - 1);
 }
 
 // One planning round over candidates [k0, k0 + kPlanSize) by the producer
 // threads; compacts the tiles with work, in order, into the list.
 template <Mode kMode>
 __device__ int plan_round(const Params &p, WorkList &list, int k0, int num_tiles, int pt) {
-    const int K = num_candidates(num_tiles);
+    const int K = num_candidates(list, num_tiles, p.H);
     Work w;
     bool has = false;
     const int k = k0 + pt;
-    if (k < K) has = plan_tile<kMode>(p, (int)blockIdx.x + k * (int)gridDim.x, w);
+    if (k < K) {
+        const int c = (int)blockIdx.x + k * (int)gridDim.x;
+        if (list.rows_per_thread > 0) {
+            const int rank = c / p.H;
+            const int head = c - rank * p.H;
+            has = plan_row<kMode>(p, balanced_row(list, rank), head, false, w);
+        } else {
+            const int b = c / p.H;
+            const int head = c - b * p.H;
+            has = plan_row<kMode>(p, b, head, head == 0, w);
+        }
+    }
     const unsigned ballot = __ballot_sync(kFull, has);
     const int lane = pt & 31, warp = pt >> 5;
     if (lane == 0) list.warp_count[warp] = __popc(ballot);
@@ -405,7 +510,7 @@ struct Cursor {
 template <Mode kMode>
 __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Cursor &c,
                                           int num_tiles, int pt) {
-    const int K = num_candidates(num_tiles);
+    const int K = num_candidates(list, num_tiles, p.H);
     Work w;
     w.tile = -1;
     while (c.idx >= c.count) {
@@ -602,6 +707,9 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
     Cursor cursor{0, 0, 0};
+    balance_scan<kMode>(p, list,
+                        lay.off_bal >= 0 ? reinterpret_cast<Balance *>(smem + lay.off_bal) : nullptr,
+                        pt);
     Work cur = next_work<kMode>(p, list, cursor, num_tiles, pt);
     int rb = 0;
     uint32_t beta_next = 0;
