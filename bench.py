@@ -110,7 +110,7 @@ def hbm_peak():
 
 
 # the sources of the verify / commit kernel (the conv kernel has its own file)
-STEP_SOURCES = ("kda_align.cuh", "kda_async.cuh", "kda_device.cuh", "kda_kernels.cu")
+STEP_SOURCES = ("kda_align.cuh", "kda_async.cuh", "kda_device.cuh", "kda_kernels.cu", "kda_tc.cuh")
 
 
 _COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)

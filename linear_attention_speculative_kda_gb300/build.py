@@ -20,6 +20,7 @@ DEPENDS = SOURCES + [
     os.path.join(CSRC, "kda_device.cuh"),
     os.path.join(CSRC, "kda_async.cuh"),
     os.path.join(CSRC, "kda_align.cuh"),
+    os.path.join(CSRC, "kda_tc.cuh"),
     os.path.join(ROOT, "include", "kda.h"),
 ]
 LIBRARY = os.path.join(PKG, "libkda.so")

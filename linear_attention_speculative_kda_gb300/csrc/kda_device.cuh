@@ -26,6 +26,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kda_tc.cuh"
+
 namespace kda {
 
 constexpr int kD = 128;             // head dim, K = V
@@ -72,6 +74,9 @@ struct Params {
     const int *block_table, *num_computed, *request_indices;
     long long bt_stride;
     int bt_width, block_size, num_requests;
+    // verify window items with no folded token on the tensor core (the
+    // launch's tensor map of the state pool is valid)
+    int tc_window;
 };
 
 // ---------------------------------------------------------------- helpers --
@@ -222,23 +227,40 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 // window form (see window_outputs) a new token's kh and qh slots hold the
 // decay-weighted G_t * k^_t and G_t * q^_t instead, and pa / pb the pair
 // coefficients of the window (Q x Q each, row t, column s).
+//
+// Two layouts.  In the tail layout the vectors start at the buffer and the
+// small arrays (beta, kq, pa, pb) follow them.  In the head layout (raw
+// records, windows of 5 or more tokens) the small arrays come first and the
+// vectors start kTokHead bytes in, on a 1024-byte boundary, with at least
+// kXBytes of them: a verify item in tensor window form (window_tc_prep)
+// overwrites those bytes with its swizzled tensor-core operands.
+constexpr int kTokHead = 1024;
+constexpr int kXBytes = 2 * 16 * kD * 4;  // X_hi and X_lo: 16 vectors of 128 fp32 each
+constexpr int kXBlock = 32 * 128;          // one 32-column block of the 32 operand rows
+
+__host__ __device__ inline int tok_small_bytes(int slots, int Q) {
+    return ((slots + 3) / 4) * 16 + ((Q + 3) / 4) * 16 + ((2 * Q * Q + 3) / 4) * 16;
+}
+
 struct TokView {
     float *kh, *e, *v, *qh, *beta, *kq, *pa, *pb;
-    __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q) {
-        kh = reinterpret_cast<float *>(base);
+    __device__ __forceinline__ TokView(unsigned char *base, int slots, int Q, bool head) {
+        kh = reinterpret_cast<float *>(head ? base + kTokHead : base);
         e = kh + slots * kD;
         v = e + slots * kD;
         qh = v + slots * kD;
-        beta = qh + Q * kD;
+        beta = head ? reinterpret_cast<float *>(base) : qh + Q * kD;
         kq = beta + ((slots + 3) / 4) * 4;  // k^ . q^ of each new token
         pa = kq + ((Q + 3) / 4) * 4;
         pb = pa + Q * Q;
     }
 };
 
-__host__ __device__ inline int tok_buffer_bytes(int slots, int Q) {
-    return (3 * slots + Q) * kD * 4 + ((slots + 3) / 4) * 16 + ((Q + 3) / 4) * 16 +
-           ((2 * Q * Q + 3) / 4) * 16;
+__host__ __device__ inline int tok_buffer_bytes(int slots, int Q, bool head) {
+    const int vec = (3 * slots + Q) * kD * 4;
+    if (!head) return vec + tok_small_bytes(slots, Q);
+    const int bytes = kTokHead + (vec > kXBytes ? vec : kXBytes);
+    return (bytes + 1023) / 1024 * 1024;  // every buffer on a 1024-byte boundary
 }
 
 // ------------------------------------------------------------ state tile --
@@ -265,6 +287,26 @@ __device__ __forceinline__ void store_tile(const Tile &h, float *tile, const Lan
 #pragma unroll
         for (int m = 0; m < 4; ++m)
             *reinterpret_cast<float4 *>(tile + L.row(i) * kD + L.col(m)) = h[i][m];
+}
+
+// The tile from / to a staging buffer in the tensor core's layout: four
+// 32-column blocks of 128 rows, 128-byte swizzled (see kda_tc.cuh).
+__device__ __forceinline__ void load_tile_sw(Tile &h, const unsigned char *staging, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            h[i][m] = *reinterpret_cast<const float4 *>(staging + m * 16384 +
+                                                        sw128_offset(L.row(i), 4 * L.j));
+}
+
+__device__ __forceinline__ void store_tile_sw(const Tile &h, unsigned char *staging, const Lane &L) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            *reinterpret_cast<float4 *>(staging + m * 16384 + sw128_offset(L.row(i), 4 * L.j)) =
+                h[i][m];
 }
 
 __device__ __forceinline__ float4 ld_cols(const float *vec, const Lane &L, int m) {
@@ -570,6 +612,166 @@ __device__ __forceinline__ void window_outputs(const Tile &h, const TokView &tv,
 #pragma unroll
             for (int s = 0; s <= t; ++s) o = __fmaf_rn(tv.pb[t * Q + s], vp[s], o);
             out0[(size_t)t * out_stride + row] = __float2bfloat16_rn(o);
+        }
+    }
+}
+
+// ----------------------------------------------------- tensor window form --
+//
+// The same window form with its 2T row dot products on the tensor core:
+// D = S X^T, S the state the new tokens start from (128 x 128) and X
+// the 16 operand vectors X_t = G_t * k^_t and X_{8+t} = G_t * q^_t (t < T;
+// the rows of the other vectors are never read back), so that D[v][t] = w_t
+// and D[v][8+t] = y_t of row v.  The products are tcgen05.mma of kind::tf32
+// with fp32 accuracy: with S = S_hi + S_lo and X = X_hi + X_lo split at the
+// TF32 precision the tensor core reads, the operand B holds X_hi in rows
+// 0..15 and X_lo in rows 16..31 (N = 32), and
+//   D_hi = S_hi [X_hi; X_lo]^T,   D_lo = S_lo [X_hi; X_lo]^T
+// are accumulated apart (every product of the four parts, 16 K steps each)
+// and added in fp32, the small terms first.  S_hi is S in the
+// swizzled staging buffer itself (the tensor core drops the low bits): the
+// staged checkpoint, or, after folded tokens, the folded state written back
+// there.  S_lo goes to TMEM, X_hi and X_lo to shared memory.  Thread ct of
+// the consumer group owns channel ct of the vectors and row ct of S, D and
+// the outputs.  New token t sits in slot p0 + t (p0 folded tokens first).
+
+// Pair coefficients, then the operand vectors of the channel into shared
+// memory (swizzled, K-major).  The thread keeps its row's v_t in vrow: the
+// vectors' bytes are overwritten.  group_sync() as in window_prep.
+template <class GroupSync>
+__device__ __forceinline__ bool window_tc_prep(const TokView &tv, int p0, int T, int Q, int ct,
+                                               float (&vrow)[kMaxQ], GroupSync &&group_sync) {
+    const int lane = ct & 31, warp = ct >> 5;
+    if (warp < (T + 1) / 2) {
+        float val[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) val[i] = 0.0f;
+        const int s0 = warp, s1 = T - 1 - warp;
+        pair_row<false>(tv, p0, T, s0, lane, val);
+        if (s1 != s0) pair_row<true>(tv, p0, T, s1, lane, val);
+        const float sum = reduce16(val, lane);
+        if (lane < 16) {
+            int s = -1, slot = lane;
+            if (slot <= 2 * (T - 1 - s0)) {
+                s = s0;
+            } else if (s1 != s0 && slot >= 15 - 2 * (T - 1 - s1)) {
+                s = s1;
+                slot = 15 - slot;
+            }
+            if (s >= 0) {
+                const int d = (slot + 1) >> 1;
+                float *dst = (slot & 1) ? tv.pa : tv.pb;
+                dst[(s + d) * Q + s] = sum;
+            }
+        }
+    }
+    float gk[kMaxQ], gq[kMaxQ];
+    float G = 1.0f;
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            G = __fmul_rn(G, tv.e[(p0 + t) * kD + ct]);
+            gk[t] = __fmul_rn(G, tv.kh[(p0 + t) * kD + ct]);
+            gq[t] = __fmul_rn(G, tv.qh[t * kD + ct]);
+            vrow[t] = tv.v[(p0 + t) * kD + ct];
+        }
+    }
+    if (!group_sync()) return false;  // every read of the vectors done
+    // head layout: the operands take the vectors' bytes, from kh on; X_hi of
+    // vector n in operand row n, X_lo in row 16 + n, the 32-column block of
+    // channel ct
+    unsigned char *xb = reinterpret_cast<unsigned char *>(tv.kh) + (ct >> 5) * kXBlock;
+    const int col = ct & 31;
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            const float hk = tf32_hi(gk[t]), hq = tf32_hi(gq[t]);
+            *reinterpret_cast<float *>(xb + sw128_offset(t, col)) = hk;
+            *reinterpret_cast<float *>(xb + sw128_offset(16 + t, col)) = __fsub_rn(gk[t], hk);
+            *reinterpret_cast<float *>(xb + sw128_offset(8 + t, col)) = hq;
+            *reinterpret_cast<float *>(xb + sw128_offset(24 + t, col)) = __fsub_rn(gq[t], hq);
+        }
+    }
+    fence_proxy_async_smem();  // the tensor core reads X through the async proxy
+    return true;
+}
+
+// S_lo of row ct (S in the staging buffer, four swizzled 32-column blocks)
+// into TMEM columns s_lo .. s_lo + 127 of the thread's lane, 16 at a time.
+__device__ __forceinline__ void s_lo_to_tmem(const unsigned char *staging, int ct,
+                                             uint32_t s_lo) {
+#pragma unroll
+    for (int half = 0; half < 8; ++half) {
+        uint32_t u[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float4 q = *reinterpret_cast<const float4 *>(
+                staging + (half >> 1) * 16384 + sw128_offset(ct, 16 * (half & 1) + 4 * c));
+            u[4 * c + 0] = __float_as_uint(__fsub_rn(q.x, tf32_hi(q.x)));
+            u[4 * c + 1] = __float_as_uint(__fsub_rn(q.y, tf32_hi(q.y)));
+            u[4 * c + 2] = __float_as_uint(__fsub_rn(q.z, tf32_hi(q.z)));
+            u[4 * c + 3] = __float_as_uint(__fsub_rn(q.w, tf32_hi(q.w)));
+        }
+        tmem_st16(s_lo + 16 * half, u);
+    }
+}
+
+// D_hi = S_hi [X_hi; X_lo]^T over K = 128 (16 steps of 8), A from the
+// staging buffer; by one thread.  A step's descriptors are the first ones
+// plus its byte offset / 16 (the start address field does not overflow).
+__device__ __forceinline__ void window_tc_mma_hi(uint32_t staging, uint32_t xbase,
+                                                 uint32_t d_hi) {
+    constexpr uint32_t idesc = tf32_idesc(128, 32);
+    const uint64_t a0 = sw128_desc(staging), b0 = sw128_desc(xbase);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        const uint32_t w = (uint32_t)(k & 3) * 32u;
+        umma_tf32_ss(d_hi, a0 + (((uint32_t)(k >> 2) * 16384u + w) >> 4),
+                     b0 + (((uint32_t)(k >> 2) * (uint32_t)kXBlock + w) >> 4), idesc, k > 0);
+    }
+}
+
+// D_lo = S_lo [X_hi; X_lo]^T, A from TMEM (S_lo, one fp32 per column).
+__device__ __forceinline__ void window_tc_mma_lo(uint32_t s_lo, uint32_t xbase, uint32_t d_lo) {
+    constexpr uint32_t idesc = tf32_idesc(128, 32);
+    const uint64_t b0 = sw128_desc(xbase);
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        umma_tf32_ts(d_lo, s_lo + 8u * (uint32_t)k,
+                     b0 + (((uint32_t)(k >> 2) * (uint32_t)kXBlock + (uint32_t)(k & 3) * 32u) >> 4),
+                     idesc, k > 0);
+}
+
+// The solve of row ct from D_hi (32 columns at TMEM address d of the
+// thread's lane) and D_lo (the 32 after them), as in window_outputs:
+// v'_t = beta_t (v_t - w_t - sum_{s<t} a_ts v'_s), o_t = y_t + sum_{s<=t} b_ts v'_s.
+__device__ __forceinline__ void window_tc_solve(const TokView &tv, int p0, int T, int Q, int ct,
+                                                const float (&vrow)[kMaxQ], uint32_t d,
+                                                __nv_bfloat16 *out0, size_t out_stride) {
+    uint32_t h0[16], h1[16], l0[16], l1[16];  // D_hi: X_hi, X_lo columns; D_lo: the same
+    tmem_ld16(d, h0);
+    tmem_ld16(d + 16u, h1);
+    tmem_ld16(d + 32u, l0);
+    tmem_ld16(d + 48u, l1);
+    tmem_wait_ld();
+    auto dot = [&](int n) {  // the small terms first
+        const float lo = __fadd_rn(__uint_as_float(l0[n]), __uint_as_float(l1[n]));
+        return __fadd_rn(__uint_as_float(h0[n]), __fadd_rn(__uint_as_float(h1[n]), lo));
+    };
+    float vp[kMaxQ];
+#pragma unroll
+    for (int t = 0; t < kMaxQ; ++t) {
+        if (t < T) {
+            const float w = dot(t);
+            const float y = dot(8 + t);
+            float acc = __fsub_rn(vrow[t], w);
+#pragma unroll
+            for (int s = 0; s < t; ++s) acc = __fmaf_rn(-tv.pa[t * Q + s], vp[s], acc);
+            vp[t] = __fmul_rn(tv.beta[p0 + t], acc);
+            float o = y;
+#pragma unroll
+            for (int s = 0; s <= t; ++s) o = __fmaf_rn(tv.pb[t * Q + s], vp[s], o);
+            out0[(size_t)t * out_stride + ct] = __float2bfloat16_rn(o);
         }
     }
 }

@@ -16,9 +16,11 @@
 // A verify item with 5 or more new tokens computes its outputs in the
 // window form (kda_device.cuh); every stored state is computed token by
 // token.  The public contract is in include/kda.h.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "kda_align.cuh"
 #include "kda_async.cuh"
@@ -225,6 +227,18 @@ constexpr int kProducerBarrier = 1;  // named barrier of the producer warps
 // take it (mixed's verify 297 -> 288 us; all items: no gain), and windows of
 // 4 tokens lose (deferred2's verify 245 -> 272 us).
 constexpr int kWindowMinT = 5;
+// The tensor window form (window items' row products on the tensor core) is
+// a build option, off by default: measured on the window-8 workload
+// (256 requests x 16 heads) its verify took 111 us against 88 us for the
+// FMA window form.  Per item, each of its 32 tcgen05.mma of 128 x 32 x 8
+// takes about 130 cycles to issue, the staging buffer stays held until the
+// products finish, and the coefficients and the solve, unchanged, dominate
+// the consumer's chain.
+#ifdef KDA_TENSOR_WINDOW
+constexpr bool kTensorWindow = true;
+#else
+constexpr bool kTensorWindow = false;
+#endif
 constexpr int kPlanSize = kProducerThreads;
 #ifdef KDA_TEST_WAIT_BUDGET
 // a test build: a short budget, so that a wait the test starves runs out fast
@@ -287,7 +301,10 @@ struct Sync {
     uint64_t full_tok[2][2];   // token vectors of an item are ready
     uint64_t empty_tok[2][2];  // the consumer is done with them
     uint64_t group[2];         // a consumer's own barrier (window form)
+    uint64_t mma_hi[2];        // a consumer's products from the staging buffer are complete
+    uint64_t mma_done[2];      // all of a consumer's tensor-core products are complete
     ItemInfo info[2][2];
+    uint32_t tmem_base;        // tensor memory of the CTA (tensor window form)
     int abort;
     int leave[2];   // per item parity: the producer threads leave (abort seen)
     int pad;
@@ -322,16 +339,21 @@ __host__ __device__ inline int raw_buffer_bytes(int slots, int Q, bool corr) {
 }
 
 // Shared-memory layout of a launch (window Q, whether the verify folds, the
-// record format).
+// record format, whether it is a window kernel).  A window kernel of the
+// tensor window form uses the head token layout: every token buffer and
+// staging buffer sits on a 1024-byte boundary of the (1024-byte aligned)
+// dynamic shared memory.
 struct Layout {
     int slots, nbuf, tok_bytes, raw_bytes;
     int off_state, off_tok, off_raw, off_list, off_sync, off_bal, total;
+    bool head;
 };
 
-__host__ __device__ inline Layout make_layout(int Q, bool fold, bool corr) {
+__host__ __device__ inline Layout make_layout(int Q, bool fold, bool corr, bool window) {
     Layout l;
     l.slots = fold ? 2 * Q : Q;
-    l.tok_bytes = tok_buffer_bytes(l.slots, Q);
+    l.head = window && kTensorWindow;
+    l.tok_bytes = tok_buffer_bytes(l.slots, Q, l.head);
     l.raw_bytes = raw_buffer_bytes(l.slots, Q, corr);
     l.off_state = 0;                                // 2 x 64 KiB staging
     l.off_tok = 2 * kD * kD * 4;
@@ -692,6 +714,27 @@ __device__ __forceinline__ void issue_state(const Params &p, const Work &w, floa
     bulk_load(dst, src, kD * kD * 4, bar);
 }
 
+// The checkpoint of a tensor-window item, swizzled for the tensor core: four
+// boxes of 32 columns x 128 rows through the pool's tensor map (rows of the
+// pool viewed as (slot * H + head) * 128 + v).
+__device__ __forceinline__ void issue_state_tc(const Params &p, const Work &w, float *dst,
+                                               uint64_t *bar, const CUtensorMap *tmap) {
+    const int row0 = (w.slot * p.H + w.head) * kD;
+    mbar_arrive_expect_tx(bar, kD * kD * 4);
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk)
+        tma_load_2d(dst + blk * (kD * 32), tmap, 32 * blk, row0, bar);
+}
+
+// A verify item in tensor window form: raw records, window kernel, the
+// launch's tensor map valid and at least kWindowMinT new tokens.  Its
+// checkpoint is staged swizzled.
+template <bool kWindow>
+__device__ __forceinline__ bool tensor_item(const Params &p, const unsigned char *smem, int T) {
+    return kWindow && kTensorWindow && p.tc_window != 0 && T >= kWindowMinT &&
+           (smem_u32(smem) & 1023u) == 0;
+}
+
 // Per-item duties of the producer warps, spread so that none carries two:
 // warp 3 (the fewest tokens to prepare, token u going to warp u mod 4)
 // stages the checkpoint, warp 2 copies g_bias and A_log, warp 1 waits for
@@ -702,7 +745,7 @@ constexpr int kHandoffThread = 32;
 
 template <Mode kMode, bool kBounded, bool kCorr, bool kWindow>
 __device__ void run_producer(const Params &p, unsigned char *smem, const Layout &lay,
-                             int num_tiles, int pt) {
+                             int num_tiles, int pt, const CUtensorMap *tmap) {
     using Raw = RawView<kCorr>;
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     WorkList &list = *reinterpret_cast<WorkList *>(smem + lay.off_list);
@@ -727,9 +770,13 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         // checkpoint of `cur` into consumer c's staging buffer
         if (pt == kStageThread) {
             if (use_c > 0) ok = wait_phase(&sy.empty_state[c], (use_c - 1) & 1, sy, p);
-            if (ok)
-                issue_state(p, cur, reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD,
-                            &sy.full_state[c]);
+            if (ok) {
+                float *dst = reinterpret_cast<float *>(smem + lay.off_state) + c * kD * kD;
+                if (tensor_item<kWindow>(p, smem, cur.T))
+                    issue_state_tc(p, cur, dst, &sy.full_state[c], tmap);
+                else
+                    issue_state(p, cur, dst, &sy.full_state[c]);
+            }
         }
         // raw inputs of `cur` have landed; start those of the next item
         Raw rv(smem + lay.off_raw + rb * lay.raw_bytes, lay.slots, p.Q);
@@ -752,8 +799,12 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
             sy.leave[n & 1] = *reinterpret_cast<volatile int *>(&sy.abort);
         }
         producer_sync();
-        if (sy.leave[n & 1]) return;
-        TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
+        if (sy.leave[n & 1]) {
+            cp_async_wait_all();  // no copy into shared memory outlives the thread
+            return;
+        }
+        TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q,
+                   lay.head);
         prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt);
         if (pt == kHandoffThread) {
             ItemInfo &it = sy.info[c][b];
@@ -807,6 +858,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     // the group's barrier: an mbarrier, so that its wait is bounded like the
     // others and every thread leaves on an abort
     uint32_t group_uses = 0;
+    uint32_t mma_uses = 0;  // tensor window items issued (parity of mma_done)
     auto group_sync = [&]() -> bool {
         mbar_arrive(&sy.group[c]);
         return wait_phase(&sy.group[c], group_uses++ & 1, sy, p);
@@ -817,39 +869,100 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         if (!wait_phase(&sy.full_tok[c][b], use_b & 1, sy, p)) return;
         const ItemInfo it = sy.info[c][b];
         if (it.end) return;
-        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q);
-        // the window form's coefficients, before the tile occupies registers
+        const TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q,
+                         lay.head);
+        // tensor window form (window kernels): the outputs' row products on
+        // the tensor core, from the swizzled staging buffer
+        const bool tensor = tensor_item<kWindow>(p, smem, it.T);
         const bool window = kWindow && it.T >= kWindowMinT;
+        unsigned char *stage = smem + lay.off_state + c * (kD * kD * 4);
+        // the FMA window form's coefficients, before the tile occupies registers
         if constexpr (kWindow)
-            if (window && !window_prep(tv, it.p, it.T, p.Q, ct, group_sync)) return;
-        if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
-        Tile h;
-        load_tile(h, staging, L);
-        mbar_arrive(&sy.empty_state[c]);
-        for (int u = 0; u < it.p; ++u) {
-            if constexpr (kCorr)
-                token_corr(h, tv, u, L);
+            if (window && !tensor && !window_prep(tv, it.p, it.T, p.Q, ct, group_sync)) return;
+        if (!tensor || it.p > 0) {
+            if (!wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
+            Tile h;
+            if (tensor)
+                load_tile_sw(h, stage, L);
             else
-                token_plain(h, tv, u, L);
-            if constexpr (kMode == Mode::kCommit) {
-                if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
-                    store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD),
-                               L);
+                load_tile(h, staging, L);
+            if (!tensor) mbar_arrive(&sy.empty_state[c]);
+            for (int u = 0; u < it.p; ++u) {
+                if constexpr (kCorr)
+                    token_corr(h, tv, u, L);
+                else
+                    token_plain(h, tv, u, L);
+                if constexpr (kMode == Mode::kCommit) {
+                    if (u + 1 == it.mid_len)  // align mode: the state at the block boundary
+                        store_tile(h, p.pool + ((size_t)it.mid * p.H + it.head) * (size_t)(kD * kD),
+                                   L);
+                }
+            }
+            if (it.p > 0)
+                store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
+            if (tensor) {
+                // the folded state back to the staging buffer, for the tensor core
+                store_tile_sw(h, stage, L);
+            } else {
+                if (kWindow && window) {
+                    window_outputs(h, tv, it.p, it.T, p.Q, L,
+                                   p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
+                } else if constexpr (kMode == Mode::kVerify) {
+                    for (int t = 0; t < it.T; ++t) {
+                        const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
+                        const float vp = token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
+                        if constexpr (kCorr)  // the token's delta into its correction record
+                            reinterpret_cast<float *>(corr_base(p, it.r, it.head) +
+                                                      (size_t)t * kCorrBytes)[L.row(L.j)] = vp;
+                        if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
+                    }
+                }
+                mbar_arrive(&sy.empty_tok[c][b]);
+                continue;
             }
         }
-        if (it.p > 0) store_tile(h, p.pool + ((size_t)it.dst * p.H + it.head) * (size_t)(kD * kD), L);
-        if (kWindow && window) {
-            window_outputs(h, tv, it.p, it.T, p.Q, L,
-                           p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
-        } else if constexpr (kMode == Mode::kVerify) {
-            for (int t = 0; t < it.T; ++t) {
-                const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
-                const float vp = token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
-                if constexpr (kCorr)  // the token's delta into its correction record
-                    reinterpret_cast<float *>(corr_base(p, it.r, it.head) +
-                                              (size_t)t * kCorrBytes)[L.row(L.j)] = vp;
-                if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
+        if constexpr (kWindow && kTensorWindow) {
+            // tensor window form, from here with no tile in registers
+            float vrow[kMaxQ];
+            if (!window_tc_prep(tv, it.p, it.T, p.Q, ct, vrow, group_sync)) return;
+            if (!group_sync()) return;  // the operands X in place
+            if (it.p == 0 && !wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
+            const uint32_t tmem = sy.tmem_base + 256u * (uint32_t)c;  // this consumer's columns
+            const uint32_t lanes = (uint32_t)(32 * (ct >> 5)) << 16;  // this warp's TMEM lanes
+            const uint32_t mbar_parity = mma_uses & 1u;
+            if (ct == 0) {
+                tc_fence_after();
+                window_tc_mma_hi(smem_u32(stage), smem_u32(tv.kh), tmem);
+                umma_commit(&sy.mma_hi[c]);
             }
+            // meanwhile S_lo into TMEM (the staging buffer is only read)
+            s_lo_to_tmem(stage, ct, tmem + lanes + 128u);
+            tmem_wait_st();
+            tc_fence_before();
+            // the products finish in microseconds whatever the other roles do:
+            // wait for them even after an abort (the TMEM and the staging
+            // buffer must not be reused under them)
+            if (!group_sync()) {  // S_lo in place
+                mbar_wait_bounded(&sy.mma_hi[c], mbar_parity, kWaitBudget);
+                return;
+            }
+            if (ct == 0) {
+                tc_fence_after();
+                window_tc_mma_lo(tmem + 128u, smem_u32(tv.kh), tmem + 32u);
+                umma_commit(&sy.mma_done[c]);
+            }
+            if (!mbar_wait_bounded(&sy.mma_hi[c], mbar_parity, kWaitBudget) ||
+                !mbar_wait_bounded(&sy.mma_done[c], mbar_parity, kWaitBudget)) {
+                *reinterpret_cast<volatile int *>(&sy.abort) = 1;
+                flag_error(p.err, kErrWaitTimeout);
+                return;
+            }
+            ++mma_uses;
+            mbar_arrive(&sy.empty_state[c]);  // the staging buffer is free
+            tc_fence_after();
+            window_tc_solve(tv, it.p, it.T, p.Q, ct, vrow, tmem + lanes,
+                            p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
+            tc_fence_before();  // this item's TMEM reads before the next item's writes
         }
         mbar_arrive(&sy.empty_tok[c][b]);
     }
@@ -858,12 +971,20 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
 // kWindow: items of the verify with at least kWindowMinT new tokens run them
 // in window form (raw records, no trajectory output); the others, and every
 // other kernel, token by token.
+//
+// With the tensor window form the window kernels allocate all 512 columns of
+// tensor memory (256 per consumer: D_hi in columns 0..31, D_lo in 32..63,
+// S_lo in 128..255); one CTA per SM, so the allocation never waits.
+constexpr uint32_t kTmemCols = 512;
+
 template <Mode kMode, bool kBounded, bool kCorr, bool kWindow>
-__global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, int num_tiles,
-                                                                  int fold) {
+__global__ void __launch_bounds__(kBlockThreads, 1)
+    step_kernel(const Params p, int num_tiles, int fold, const __grid_constant__ CUtensorMap tmap) {
     static_assert(!kWindow || (kMode == Mode::kVerify && !kCorr), "window form: raw verify only");
-    extern __shared__ __align__(128) unsigned char smem[];
-    const Layout lay = make_layout(p.Q, fold != 0, kCorr);
+    // the head layout's buffers (swizzled operands) need a 1024-byte aligned
+    // base; tensor_item checks it
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const Layout lay = make_layout(p.Q, fold != 0, kCorr, kWindow);
     Sync &sy = *reinterpret_cast<Sync *>(smem + lay.off_sync);
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -871,6 +992,8 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
             mbar_init(&sy.full_state[c], 1);
             mbar_init(&sy.empty_state[c], kConsumerThreads);
             mbar_init(&sy.group[c], kConsumerThreads);
+            mbar_init(&sy.mma_hi[c], 1);
+            mbar_init(&sy.mma_done[c], 1);
             for (int b = 0; b < 2; ++b) {
                 mbar_init(&sy.full_tok[c][b], 1);
                 mbar_init(&sy.empty_tok[c][b], kConsumerThreads);
@@ -879,7 +1002,12 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
         sy.abort = 0;
         fence_mbar_init();
     }
+    if constexpr (kWindow && kTensorWindow) {
+        if (tid < 32) tmem_alloc(&sy.tmem_base, kTmemCols);
+        tc_fence_before();
+    }
     __syncthreads();
+    if constexpr (kWindow && kTensorWindow) tc_fence_after();
     // let the next launch start its set-up, and wait for the previous one
     // before any global memory is touched
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -894,7 +1022,17 @@ __global__ void __launch_bounds__(kBlockThreads, 1) step_kernel(const Params p, 
     } else {
         reg_dealloc<kProducerRegs>();
         run_producer<kMode, kBounded, kCorr, kWindow>(p, smem, lay, num_tiles,
-                                                      tid - 2 * kConsumerThreads);
+                                                      tid - 2 * kConsumerThreads, &tmap);
+    }
+    if constexpr (kWindow && kTensorWindow) {
+        // every role has left (an abort included); the consumers waited for
+        // their products, so the tensor memory is idle
+        tc_fence_before();
+        __syncthreads();
+        if (tid < 32) {
+            tc_fence_after();
+            tmem_dealloc(sy.tmem_base, kTmemCols);
+        }
     }
 }
 
@@ -982,8 +1120,8 @@ int sm_count() {
 // verify without a trajectory output whose window can hold kWindowMinT
 // tokens, the kernel that runs such items in window form.
 template <kda::Mode M>
-void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const Params, int,
-                                                                         int) {
+void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const Params, int, int,
+                                                                         const CUtensorMap) {
     using kda::step_kernel;
     if constexpr (M == kda::Mode::kVerify) {
         if (!corr && !traj && window)
@@ -993,19 +1131,69 @@ void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const P
     return bounded ? step_kernel<M, true, false, false> : step_kernel<M, false, false, false>;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (the
+// library links no driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of the state pool for the tensor window form: the pool as a
+// 2-D fp32 array of S * H * 128 rows of 128, read in boxes of 32 columns x
+// 128 rows with the 128-byte swizzle.  False when it cannot be made (then
+// the window items take the FMA form).
+bool pool_tensor_map(const Params &p, CUtensorMap *map) {
+#ifndef KDA_TENSOR_WINDOW
+    (void)p, (void)map;
+    return false;  // the tensor window form is a build option
+#else
+    const long long rows = (long long)p.S * p.H * kda::kD;
+    if (rows >= 0x7fffffffLL) return false;  // row coordinates are 32-bit signed
+    const EncodeTiledFn enc = encode_tiled();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kda::kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kda::kD * 4};
+    const cuuint32_t box[2] = {32, (cuuint32_t)kda::kD};
+    const cuuint32_t elem[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p.pool, dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+#endif
+}
+
 // Launch the warp-specialized step kernel: one CTA per SM (or one per tile
 // when there are fewer tiles), the shared-memory layout sized by the window.
 template <kda::Mode M>
-kda_status launch_step(const Params &p, const kda_config *cfg, bool fold, cudaStream_t stream) {
+kda_status launch_step(const Params &p_in, const kda_config *cfg, bool fold, cudaStream_t stream) {
+    Params p = p_in;
     const long long tiles = (long long)p.B * p.H;
     const int sms = sm_count();
     if (sms <= 0) return KDA_ERR_CUDA;
     const int grid = (int)(tiles < (long long)sms ? tiles : (long long)sms);
     const bool bounded = cfg->use_lower_bound != 0;
     const bool corr = cfg->record_format == KDA_RECORDS_CORRECTION;
-    const kda::Layout lay = kda::make_layout(p.Q, fold, corr);
-    void (*kern)(const Params, int, int) =
-        step_kernel_for<M>(bounded, corr, p.traj != nullptr, p.Q >= kda::kWindowMinT);
+    const bool window =
+        M == kda::Mode::kVerify && !corr && p.traj == nullptr && p.Q >= kda::kWindowMinT;
+    const kda::Layout lay = kda::make_layout(p.Q, fold, corr, window);
+    void (*kern)(const Params, int, int, const CUtensorMap) =
+        step_kernel_for<M>(bounded, corr, p.traj != nullptr, window);
+    CUtensorMap map;
+    memset(&map, 0, sizeof(map));
+    p.tc_window = window && pool_tensor_map(p, &map) ? 1 : 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total) !=
             cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -1024,7 +1212,7 @@ kda_status launch_step(const Params &p, const kda_config *cfg, bool fold, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, kern, p, (int)tiles, fold ? 1 : 0) != cudaSuccess)
+    if (cudaLaunchKernelEx(&lc, kern, p, (int)tiles, fold ? 1 : 0, map) != cudaSuccess)
         return KDA_ERR_CUDA;
     return finish_launch();
 }
