@@ -629,10 +629,11 @@ __device__ __forceinline__ void fetch_raw(const Params &p, const Work &w, RawVie
 // (u mod 4), four channels per lane, the norms summed across the warp; every
 // token is computed the same way however many tokens the item has.  The
 // verify also writes the new tokens' records (raw: k, v, g_raw, beta_raw;
-// correction: k and g_raw, the consumer adds the delta).
+// correction: k and g_raw, the consumer adds the delta).  An item in window
+// form (window_item) needs no k^ . q^.
 template <Mode kMode, bool kBounded, bool kCorr>
 __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawView<kCorr> rv,
-                                          const TokView &tv, int pt) {
+                                          const TokView &tv, int pt, bool window_item) {
     const int lane = pt & 31, warp = pt >> 5;
     const float a = expf(*rv.a_log);
     const float4 bias = *reinterpret_cast<const float4 *>(rv.bias + 4 * lane);
@@ -676,19 +677,21 @@ __device__ __forceinline__ void prep_item(const Params &p, const Work &w, RawVie
             sq = __fmaf_rn(q.y, q.y, sq);
             sq = __fmaf_rn(q.z, q.z, sq);
             sq = __fmaf_rn(q.w, q.w, sq);
-            float skq = __fmul_rn(k.x, q.x);
-            skq = __fmaf_rn(k.y, q.y, skq);
-            skq = __fmaf_rn(k.z, q.z, skq);
-            skq = __fmaf_rn(k.w, q.w, skq);
             const float iq = inv_l2(warp_allsum(sq));
-            const float dkq = warp_allsum(skq);
             *reinterpret_cast<float4 *>(tv.qh + t * kD + 4 * lane) =
                 make_float4(__fmul_rn(__fmul_rn(q.x, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.y, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.z, iq), p.scale),
                             __fmul_rn(__fmul_rn(q.w, iq), p.scale));
-            // k^ . q^ from the raw dot product and the two norms
-            if (lane == 0) tv.kq[t] = __fmul_rn(__fmul_rn(__fmul_rn(dkq, ik), iq), p.scale);
+            if (!window_item) {
+                // k^ . q^ from the raw dot product and the two norms
+                float skq = __fmul_rn(k.x, q.x);
+                skq = __fmaf_rn(k.y, q.y, skq);
+                skq = __fmaf_rn(k.z, q.z, skq);
+                skq = __fmaf_rn(k.w, q.w, skq);
+                const float dkq = warp_allsum(skq);
+                if (lane == 0) tv.kq[t] = __fmul_rn(__fmul_rn(__fmul_rn(dkq, ik), iq), p.scale);
+            }
             if constexpr (kCorr) {
                 unsigned char *tok = corr_base(p, w.r, w.head) + (size_t)t * kCorrBytes;
                 reinterpret_cast<uint2 *>(tok + kCorrK)[lane] = kb;
@@ -805,7 +808,7 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         }
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q,
                    lay.head);
-        prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt);
+        prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt, kWindow && cur.T >= kWindowMinT);
         if (pt == kHandoffThread) {
             ItemInfo &it = sy.info[c][b];
             it.head = cur.head;
