@@ -229,11 +229,12 @@ __device__ __forceinline__ void flag_error(int *err, int bits) {
 // coefficients of the window (Q x Q each, row t, column s).
 //
 // Two layouts.  In the tail layout the vectors start at the buffer and the
-// small arrays (beta, kq, pa, pb) follow them.  In the head layout (raw
-// records, windows of 5 or more tokens) the small arrays come first and the
-// vectors start kTokHead bytes in, on a 1024-byte boundary, with at least
-// kXBytes of them: a verify item in tensor window form (window_tc_prep)
-// overwrites those bytes with its swizzled tensor-core operands.
+// small arrays (beta, kq, pa, pb) follow them.  In the head layout (the
+// window kernels of the tensor window form) the small arrays come first and
+// the vectors start kTokHead bytes in, on a 1024-byte boundary, with at
+// least kXBytes of them: a verify item in tensor window form
+// (window_tc_prep) overwrites those bytes with its swizzled tensor-core
+// operands.
 constexpr int kTokHead = 1024;
 constexpr int kXBytes = 2 * 16 * kD * 4;  // X_hi and X_lo: 16 vectors of 128 fp32 each
 constexpr int kXBlock = 32 * 128;          // one 32-column block of the 32 operand rows

@@ -231,9 +231,9 @@ constexpr int kWindowMinT = 5;
 // a build option, off by default: measured on the window-8 workload
 // (256 requests x 16 heads) its verify took 111 us against 88 us for the
 // FMA window form.  Per item, each of its 32 tcgen05.mma of 128 x 32 x 8
-// takes about 130 cycles to issue, the staging buffer stays held until the
-// products finish, and the coefficients and the solve, unchanged, dominate
-// the consumer's chain.
+// takes about 80 to 130 cycles to issue, the staging buffer stays held until
+// the products finish, and the coefficients and the solve, unchanged,
+// dominate the consumer's chain.
 #ifdef KDA_TENSOR_WINDOW
 constexpr bool kTensorWindow = true;
 #else
@@ -861,7 +861,7 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
     // the group's barrier: an mbarrier, so that its wait is bounded like the
     // others and every thread leaves on an abort
     uint32_t group_uses = 0;
-    uint32_t mma_uses = 0;  // tensor window items issued (parity of mma_done)
+    uint32_t mma_uses = 0;  // tensor window items done (parity of mma_hi and mma_done)
     auto group_sync = [&]() -> bool {
         mbar_arrive(&sy.group[c]);
         return wait_phase(&sy.group[c], group_uses++ & 1, sy, p);
