@@ -532,11 +532,10 @@ struct Cursor {
 template <Mode kMode>
 __device__ __forceinline__ Work next_work(const Params &p, WorkList &list, Cursor &c,
                                           int num_tiles, int pt) {
-    const int K = num_candidates(list, num_tiles, p.H);
     Work w;
     w.tile = -1;
     while (c.idx >= c.count) {
-        if (c.next_k >= K) return w;
+        if (c.next_k >= num_candidates(list, num_tiles, p.H)) return w;
         c.count = plan_round<kMode>(p, list, c.next_k, num_tiles, pt);
         c.next_k += kPlanSize;
         c.idx = 0;
