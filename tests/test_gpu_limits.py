@@ -66,3 +66,44 @@ def test_max_heads_verify_and_commit(Q, T, bounded):
     assert_out_close(out[:, hs], res.out)
     for i in range(len(heads)):
         assert_state_close(pool[1, heads[i]].double().cpu().numpy(), cache.written[(1, i)])
+
+
+def test_deferred_chain_beyond_the_balanced_plan_rows():
+    """4500 rows, more than the 4096 the commits' balanced plan takes: the
+    deferred commits fall back to the strided plan, where each row's pending
+    count is written by the CTA that plans the row's head 0.  Two deferred
+    steps (a fold in the second verify), checked on sampled rows, the last
+    ones among them, against the oracle: outputs, stored states and pending
+    counts."""
+    from linear_attention_speculative_kda_gb300 import workloads as W
+    from tests.helpers import DeviceRun, oracle_cache, oracle_layer, oracle_step
+
+    B = 4500
+    lens = np.random.default_rng(5).integers(0, 3, size=B).tolist()
+    wl = W.custom(B=B, H=2, Q=2, lens=lens, S=B + 2, R=B + 4, deferred=True, steps=2,
+                  seed=77, eager_prob=0.3)
+    g = DeviceRun(wl, sentinel=False)
+    g.verify(0, pending=True)
+    g.commit(0, deferred=True)
+    g.verify(1, pending=True)
+    g.commit(1, deferred=True)
+    torch.cuda.synchronize()
+    assert int(g.err.item()) == 0
+    rng = np.random.default_rng(9)
+    rows = sorted(set(rng.choice(B, size=20, replace=False).tolist()) | {4095, 4096, 4097, B - 1})
+    layer, cache = oracle_layer(wl), oracle_cache(wl)
+    s1, s2 = oracle_step(wl, 0), oracle_step(wl, 1)
+    O.verify(layer, cache, s1, pending=True, rows=rows)
+    O.commit(layer, cache, s1, wl.steps[0].num_accepted.numpy(), deferred=True,
+             eager=wl.steps[0].eager.numpy(), rows=rows)
+    r2 = O.verify(layer, cache, s2, pending=True, rows=rows)
+    O.commit(layer, cache, s2, wl.steps[1].num_accepted.numpy(), deferred=True,
+             eager=wl.steps[1].eager.numpy(), rows=rows)
+    assert_out_close(g.out, r2.out)
+    pool = g.pool.cpu()
+    for (slot, h), ref in cache.written.items():
+        assert_state_close(pool[slot, h].double().numpy(), ref)
+    pending = g.pending.cpu().numpy()
+    rr = wl.record_rows.numpy()
+    for b in rows:
+        assert pending[rr[b]] == cache.pending[rr[b]], b
