@@ -1133,6 +1133,7 @@ void (*step_kernel_for(bool bounded, bool corr, bool traj, bool window))(const P
     return bounded ? step_kernel<M, true, false, false> : step_kernel<M, false, false, false>;
 }
 
+#ifdef KDA_TENSOR_WINDOW
 // The driver's tensor-map encoder, looked up once through the runtime (the
 // library links no driver library).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1152,6 +1153,7 @@ EncodeTiledFn encode_tiled() {
     }();
     return fn;
 }
+#endif
 
 // Tensor map of the state pool for the tensor window form: the pool as a
 // 2-D fp32 array of S * H * 128 rows of 128, read in boxes of 32 columns x
