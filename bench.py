@@ -672,13 +672,14 @@ def l2_note(pool_bytes: int) -> str:
 
 
 def conv_compact_bytes(wl: W.Workload, conv_dim: int, hist: int, elem_bytes: int, acc) -> int:
-    """Algorithmic bytes of one conv compaction: every committed row (slot > 0,
-    n > 0) reads its window of conv_dim x history elements and writes it
-    back at column 0."""
+    """Algorithmic bytes of one conv compaction: every row that moves its
+    windows (slot > 0, n > 1; with n = 1 each window is already at column 0)
+    reads its window of conv_dim x history elements and writes it back at
+    column 0."""
     lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
     slots = wl.state_indices.tolist()
     rows = sum(1 for b in range(wl.spec.B)
-               if slots[b] > 0 and min(max(int(acc[b]), 0), lens[b], wl.spec.Q) > 0)
+               if slots[b] > 0 and min(max(int(acc[b]), 0), lens[b], wl.spec.Q) > 1)
     return 2 * rows * conv_dim * hist * elem_bytes
 
 

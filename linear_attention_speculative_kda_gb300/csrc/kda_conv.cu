@@ -5,12 +5,13 @@
 // moves to column 0.  Every element a thread writes it has read itself (or,
 // in the staged form, the CTA has read it into shared memory) before any
 // write, so a window that overlaps its destination is moved correctly.
-// Three forms, chosen on the host from the strides:
+// A row with n = 1 keeps every window where it is and is skipped.  Three
+// forms, chosen on the host from the strides:
 //  - channel-major and dense (column stride 1, channel stride = width): a
-//    CTA stages a 16-byte-aligned run of whole channels in shared memory with
-//    16-byte loads, moves each channel's window there and writes the run back
-//    with 16-byte stores (the bytes of a channel are not 16-byte aligned on
-//    their own, e.g. 6 bf16 columns);
+//    CTA loads a 16-byte-aligned run of whole channels (up to 24 KiB) into
+//    shared memory with one TMA bulk copy, moves each channel's window there
+//    and writes the run back with one bulk copy (the bytes of a channel are
+//    not 16-byte aligned on their own, e.g. 6 bf16 columns);
 //  - column-major (channel stride 1) with 16-byte rows: a thread moves 16
 //    bytes of channels through the window's columns;
 //  - anything else: a thread moves one channel, element by element.
@@ -22,6 +23,7 @@
 
 #include "../../include/kda.h"
 #include "kda_align.cuh"
+#include "kda_async.cuh"
 
 namespace kda_conv {
 
@@ -36,7 +38,8 @@ struct Params {
     int *err;
 };
 
-// Row checks shared by the three forms: the commit count n, or 0 to skip.
+// Row checks shared by the three forms: the commit count n, or 0 to skip
+// (n = 1 moves the window at column 0 onto itself).
 __device__ __forceinline__ int row_count(const Params &p, int b) {
     const int len = p.cu[b + 1] - p.cu[b];
     const int slot = p.slots[b];
@@ -50,7 +53,7 @@ __device__ __forceinline__ int row_count(const Params &p, int b) {
         return 0;
     }
     const int n = min(max(p.acc[b], 0), min(len, p.Q));
-    return slot > 0 ? n : 0;
+    return slot > 0 && n > 1 ? n : 0;
 }
 
 // Any strides: one thread per channel, element by element.
@@ -73,135 +76,90 @@ __global__ void __launch_bounds__(kThreads) compact_kernel(const Params p) {
     }
 }
 
-constexpr int kStageBytes = 16384;                  // shared-memory run of the staged form
-constexpr int kStageVecs = kStageBytes / 16 / kThreads;  // 16-byte loads per thread
+// Channel-major, dense, in bulk: CTA (x, row) moves run x of the row's slot,
+// `run` whole channels (a multiple of the channels whose bytes make 16-byte
+// units, at most kBulkBytes), with one bulk copy each way: thread 0 loads
+// the run into shared memory on an mbarrier, every thread moves its
+// channels' windows there, and thread 0 stores the run back and waits until
+// the store has read shared memory before the stage is reused.
+constexpr int kBulkBytes = 24576;
+constexpr long long kBulkWaitBudget = 4000000000LL;  // clock cycles (about 2 s)
 
-// Channel-major, dense: run r of a slot covers channels [r*run, (r+1)*run),
-// `run` a multiple of the channels whose bytes make 16-byte units.
+// One bulk copy shared -> global (a multiple of 16 bytes, both addresses
+// 16-byte aligned) in this thread's bulk group; bulk_commit closes the
+// group and bulk_wait_read waits until every committed bulk store of the
+// thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_store(void *dst_gmem, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst_gmem),
+                 "r"(kda::smem_u32(src_smem)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kThreads) staged_kernel(const Params p, int run) {
-    __shared__ __align__(16) unsigned char stage[kStageBytes];
+__global__ void __launch_bounds__(kThreads) bulk_kernel(const Params p, int run) {
+    __shared__ __align__(128) unsigned char stage[kBulkBytes];
+    __shared__ __align__(8) uint64_t bar;
     const int W = (int)p.stride_dim;  // = width
+    if (threadIdx.x == 0) {
+        kda::mbar_init(&bar, 1);
+        kda::fence_mbar_init();
+    }
+    __syncthreads();
+    uint32_t phase = 0;
     for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
         const int n = row_count(p, b);
         if (n <= 0) continue;  // uniform over the CTA
-        unsigned char *slot_base =
-            p.conv + (long long)p.slots[b] * p.stride_slot * (long long)sizeof(T);
-        for (int c0 = blockIdx.x * run; c0 < p.C; c0 += gridDim.x * run) {
-            const int chans = min(run, p.C - c0);
-            const int vecs = chans * W * (int)sizeof(T) / 16;
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                slot_base + (long long)c0 * W * (long long)sizeof(T));
-            uint4 *sv = reinterpret_cast<uint4 *>(stage);
-            uint4 r[kStageVecs];  // all loads in flight before the first store
-#pragma unroll
-            for (int j = 0; j < kStageVecs; ++j) {
-                const int i = threadIdx.x + j * kThreads;
-                if (i < vecs) r[j] = src[i];
-            }
-#pragma unroll
-            for (int j = 0; j < kStageVecs; ++j) {
-                const int i = threadIdx.x + j * kThreads;
-                if (i < vecs) sv[i] = r[j];
-            }
-            __syncthreads();
-            T *se = reinterpret_cast<T *>(stage);
-            for (int d = threadIdx.x; d < chans; d += kThreads) {
-                T w[KDA_MAX_CONV_HISTORY];
-#pragma unroll
-                for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
-                    if (h < p.hist) w[h] = se[d * W + n - 1 + h];
-#pragma unroll
-                for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
-                    if (h < p.hist) se[d * W + h] = w[h];
-            }
-            __syncthreads();
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                slot_base + (long long)c0 * W * (long long)sizeof(T));
-#pragma unroll
-            for (int j = 0; j < kStageVecs; ++j) {
-                const int i = threadIdx.x + j * kThreads;
-                if (i < vecs) r[j] = sv[i];
-            }
-#pragma unroll
-            for (int j = 0; j < kStageVecs; ++j) {
-                const int i = threadIdx.x + j * kThreads;
-                if (i < vecs) dst[i] = r[j];
-            }
-            __syncthreads();  // the stage is reused by the next run
+        const int c0 = blockIdx.x * run;
+        if (c0 >= p.C) continue;
+        const int chans = min(run, p.C - c0);
+        const uint32_t bytes = (uint32_t)(chans * W * (int)sizeof(T));
+        unsigned char *src = p.conv + ((long long)p.slots[b] * p.stride_slot +
+                                       (long long)c0 * W) * (long long)sizeof(T);
+        if (threadIdx.x == 0) {
+            kda::mbar_arrive_expect_tx(&bar, bytes);
+            kda::bulk_load(stage, src, bytes, &bar);
         }
-    }
-}
-
-// Channel-major, dense, small units: a unit is the fewest whole channels
-// whose bytes make 16-byte pieces (at most 4 channels, 64 bytes).  A thread
-// loads kUnits units with 16-byte loads into its own slice of shared memory,
-// moves each channel's window there, and stores the units back: no barrier,
-// and every load is in flight before the first store.  Piece v of unit k of
-// thread t sits at 16 * ((4k + v) * kThreads + t), so a warp's 16-byte
-// accesses fall on distinct banks.
-constexpr int kUnitMaxBytes = 64;
-
-template <typename T, int kUnits>
-__global__ void __launch_bounds__(kThreads) unit_kernel(const Params p, int unit_chans) {
-    __shared__ __align__(16) unsigned char stage[kThreads * kUnits * kUnitMaxBytes];
-    const int W = (int)p.stride_dim;  // = width
-    const int unit_bytes = unit_chans * W * (int)sizeof(T);
-    const int uv = unit_bytes / 16;    // 16-byte pieces per unit, <= 4
-    const int units = p.C / unit_chans;
-    constexpr int kPieces = kUnitMaxBytes / 16;
-    for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-        const int n = row_count(p, b);
-        if (n <= 0) continue;
-        unsigned char *slot_base =
-            p.conv + (long long)p.slots[b] * p.stride_slot * (long long)sizeof(T);
-        for (int u0 = blockIdx.x * kThreads * kUnits + threadIdx.x; u0 < units;
-             u0 += gridDim.x * kThreads * kUnits) {
-            uint4 r[kUnits][kUnitMaxBytes / 16];
-#pragma unroll
-            for (int k = 0; k < kUnits; ++k) {
-                const int u = u0 + k * kThreads;
-                const uint4 *src = reinterpret_cast<const uint4 *>(slot_base + (long long)u * unit_bytes);
-#pragma unroll
-                for (int v = 0; v < kUnitMaxBytes / 16; ++v)
-                    if (u < units && v < uv) r[k][v] = src[v];
+        const bool landed = kda::mbar_wait_bounded(&bar, phase, kBulkWaitBudget);
+        if (__syncthreads_or(!landed)) {
+            // the load did not land in time: report it, give it one more
+            // bounded wait so that no copy into shared memory outlives the
+            // CTA, and leave with nothing written
+            if (threadIdx.x == 0) {
+                if (p.err != nullptr) atomicOr(p.err, KDA_ERR_WAIT_TIMEOUT);
+                kda::mbar_wait_bounded(&bar, phase, kBulkWaitBudget);
+                bulk_wait_read();
             }
-            constexpr int kPer = 16 / (int)sizeof(T);  // elements per piece
-#pragma unroll
-            for (int k = 0; k < kUnits; ++k) {
-                uint4 *sv = reinterpret_cast<uint4 *>(stage) + (k * kPieces) * kThreads + threadIdx.x;
-#pragma unroll
-                for (int v = 0; v < kPieces; ++v)
-                    if (v < uv) sv[v * kThreads] = r[k][v];
-                // element e of the unit: piece e / kPer, slot e % kPer
-                T *se = reinterpret_cast<T *>(sv);
-                for (int c = 0; c < unit_chans; ++c) {
-                    T w[4];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int e = c * W + n - 1 + h;
-                        if (h < p.hist) w[h] = se[(e / kPer) * kThreads * kPer + e % kPer];
-                    }
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        const int e = c * W + h;
-                        if (h < p.hist) se[(e / kPer) * kThreads * kPer + e % kPer] = w[h];
-                    }
-                }
-#pragma unroll
-                for (int v = 0; v < kPieces; ++v)
-                    if (v < uv) r[k][v] = sv[v * kThreads];
-            }
-#pragma unroll
-            for (int k = 0; k < kUnits; ++k) {
-                const int u = u0 + k * kThreads;
-                uint4 *dst = reinterpret_cast<uint4 *>(slot_base + (long long)u * unit_bytes);
-#pragma unroll
-                for (int v = 0; v < kUnitMaxBytes / 16; ++v)
-                    if (u < units && v < uv) dst[v] = r[k][v];
-            }
+            return;
         }
+        phase ^= 1u;
+        T *se = reinterpret_cast<T *>(stage);
+        for (int d = threadIdx.x; d < chans; d += kThreads) {
+            T w[KDA_MAX_CONV_HISTORY];
+#pragma unroll
+            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
+                if (h < p.hist) w[h] = se[d * W + n - 1 + h];
+#pragma unroll
+            for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
+                if (h < p.hist) se[d * W + h] = w[h];
+        }
+        kda::fence_proxy_async_smem();  // the bulk store reads through the async proxy
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            bulk_store(src, stage, bytes);
+            bulk_commit();
+            bulk_wait_read();
+        }
+        __syncthreads();  // the stage is free for the next row
     }
+    if (threadIdx.x == 0) bulk_wait_read();
 }
 
 // Column-major with 16-byte rows: a thread moves kVec 16-byte pieces of
@@ -377,23 +335,13 @@ kda_status kda_conv_compact(const kda_conv_config *cc, void *conv_state,
     long long unit = 1;
     while ((unit * chan_bytes) % 16 != 0) ++unit;
     if (slots16 && cc->stride_col == 1 && cc->stride_dim == cc->width &&
-        cc->conv_dim % unit == 0 && unit <= 4 && unit * chan_bytes <= kUnitMaxBytes &&
-        p.hist <= 4) {
-        constexpr int kUnits = 2;
-        const int units = (int)(cc->conv_dim / unit);
-        const dim3 grid((units + kThreads * kUnits - 1) / (kThreads * kUnits), rows);
-        if (cc->elem_bytes == 2)
-            unit_kernel<uint16_t, kUnits><<<grid, kThreads, 0, st>>>(p, (int)unit);
-        else
-            unit_kernel<uint32_t, kUnits><<<grid, kThreads, 0, st>>>(p, (int)unit);
-    } else if (slots16 && cc->stride_col == 1 && cc->stride_dim == cc->width &&
-               cc->conv_dim % unit == 0 && unit * chan_bytes <= kStageBytes) {
-        const int run = (int)(unit * (kStageBytes / (unit * chan_bytes)));
+        cc->conv_dim % unit == 0 && unit * chan_bytes <= kBulkBytes) {
+        const int run = (int)(unit * (kBulkBytes / (unit * chan_bytes)));
         const dim3 grid((cc->conv_dim + run - 1) / run, rows);
         if (cc->elem_bytes == 2)
-            staged_kernel<uint16_t><<<grid, kThreads, 0, st>>>(p, run);
+            bulk_kernel<uint16_t><<<grid, kThreads, 0, st>>>(p, run);
         else
-            staged_kernel<uint32_t><<<grid, kThreads, 0, st>>>(p, run);
+            bulk_kernel<uint32_t><<<grid, kThreads, 0, st>>>(p, run);
     } else if (slots16 && cc->stride_dim == 1 && ((long long)cc->conv_dim * eb) % 16 == 0 &&
                (cc->stride_col * eb) % 16 == 0) {
         const int vecs = (int)((long long)cc->conv_dim * eb / 16);

@@ -225,10 +225,12 @@ def test_code_text_strips_comments():
     assert bench.code_text(src) == "a = 1; b = 2;"
 
 
-def test_conv_compact_bytes_counts_committed_rows():
+def test_conv_compact_bytes_counts_rows_that_move():
     wl = W.custom(B=6, H=2, Q=4, lens=[4, 0, 3, 4, 2, 4], S=10, seed=8,
                   slots=[1, 2, 3, 0, 5, 6])
-    acc = [2, 3, 0, 4, 9, -1]  # committed: rows 0 (n 2) and 4 (n clamped to 2)
+    # moved: rows 0 (n 2) and 4 (n clamped to 2); row 5 (n 1) leaves its
+    # windows where they are
+    acc = [2, 3, 0, 4, 9, 1]
     assert bench.conv_compact_bytes(wl, 768, 3, 2, acc) == 2 * 2 * 768 * 3 * 2
 
 
