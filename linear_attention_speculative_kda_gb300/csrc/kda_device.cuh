@@ -476,8 +476,10 @@ __device__ __forceinline__ void token_corr(Tile &h, const TokView &tv, int slot,
 // One token with its output o = S' q^ (S' the state after the token) to
 // out_row (bf16), from the decayed state D = S diag(e) in one pass:
 // S' q^ = D q^ + v' (k^ . q^), so u = D k^ and D q^ share the pass and the
-// reduction.  The state update is the one token_plain does (same bits).
-// Returns the lane's v' (of row L.row(L.j)).
+// reduction.  The state update is the one token_plain does (same bits);
+// kUpdate false leaves it out (a verify's last new token, when no state
+// after it is stored).  Returns the lane's v' (of row L.row(L.j)).
+template <bool kUpdate>
 __device__ __forceinline__ float token_out(Tile &h, const TokView &tv, int slot, int qslot,
                                            const Lane &L, __nv_bfloat16 *out_row) {
     decay(h, tv.e + slot * kD, L);
@@ -488,7 +490,7 @@ __device__ __forceinline__ float token_out(Tile &h, const TokView &tv, int slot,
     const float vr = tv.v[slot * kD + L.row(L.j)];
     const float vp = __fmul_rn(tv.beta[slot], __fsub_rn(vr, u));
     out_row[L.row(L.j)] = __float2bfloat16_rn(__fmaf_rn(vp, tv.kq[qslot], dq));
-    delta_update_vp(h, tv, slot, vp, L);
+    if constexpr (kUpdate) delta_update_vp(h, tv, slot, vp, L);
     return vp;
 }
 

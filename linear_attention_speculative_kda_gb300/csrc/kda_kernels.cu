@@ -910,13 +910,26 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
                     window_outputs(h, tv, it.p, it.T, p.Q, L,
                                    p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
                 } else if constexpr (kMode == Mode::kVerify) {
-                    for (int t = 0; t < it.T; ++t) {
-                        const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
-                        const float vp = token_out(h, tv, it.p + t, t, L, p.out + tok * kD);
+                    // the state after the last new token is stored only as a
+                    // trajectory output: without one, that token's update is
+                    // left out (its output does not depend on it).  Not in
+                    // the window kernels, where the second copy of the token
+                    // code spills registers.
+                    const int updated = (kWindow || p.traj != nullptr) ? it.T : it.T - 1;
+                    auto record_delta = [&](int t, float vp) {
                         if constexpr (kCorr)  // the token's delta into its correction record
                             reinterpret_cast<float *>(corr_base(p, it.r, it.head) +
                                                       (size_t)t * kCorrBytes)[L.row(L.j)] = vp;
+                    };
+                    int t = 0;
+                    for (; t < updated; ++t) {
+                        const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
+                        record_delta(t, token_out<true>(h, tv, it.p + t, t, L, p.out + tok * kD));
                         if (p.traj != nullptr) store_tile(h, p.traj + tok * (size_t)(kD * kD), L);
+                    }
+                    if (t < it.T) {
+                        const size_t tok = (size_t)(it.bos + t) * p.H + it.head;
+                        record_delta(t, token_out<false>(h, tv, it.p + t, t, L, p.out + tok * kD));
                     }
                 }
                 mbar_arrive(&sy.empty_tok[c][b]);
