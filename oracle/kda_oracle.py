@@ -32,6 +32,11 @@ the pages define around it, each function citing the passage it follows:
   to the block that holds that token, and, when the step crosses a block
   boundary before its last token, the state at the boundary goes to the
   block that ends there; the conv windows follow the same two blocks.
+* ``record_state_blocks`` -- ``_record_state_block_kernel`` of recoverssm.py:
+  after an align-mode commit, each committed request's running state column
+  points at the block holding its last committed token (the final block of
+  ``commit_align`` when its sampled count is the commit count n) and its
+  accepted count is reset to 1.
 * ``conv_compact`` -- ``_compact_conv_state_kernel`` of recoverssm.py in its
   non-align form: after the verify a row's conv state holds
   ``[history[1:], x_0 .. x_{Q-1}]``; once n tokens are accepted the window
@@ -277,7 +282,7 @@ class Cache:
 @dataclass
 class RowIssue:
     row: int
-    reason: str  # "length", "slot", "record", "pending"
+    reason: str  # "length", "slot", "record", "pending", "block"
 
 
 @dataclass
@@ -684,6 +689,44 @@ def conv_compact_align(conv, cu_seqlens, state_indices, num_accepted, window: in
             out[plan.boundary, :, 0:hist] = bnd
         out[plan.final, :, 0:hist] = fin
     return out, issues
+
+
+def record_state_blocks(idx_mapping, num_sampled, num_computed, state_column, num_accepted,
+                        block_size: int, block_table_width: int, *, num_rows=None,
+                        request_indices=None):
+    """Align-mode bookkeeping after a commit (recoverssm.py,
+    ``_record_state_block_kernel`` and ``record_state_blocks``): each spec
+    row's request q (``request_indices[i]``, or i) has a slot s =
+    ``idx_mapping[q]`` in the running arrays; s < 0 means nothing to record.
+    Its last committed token sits at position max(num_computed[q] +
+    num_sampled[q] - 1, 0); ``state_column[s]`` becomes the block-table
+    column holding it (the last column when it runs past the table) and
+    ``num_accepted[s]`` becomes 1.  Rows whose q lies outside the request
+    arrays ("block") or whose s lies outside the running arrays ("slot")
+    are skipped (this build's reading; the page checks neither).  Returns
+    (state_column, num_accepted, list of RowIssue) as new arrays."""
+    col = np.array(state_column, dtype=np.int64, copy=True)
+    acc = np.array(num_accepted, dtype=np.int64, copy=True)
+    if num_rows is not None:
+        n_rows = num_rows
+    else:
+        n_rows = len(idx_mapping) if request_indices is None else len(request_indices)
+    issues = []
+    for i in range(n_rows):
+        q = i if request_indices is None else int(request_indices[i])
+        if q < 0 or q >= len(idx_mapping):
+            issues.append(RowIssue(i, "block"))
+            continue
+        s = int(idx_mapping[q])
+        if s < 0:
+            continue
+        if s >= len(col):
+            issues.append(RowIssue(i, "slot"))
+            continue
+        last = max(int(num_computed[q]) + int(num_sampled[q]) - 1, 0)
+        col[s] = min(last // block_size, block_table_width - 1)
+        acc[s] = 1
+    return col, acc, issues
 
 
 def default_threads() -> int:

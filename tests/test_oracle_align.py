@@ -222,3 +222,90 @@ def test_deferred_align_then_flush_equals_the_eager_align_commit():
     for s in range(wl.spec.S):
         for h in range(wl.spec.H):
             assert np.array_equal(eager_cache.state(s, h), deferred_cache.state(s, h)), (s, h)
+
+
+# --- record_state_blocks: the running state column after an align commit ---
+
+def _column_of(position, block_size, width):
+    """Block-table column holding a token position, by walking the block
+    ranges (no division), the last column when it runs past the table."""
+    j = 0
+    while position >= (j + 1) * block_size:
+        j += 1
+    return min(j, width - 1)
+
+
+def test_record_state_blocks_column_by_walk():
+    rng = np.random.default_rng(11)
+    R, S, bs, width = 40, 50, 16, 6
+    idx = rng.permutation(S)[:R].astype(np.int64)
+    idx[rng.random(R) < 0.2] = -1                       # requests without a running slot
+    nc = rng.integers(0, 120, size=R)
+    ns = rng.integers(0, 9, size=R)
+    col0 = rng.integers(0, 99, size=S)
+    acc0 = rng.integers(2, 9, size=S)
+    col, acc, issues = O.record_state_blocks(idx, ns, nc, col0, acc0, bs, width)
+    assert issues == []
+    touched = set()
+    for q in range(R):
+        s = int(idx[q])
+        if s < 0:
+            continue
+        touched.add(s)
+        assert col[s] == _column_of(max(nc[q] + ns[q] - 1, 0), bs, width)
+        assert acc[s] == 1
+    for s in range(S):
+        if s not in touched:
+            assert col[s] == col0[s] and acc[s] == acc0[s]
+
+
+def test_record_state_blocks_points_at_the_commit_final_block():
+    """With the sampled count equal to the commit count n, the recorded
+    column holds the block the align commit wrote the final state to."""
+    rng = np.random.default_rng(12)
+    bs, width, R = 8, 5, 60
+    table = np.arange(1, R * width + 1).reshape(R, width)   # distinct block ids
+    nc = rng.integers(0, 45, size=R)
+    n = rng.integers(1, 9, size=R)
+    idx = np.arange(R)
+    col, _, issues = O.record_state_blocks(idx, n, nc, np.zeros(R, np.int64),
+                                           np.zeros(R, np.int64), bs, width)
+    assert issues == []
+    for q in range(R):
+        plan = O.align_plan(int(n[q]), int(nc[q]), table[q], bs)
+        if plan is None:       # the boundary block lies past the table
+            continue
+        assert table[q][col[q]] == plan.final
+
+
+def test_record_state_blocks_hand_cases():
+    # block_size 16, width 4; per request (slot, num_computed, num_sampled):
+    #   q0: slot 2, 30 + 3 - 1 = 32  -> column 2
+    #   q1: slot -1                   -> nothing
+    #   q2: slot 0, max(0 + 0 - 1, 0) = 0 -> column 0
+    #   q3: slot 5, 60 + 10 - 1 = 69 -> column 4, clamped to 3
+    #   q4: slot 3, 15 + 1 - 1 = 15  -> column 0 (last position of block 0)
+    #   q5: slot 4, 16 + 1 - 1 = 16  -> column 1 (first position of block 1)
+    idx = [2, -1, 0, 5, 3, 4]
+    nc = [30, 7, 0, 60, 15, 16]
+    ns = [3, 2, 0, 10, 1, 1]
+    col, acc, issues = O.record_state_blocks(idx, ns, nc, [9] * 6, [7] * 6, 16, 4)
+    assert issues == []
+    assert col.tolist() == [0, 9, 2, 0, 1, 3]
+    assert acc.tolist() == [1, 7, 1, 1, 1, 1]
+    # spec rows through request_indices: only requests 3 and 0
+    col, acc, _ = O.record_state_blocks(idx, ns, nc, [9] * 6, [7] * 6, 16, 4,
+                                        request_indices=[3, 0])
+    assert col.tolist() == [9, 9, 2, 9, 9, 3]
+    assert acc.tolist() == [7, 7, 1, 7, 7, 1]
+
+
+def test_record_state_blocks_skips_and_reports():
+    idx = [0, 7, 1]          # request 1's slot 7 is past the 4 running slots
+    col, acc, issues = O.record_state_blocks(idx, [1, 1, 1], [0, 0, 40], [5] * 4, [5] * 4, 16, 8,
+                                             request_indices=[0, 3, 1, 2])
+    # row 1 names request 3 (outside the 3 requests): "block"; row 2 -> request
+    # 1 -> slot 7: "slot"; rows 0 and 3 record columns 0 and 2
+    assert [(i.row, i.reason) for i in issues] == [(1, "block"), (2, "slot")]
+    assert col.tolist() == [0, 2, 5, 5]
+    assert acc.tolist() == [1, 1, 5, 5]
