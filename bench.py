@@ -761,6 +761,47 @@ def align_commit_bytes(wl: W.Workload, table, num_computed, block_size: int, acc
     return total * wl.spec.H
 
 
+def record_blocks_bytes(idx_mapping) -> int:
+    """Algorithmic bytes of one kda_record_state_blocks launch with one spec
+    row per request: every row reads its request's running slot (4 bytes);
+    a row with a slot also reads num_computed and num_sampled and writes the
+    column and the accepted count (16 bytes)."""
+    recorded = sum(1 for s in idx_mapping if int(s) >= 0)
+    return 4 * len(idx_mapping) + 16 * recorded
+
+
+def measure_record_state_blocks(wl: W.Workload, device, iters: int, warmup: int):
+    """The align-mode bookkeeping after the commit on the workload's rows, timed
+    alone from a CUDA graph replay: one spec row per request, null rows
+    without a running slot, running slots a permutation of twice as many,
+    num_computed drawn below 64, num_sampled the first step's accepted
+    counts.  A few bytes per row: the launch is bound by its latency, not by
+    HBM."""
+    from linear_attention_speculative_kda_gb300 import api
+    B = wl.spec.B
+    gen = torch.Generator().manual_seed(19)
+    idx = torch.randperm(2 * B, generator=gen)[:B].to(torch.int32)
+    idx = torch.where(wl.state_indices > 0, idx, torch.full_like(idx, -1))
+    num_computed = torch.randint(0, 64, (B,), generator=gen, dtype=torch.int32)
+    num_sampled = wl.steps[0].num_accepted.clamp(min=0).to(torch.int32)
+    i32 = dict(dtype=torch.int32, device=device)
+    d_idx, d_ns, d_nc = idx.to(**i32), num_sampled.to(**i32), num_computed.to(**i32)
+    col = torch.zeros(2 * B, **i32)
+    acc = torch.zeros(2 * B, **i32)
+    err = torch.zeros(1, **i32)
+
+    def launch(_k):
+        api.kda_record_state_blocks(d_idx, d_ns, d_nc, col, acc, block_size=16,
+                                    block_table_width=8, error_word=err)
+
+    us, how = time_launches(launch, iters, warmup)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in record_state_blocks")
+    b = record_blocks_bytes(idx.tolist())
+    return {"rows": B, "timing": how, "launches": iters, "avg_us": us, "bytes_per_launch": b,
+            "bound": "latency"}
+
+
 def measure_commit_align(wl: W.Workload, device, iters: int, warmup: int, peak: float):
     """The align-mode commit on the workload's rows, timed alone: a pool with
     the row checkpoints and two blocks per request (block size 16; each
@@ -933,9 +974,10 @@ def run_ours(args):
 
     # the align-mode (paged-block) commit on the same rows, timed on its own
     del hio
-    align = None
+    align = record = None
     if not args.no_extras:
         align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
+        record = measure_record_state_blocks(wl, device, max(20, args.steps // 4), args.warmup)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -951,7 +993,8 @@ def run_ours(args):
             "gpu_launches": nl * args.steps,
             "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
             "extras": None if args.no_extras else {"conv_compact": conv,
-                                                   "commit_align": align}}
+                                                   "commit_align": align,
+                                                   "record_state_blocks": record}}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:

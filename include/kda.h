@@ -337,6 +337,43 @@ kda_status kda_conv_compact_align(const kda_conv_config *cc, void *conv_state,
                                   const kda_align *align,
                                   int32_t *error_word, void *stream);
 
+/*
+ * kda_record_state_blocks -- the align-mode bookkeeping after a commit
+ * (recoverssm.py, `_record_state_block_kernel` and `record_state_blocks`,
+ * run from the runner's commit hook): each committed request's running
+ * state column is pointed at the block that holds its last committed token,
+ * where kda_commit_align left its state, and its accepted count is reset to
+ * 1, so that the next step's pre-step copy reads the state from there.  For
+ * each spec row i in [0, B):
+ *   q    = align->request_indices[i] (NULL: q = i)
+ *   s    = idx_mapping[q], the request's index in the running arrays;
+ *          s < 0: nothing is recorded for the row
+ *   last = max(align->num_computed[q] + num_sampled[q] - 1, 0)
+ *   state_column[s] = min(last / align->block_size, align->block_table_width - 1)
+ *   num_accepted[s] = 1
+ * With num_sampled[q] equal to the commit count n of the row, state_column[s]
+ * is the column of the final block in kda_commit_align.
+ *
+ * align: block_size >= 1, block_table_width >= 1, num_requests >= 1 and
+ *   num_computed are read; block_table and block_table_stride are not (the
+ *   descriptor passed to kda_commit_align can be reused as it is).
+ * idx_mapping, num_sampled: int32 [num_requests], device.
+ * state_column, num_accepted: int32 [num_states], device, written for the
+ *   rows' s only; num_states >= 1.
+ * Device-detected bad data: q outside [0, num_requests) flags
+ * KDA_ROW_BAD_BLOCK, s >= num_states flags KDA_ROW_BAD_SLOT; the row is
+ * skipped.  Two rows with the same s are the caller's error (one of the two
+ * writes wins).  B == 0: KDA_OK, nothing inspected or launched.  A host check
+ * above that fails (or a NULL or misaligned pointer) returns
+ * KDA_ERR_INVALID_ARG.  One thread per row, one launch on `stream`.
+ */
+kda_status kda_record_state_blocks(const kda_align *align,
+                                   const int32_t *idx_mapping, const int32_t *num_sampled,
+                                   int32_t B,
+                                   int32_t *state_column, int32_t *num_accepted,
+                                   int32_t num_states,
+                                   int32_t *error_word, void *stream);
+
 /* Name of a status code (static string). */
 const char *kda_status_string(kda_status status);
 

@@ -46,6 +46,7 @@ EXPORTED = (
     "kda_conv_compact",
     "kda_commit_align",
     "kda_conv_compact_align",
+    "kda_record_state_blocks",
     "kda_status_string",
     "kda_abi_version",
 )
@@ -153,6 +154,8 @@ def bind_library(path: str):
     lib.kda_conv_compact_align.restype = ctypes.c_int
     lib.kda_conv_compact_align.argtypes = ([ctypes.POINTER(KdaConvConfig)] + [vp] * 3 + [i32] +
                                            [vp, alp, vp, vp])
+    lib.kda_record_state_blocks.restype = ctypes.c_int
+    lib.kda_record_state_blocks.argtypes = [alp, vp, vp, i32, vp, vp, i32, vp, vp]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_abi_version.restype = i32
@@ -608,3 +611,51 @@ def kda_conv_compact_align(conv_state, cu_seqlens, state_indices, num_accepted, 
                                     _ptr(state_indices), B, _ptr(num_accepted),
                                     ctypes.byref(al), _ptr(error_word), _stream_ptr(dev))
     _check("kda_conv_compact_align", st)
+
+
+def kda_record_state_blocks(idx_mapping, num_sampled, num_computed, state_column, num_accepted,
+                            *, block_size: int, block_table_width: int, num_rows=None,
+                            request_indices=None, error_word=None) -> None:
+    """``kda_record_state_blocks``: after an align-mode commit, point each
+    committed request's running state column at the block of its last
+    committed token and reset its accepted count to 1.  idx_mapping,
+    num_sampled and num_computed are int32 per request; state_column and
+    num_accepted int32 per running slot.  ``num_rows`` spec rows (default:
+    request_indices' length, else one per request)."""
+    dev = state_column.device
+    i32 = torch.int32
+    for name, t in (("idx_mapping", idx_mapping), ("num_sampled", num_sampled),
+                    ("num_computed", num_computed), ("state_column", state_column),
+                    ("num_accepted", num_accepted)):
+        _req(t, i32, name, dev)
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    _opt(request_indices, i32, "request_indices", dev)
+    _opt(error_word, i32, "error_word", dev)
+    num_requests = idx_mapping.shape[0]
+    if num_sampled.shape[0] < num_requests or num_computed.shape[0] < num_requests:
+        raise ValueError("num_sampled and num_computed need one entry per request")
+    if num_accepted.shape[0] != state_column.shape[0]:
+        raise ValueError("state_column and num_accepted must have the same length")
+    if num_rows is None:
+        num_rows = num_requests if request_indices is None else request_indices.shape[0]
+    if request_indices is not None:
+        if not request_indices.is_contiguous():
+            raise ValueError("request_indices must be contiguous")
+        _at_least(request_indices, num_rows, "request_indices")
+    elif num_rows > num_requests:
+        raise ValueError("more spec rows than requests without request_indices")
+    al = KdaAlign()
+    al.block_table = None  # not read by this call
+    al.block_table_stride = 0
+    al.block_table_width = block_table_width
+    al.block_size = block_size
+    al.num_requests = num_requests
+    al.reserved = 0
+    al.num_computed = num_computed.data_ptr()
+    al.request_indices = None if request_indices is None else request_indices.data_ptr()
+    lib = load_library()
+    st = lib.kda_record_state_blocks(ctypes.byref(al), _ptr(idx_mapping), _ptr(num_sampled),
+                                     num_rows, _ptr(state_column), _ptr(num_accepted),
+                                     state_column.shape[0], _ptr(error_word), _stream_ptr(dev))
+    _check("kda_record_state_blocks", st)

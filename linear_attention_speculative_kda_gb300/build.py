@@ -1,6 +1,6 @@
 """Compile the CUDA library ``libkda.so`` in-tree for sm_103a.
 
-Two translation units in one nvcc call, one ``-gencode`` (compute_103a /
+Three translation units in one nvcc call, one ``-gencode`` (compute_103a /
 sm_103a), the CUDA runtime linked statically so the library only needs the
 driver at run time.
 """
@@ -15,7 +15,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "kda_kernels.cu"), os.path.join(CSRC, "kda_conv.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("kda_kernels.cu", "kda_conv.cu", "kda_blocks.cu")]
 DEPENDS = SOURCES + [
     os.path.join(CSRC, "kda_device.cuh"),
     os.path.join(CSRC, "kda_async.cuh"),

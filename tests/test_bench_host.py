@@ -285,3 +285,9 @@ def test_cpu_baseline_reports_three_legs():
         ("fp64", line["cores"]), ("fp32", line["cores"]), ("fp64", 1)]
     assert line["kind"] == "oracle" and line["value"] == legs[0]["value"]
     assert all(leg["value"] > 0 for leg in legs)
+
+
+def test_record_blocks_bytes_by_recorded_rows():
+    # 3 rows read their slot (12 bytes); 2 have one and move 16 bytes each
+    assert bench.record_blocks_bytes([4, -1, 0]) == 3 * 4 + 2 * 16
+    assert bench.record_blocks_bytes([]) == 0

@@ -225,6 +225,30 @@ def test_conv_compact_align_host_checks(lib):
     assert call(None, B=0) == api.KDA_OK
 
 
+def test_record_state_blocks_host_checks(lib):
+    def call(al, B=3, idx=FAKE, ns=FAKE, col=FAKE, acc=FAKE, num_states=8, err=None):
+        alp = None if al is None else ctypes.byref(al)
+        return lib.kda_record_state_blocks(alp, idx, ns, B, col, acc, num_states, err, None)
+
+    assert call(None) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(block_size=0)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(block_table_width=0)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(num_requests=0)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(reserved=1)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(num_computed=None)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(num_computed=FAKE + 2)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(request_indices=FAKE + 1)) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), idx=None) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), ns=None) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), col=FAKE + 2) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), acc=None) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), err=FAKE + 1) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), num_states=0) == api.KDA_ERR_INVALID_ARG
+    assert call(_align(), B=-1) == api.KDA_ERR_INVALID_ARG
+    # B == 0: nothing to do, and no pointer is looked at
+    assert call(None, B=0, idx=None, ns=None, col=None, acc=None) == api.KDA_OK
+
+
 def test_binding_refuses_small_records_buffer(lib):
     # the size check runs before any device call, so CPU tensors suffice
     import torch

@@ -291,3 +291,41 @@ def test_deferred_align_commit_against_oracle_and_eager(Q, bounded):
     torch.cuda.synchronize()
     assert int(g.err.item()) == 0
     assert torch.equal(g.pool, e.pool)
+
+
+@pytest.mark.parametrize("with_indices", [False, True], ids=["rows_are_requests", "request_indices"])
+def test_record_state_blocks_bit_exact(with_indices):
+    """kda_record_state_blocks against the oracle, bit for bit: 700 requests
+    (three CTAs and a ragged tail), a third of them without a running slot,
+    columns past the table clamped; through request_indices, a permuted
+    subset of the requests, plus one request index and one slot out of range
+    (flagged, skipped)."""
+    rng = np.random.default_rng(21 if with_indices else 20)
+    dev = torch.device("cuda", 0)
+    R, S, bs, width = 700, 900, 16, 8
+    idx = rng.permutation(S)[:R].astype(np.int32)
+    idx[rng.random(R) < 0.33] = -1
+    nc = rng.integers(0, 150, size=R).astype(np.int32)
+    ns = rng.integers(0, 9, size=R).astype(np.int32)
+    req = None
+    if with_indices:
+        req = rng.permutation(R)[:500].astype(np.int32)
+        req[7] = R + 3                      # past the requests: KDA_ROW_BAD_BLOCK
+        idx[req[11]] = S + 5                # past the running slots: KDA_ROW_BAD_SLOT
+    col0 = rng.integers(0, 99, size=S).astype(np.int32)
+    acc0 = rng.integers(2, 9, size=S).astype(np.int32)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    col, acc, err = t(col0), t(acc0), torch.zeros(1, dtype=torch.int32, device=dev)
+    api.kda_record_state_blocks(t(idx), t(ns), t(nc), col, acc, block_size=bs,
+                                block_table_width=width,
+                                request_indices=None if req is None else t(req), error_word=err)
+    torch.cuda.synchronize()
+    want_col, want_acc, issues = O.record_state_blocks(idx, ns, nc, col0, acc0, bs, width,
+                                                       request_indices=req)
+    assert col.cpu().numpy().tolist() == want_col.tolist()
+    assert acc.cpu().numpy().tolist() == want_acc.tolist()
+    want_err = 0
+    for i in issues:
+        want_err |= api.ROW_BAD_BLOCK if i.reason == "block" else api.ROW_BAD_SLOT
+    assert int(err.item()) == want_err
+    assert want_err == ((api.ROW_BAD_BLOCK | api.ROW_BAD_SLOT) if with_indices else 0)
