@@ -1045,7 +1045,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the separately timed conv compaction and align commit")
+                    help="skip the separately timed conv compaction, align commit and "
+                         "running state column")
     ap.add_argument("--reference-rows", type=int, default=8)
     ap.add_argument("--records", choices=["raw", "correction"], default="raw",
                     help="record format: raw inputs replayed (default) or fp32 deltas folded")
