@@ -3,7 +3,7 @@
 // recoverssm.py, `_compact_conv_state_kernel` (non-align form): after n
 // accepted tokens the window of each channel that starts at column n - 1
 // moves to column 0.  Every element a thread writes it has read itself (or,
-// in the staged form, the CTA has read it into shared memory) before any
+// in the bulk form, the CTA has loaded it into shared memory) before any
 // write, so a window that overlaps its destination is moved correctly.
 // A row with n = 1 keeps every window where it is and is skipped.  Three
 // forms, chosen on the host from the strides:
