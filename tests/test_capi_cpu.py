@@ -339,3 +339,29 @@ def test_binding_checks_shapes_before_any_launch(lib):
     with pytest.raises(ValueError):   # pending shorter than the record slots
         api.kda_flush(a["A_log"], a["g_bias"], a["state_pool"], a["state_indices"], a["records"],
                       torch.zeros(0, dtype=i32), window=4, record_slots=1)
+
+
+def test_binding_checks_record_state_blocks_sizes(lib):
+    # every check raises before the library is called, so CPU tensors suffice
+    import torch
+    i32 = torch.int32
+    idx = torch.zeros(4, dtype=i32)
+    col = torch.zeros(6, dtype=i32)
+
+    def call(**kw):
+        args = dict(idx_mapping=idx, num_sampled=torch.zeros(4, dtype=i32),
+                    num_computed=torch.zeros(4, dtype=i32), state_column=col,
+                    num_accepted=torch.zeros(6, dtype=i32))
+        args.update(kw)
+        api.kda_record_state_blocks(block_size=16, block_table_width=4, **args)
+
+    with pytest.raises(ValueError, match="per request"):
+        call(num_sampled=torch.zeros(3, dtype=i32))
+    with pytest.raises(ValueError, match="same length"):
+        call(num_accepted=torch.zeros(5, dtype=i32))
+    with pytest.raises(ValueError, match="more spec rows"):
+        call(num_rows=5)
+    with pytest.raises(ValueError, match="request_indices needs"):
+        call(request_indices=torch.zeros(2, dtype=i32), num_rows=3)
+    with pytest.raises(TypeError):
+        call(idx_mapping=torch.zeros(4, dtype=torch.int64))
