@@ -184,7 +184,7 @@ kda_status kda_verify(const kda_config *cfg,
  * state_indices[b] > 0, n > 0 and its record slot r >= 0.
  * Eager mode (pending == NULL): a valid row replays its first n records from
  * state_pool[s][h] and writes the resulting state once (bit-identical to the
- * state the verify computed after its n-th token: same kernels, same order).
+ * verify's trajectory state after its n-th token: same kernels, same order).
  * Deferred mode (pending != NULL): for every row with r >= 0, pending[r] is
  * set to n if the row is valid and not eager, else 0; rows with
  * eager[b] != 0 (eager may be NULL: no row) are committed now as above.
