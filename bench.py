@@ -349,6 +349,50 @@ def plan_bytes(wl: W.Workload, record_format: str = "raw"):
             ("verify_fused", float(v2)), ("commit", float(c2))]
 
 
+STATE_ELEMS = 128 * 128
+FP32_LANES_PER_SM = 128  # 4 SMSPs x 32 FP32 lanes
+
+
+def plan_fp32_ops(wl: W.Workload, record_format: str = "raw"):
+    """Algorithmic FP32 operations (a multiply or a fused multiply-add each
+    counts one) of each launch of one step, from the same drawn counts as
+    plan_bytes: per state element, 4 per verified token (the decay, u = S k^,
+    the rank-one update and o = S q^) and 3 per replayed token (no output;
+    2 with correction records, which skip u)."""
+    rep_ops = 2 if record_format == "correction" else 3
+    sp = wl.spec
+    H = sp.H
+    lens = wl.lens.numpy().astype(np.int64)
+    live = wl.state_indices.numpy() > 0
+
+    def commit_n(acc):
+        return np.minimum(np.maximum(acc, 0), np.minimum(lens, sp.Q))
+
+    def ops(tokens, per):
+        return float(np.where(live, tokens, 0).sum() * H * per * STATE_ELEMS)
+
+    v1 = ops(lens, 4)
+    if not sp.deferred:
+        n = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
+        return [("verify", v1), ("commit", ops(n, rep_ops))]
+    n1 = commit_n(wl.steps[0].num_accepted.numpy().astype(np.int64))
+    eager1 = wl.steps[0].eager.numpy().astype(bool)
+    n2 = commit_n(wl.steps[1].num_accepted.numpy().astype(np.int64))
+    pend = np.where(live & (n1 > 0) & ~eager1, n1, 0)
+    return [("verify", v1), ("commit_deferred", ops(np.where(eager1, n1, 0), rep_ops)),
+            ("verify_fused", v1 + ops(pend, rep_ops)), ("commit", ops(n2, rep_ops))]
+
+
+def fp32_peak(device, clock_summary):
+    """FP32 FMA-pipe peak in T ops/s from the unit counts: SMs x 128 lanes x
+    the SM clock sampled during the run (else the part's 2,070 MHz maximum)."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mhz = clock_summary.get("sm_mhz") or 2070.0
+    src = ("sampled SM clock" if clock_summary.get("sm_mhz") else "maximum SM clock")
+    return sms * FP32_LANES_PER_SM * mhz * 1e6 / 1e12, (
+        f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz ({src})")
+
+
 def units_per_step(wl: W.Workload) -> int:
     return wl.spec.B * wl.spec.H * wl.spec.steps
 
@@ -906,12 +950,15 @@ def run_ours(args):
     ms_per_step = ms_total / args.steps
 
     peak, peak_src = hbm_peak()
+    clock_summary = clocks.summary()
+    ops_per = dict(plan_fp32_ops(wl, args.records))
     kernels = []
     for n in names:
         avg_ms = statistics.mean(per_kernel[n])
         b = bytes_per[n]
         kernels.append({"name": n, "launches": args.steps, "avg_us": avg_ms * 1e3,
                         "bytes_per_launch": b, "gbs": b / (avg_ms / 1e3) / 1e9,
+                        "fp32_ops_per_launch": ops_per[n],
                         "share": sum(per_kernel[n]) / max(1e-9, sum(sum(v) for v in
                                                                   per_kernel.values()))})
     dom = max(kernels, key=lambda x: x["share"])
@@ -923,6 +970,17 @@ def run_ours(args):
                 "peak_source": f"{peak_src} ({'of measured' if peak_src == 'measured' else 'of fallback'})",
                 "traffic": traffic, "traffic_source": traffic_src,
                 "algorithmic_bytes_per_launch": dom["bytes_per_launch"]}
+    # the FP32 pipe beside it, and the launch against the lower of the two roofs
+    alu_peak, alu_src = fp32_peak(device, clock_summary)
+    dom_s = dom["avg_us"] / 1e6
+    t_hbm = dom["bytes_per_launch"] / (peak * 1e9)
+    t_alu = dom["fp32_ops_per_launch"] / (alu_peak * 1e12)
+    roofline["alu"] = {"ops_per_launch": dom["fp32_ops_per_launch"], "unit": "T ops/s",
+                       "achieved": dom["fp32_ops_per_launch"] / dom_s / 1e12,
+                       "peak": alu_peak, "frac": t_alu / dom_s, "peak_source": alu_src}
+    roofline["min_roof"] = {"bound": "hbm" if t_hbm >= t_alu else "alu",
+                            "roof_us": max(t_hbm, t_alu) * 1e6,
+                            "frac": max(t_hbm, t_alu) / dom_s}
     step_gbs = step_bytes * args.steps / (ms_total / 1e3) / 1e9
 
     # end to end through the public API with host buffers: issued call by
@@ -991,7 +1049,7 @@ def run_ours(args):
             "roofline": roofline, "kernels": kernels,
             "kernel_timing": "per-launch CUDA events over a second pass of the same steps",
             "gpu_launches": nl * args.steps,
-            "e2e": e2e, "clocks": clocks.summary(), "cpu_baseline": cpu,
+            "e2e": e2e, "clocks": clock_summary, "cpu_baseline": cpu,
             "extras": None if args.no_extras else {"conv_compact": conv,
                                                    "commit_align": align,
                                                    "record_state_blocks": record}}

@@ -291,3 +291,27 @@ def test_record_blocks_bytes_by_recorded_rows():
     # 3 rows read their slot (12 bytes); 2 have one and move 16 bytes each
     assert bench.record_blocks_bytes([4, -1, 0]) == 3 * 4 + 2 * 16
     assert bench.record_blocks_bytes([]) == 0
+
+
+def test_plan_fp32_ops_by_hand():
+    # eager workload: rows of T = 4, 0, 2 (the middle one a null row), H = 2
+    wl = W.custom(B=3, H=2, Q=4, lens=[4, 3, 2], S=6, seed=3, slots=[1, 0, 2])
+    wl.steps[0].num_accepted[:] = torch.tensor([3, 4, 9])
+    ops = dict(bench.plan_fp32_ops(wl))
+    E = 128 * 128
+    assert ops["verify"] == (4 + 2) * 2 * 4 * E          # live rows' tokens x H x 4
+    assert ops["commit"] == (3 + 2) * 2 * 3 * E          # n = 3 and min(9, 2) = 2
+    assert dict(bench.plan_fp32_ops(wl, "correction"))["commit"] == (3 + 2) * 2 * 2 * E
+
+
+def test_plan_fp32_ops_deferred_steps():
+    wl = W.custom(B=4, H=1, Q=4, lens=[4, 4, 4, 4], S=6, R=4, deferred=True, steps=2, seed=5)
+    wl.steps[0].num_accepted[:] = torch.tensor([2, 3, 0, 4])
+    wl.steps[0].eager[:] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8)
+    wl.steps[1].num_accepted[:] = torch.tensor([1, 1, 1, 1])
+    ops = dict(bench.plan_fp32_ops(wl))
+    E = 128 * 128
+    assert ops["verify"] == 16 * 4 * E
+    assert ops["commit_deferred"] == 2 * 3 * E            # the eager row replays 2
+    assert ops["verify_fused"] == 16 * 4 * E + (3 + 4) * 3 * E   # folds 3 and 4 pending
+    assert ops["commit"] == 4 * 3 * E
