@@ -636,12 +636,15 @@ __device__ __forceinline__ void window_outputs(const Tile &h, const TokView &tv,
 // 0..15 and X_lo in rows 16..31 (N = 32), and
 //   D_hi = S_hi [X_hi; X_lo]^T,   D_lo = S_lo [X_hi; X_lo]^T
 // are accumulated apart (every product of the four parts, 16 K steps each)
-// and added in fp32, the small terms first.  S_hi is S in the
-// swizzled staging buffer itself (the tensor core drops the low bits): the
+// and added in fp32, the small terms first.  Operand A comes from TMEM: each
+// thread copies its row of S there from the swizzled staging buffer (the
 // staged checkpoint, or, after folded tokens, the folded state written back
-// there.  S_lo goes to TMEM, X_hi and X_lo to shared memory.  Thread ct of
-// the consumer group owns channel ct of the vectors and row ct of S, D and
-// the outputs.  New token t sits in slot p0 + t (p0 folded tokens first).
+// there), which frees the staging buffer at once; the tensor core reads the
+// fp32 columns as TF32, that is S_hi.  Once D_hi is complete each thread
+// replaces its row by S_lo in the same columns for D_lo.  X_hi and X_lo go
+// to shared memory.  Thread ct of the consumer group owns channel ct of the
+// vectors and row ct of S, D and the outputs.  New token t sits in slot
+// p0 + t (p0 folded tokens first).
 
 // Pair coefficients, then the operand vectors of the channel into shared
 // memory (swizzled, K-major).  The thread keeps its row's v_t in vrow: the
@@ -704,10 +707,10 @@ __device__ __forceinline__ bool window_tc_prep(const TokView &tv, int p0, int T,
     return true;
 }
 
-// S_lo of row ct (S in the staging buffer, four swizzled 32-column blocks)
-// into TMEM columns s_lo .. s_lo + 127 of the thread's lane, 16 at a time.
-__device__ __forceinline__ void s_lo_to_tmem(const unsigned char *staging, int ct,
-                                             uint32_t s_lo) {
+// Row ct of S (the staging buffer, four swizzled 32-column blocks) into
+// TMEM columns a .. a + 127 of the thread's lane, 16 at a time.  The tensor
+// core reads these fp32 columns as TF32, that is S_hi.
+__device__ __forceinline__ void s_row_to_tmem(const unsigned char *staging, int ct, uint32_t a) {
 #pragma unroll
     for (int half = 0; half < 8; ++half) {
         uint32_t u[16];
@@ -715,37 +718,47 @@ __device__ __forceinline__ void s_lo_to_tmem(const unsigned char *staging, int c
         for (int c = 0; c < 4; ++c) {
             const float4 q = *reinterpret_cast<const float4 *>(
                 staging + (half >> 1) * 16384 + sw128_offset(ct, 16 * (half & 1) + 4 * c));
-            u[4 * c + 0] = __float_as_uint(__fsub_rn(q.x, tf32_hi(q.x)));
-            u[4 * c + 1] = __float_as_uint(__fsub_rn(q.y, tf32_hi(q.y)));
-            u[4 * c + 2] = __float_as_uint(__fsub_rn(q.z, tf32_hi(q.z)));
-            u[4 * c + 3] = __float_as_uint(__fsub_rn(q.w, tf32_hi(q.w)));
+            u[4 * c + 0] = __float_as_uint(q.x);
+            u[4 * c + 1] = __float_as_uint(q.y);
+            u[4 * c + 2] = __float_as_uint(q.z);
+            u[4 * c + 3] = __float_as_uint(q.w);
         }
-        tmem_st16(s_lo + 16 * half, u);
+        tmem_st16(a + 16 * half, u);
     }
 }
 
-// D_hi = S_hi [X_hi; X_lo]^T over K = 128 (16 steps of 8), A from the
-// staging buffer; by one thread.  A step's descriptors are the first ones
-// plus its byte offset / 16 (the start address field does not overflow).
-__device__ __forceinline__ void window_tc_mma_hi(uint32_t staging, uint32_t xbase,
-                                                 uint32_t d_hi) {
-    constexpr uint32_t idesc = tf32_idesc(128, 32);
-    const uint64_t a0 = sw128_desc(staging), b0 = sw128_desc(xbase);
+// S in TMEM columns a .. a + 127 of the thread's lane replaced by
+// S_lo = S - tf32(S), in two halves of 64 columns (once the product that
+// reads S from them has completed).
+__device__ __forceinline__ void s_lo_in_tmem(uint32_t a) {
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-        const uint32_t w = (uint32_t)(k & 3) * 32u;
-        umma_tf32_ss(d_hi, a0 + (((uint32_t)(k >> 2) * 16384u + w) >> 4),
-                     b0 + (((uint32_t)(k >> 2) * (uint32_t)kXBlock + w) >> 4), idesc, k > 0);
+    for (int h = 0; h < 2; ++h) {
+        uint32_t u[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tmem_ld16(a + 64u * h + 16u * i, u[i]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float x = __uint_as_float(u[i][j]);
+                u[i][j] = __float_as_uint(__fsub_rn(x, tf32_hi(x)));
+            }
+            tmem_st16(a + 64u * h + 16u * i, u[i]);
+        }
     }
 }
 
-// D_lo = S_lo [X_hi; X_lo]^T, A from TMEM (S_lo, one fp32 per column).
-__device__ __forceinline__ void window_tc_mma_lo(uint32_t s_lo, uint32_t xbase, uint32_t d_lo) {
+// D = A [X_hi; X_lo]^T over K = 128 (16 steps of 8), A from TMEM (one fp32
+// per column: S, read as S_hi, or S_lo); by one thread.  A step's B
+// descriptor is the first one plus its byte offset / 16 (the start address
+// field does not overflow).
+__device__ __forceinline__ void window_tc_mma(uint32_t a, uint32_t xbase, uint32_t d) {
     constexpr uint32_t idesc = tf32_idesc(128, 32);
     const uint64_t b0 = sw128_desc(xbase);
 #pragma unroll
     for (int k = 0; k < 16; ++k)
-        umma_tf32_ts(d_lo, s_lo + 8u * (uint32_t)k,
+        umma_tf32_ts(d, a + 8u * (uint32_t)k,
                      b0 + (((uint32_t)(k >> 2) * (uint32_t)kXBlock + (uint32_t)(k & 3) * 32u) >> 4),
                      idesc, k > 0);
 }

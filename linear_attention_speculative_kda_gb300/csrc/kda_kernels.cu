@@ -807,7 +807,11 @@ __device__ void run_producer(const Params &p, unsigned char *smem, const Layout 
         }
         TokView tv(smem + lay.off_tok + (c * lay.nbuf + b) * lay.tok_bytes, lay.slots, p.Q,
                    lay.head);
-        prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt, kWindow && cur.T >= kWindowMinT);
+        // an item in either window form needs no k^ . q^ (the tensor build's
+        // window items that cannot take the tensor form run token by token)
+        const bool window_item = tensor_item<kWindow>(p, smem, cur.T) ||
+                                 (kWindow && !kTensorWindow && cur.T >= kWindowMinT);
+        prep_item<kMode, kBounded, kCorr>(p, cur, rv, tv, pt, window_item);
         if (pt == kHandoffThread) {
             ItemInfo &it = sy.info[c][b];
             it.head = cur.head;
@@ -876,7 +880,9 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
         // tensor window form (window kernels): the outputs' row products on
         // the tensor core, from the swizzled staging buffer
         const bool tensor = tensor_item<kWindow>(p, smem, it.T);
-        const bool window = kWindow && it.T >= kWindowMinT;
+        // the FMA window form; the tensor build has none (its window items
+        // that cannot take the tensor form run token by token)
+        const bool window = kWindow && !kTensorWindow && it.T >= kWindowMinT;
         unsigned char *stage = smem + lay.off_state + c * (kD * kD * 4);
         // the FMA window form's coefficients, before the tile occupies registers
         if constexpr (kWindow)
@@ -940,40 +946,48 @@ __device__ void run_consumer(const Params &p, unsigned char *smem, const Layout 
             // tensor window form, from here with no tile in registers
             float vrow[kMaxQ];
             if (!window_tc_prep(tv, it.p, it.T, p.Q, ct, vrow, group_sync)) return;
-            if (!group_sync()) return;  // the operands X in place
             if (it.p == 0 && !wait_phase(&sy.full_state[c], k & 1, sy, p)) return;
             const uint32_t tmem = sy.tmem_base + 256u * (uint32_t)c;  // this consumer's columns
             const uint32_t lanes = (uint32_t)(32 * (ct >> 5)) << 16;  // this warp's TMEM lanes
+            const uint32_t a_cols = tmem + lanes + 128u;               // A: S, then S_lo
             const uint32_t mbar_parity = mma_uses & 1u;
-            if (ct == 0) {
-                tc_fence_after();
-                window_tc_mma_hi(smem_u32(stage), smem_u32(tv.kh), tmem);
-                umma_commit(&sy.mma_hi[c]);
-            }
-            // meanwhile S_lo into TMEM (the staging buffer is only read)
-            s_lo_to_tmem(stage, ct, tmem + lanes + 128u);
+            // the state's row into A (read by the tensor core as S_hi); the
+            // staging buffer is free once every row is read
+            s_row_to_tmem(stage, ct, a_cols);
+            mbar_arrive(&sy.empty_state[c]);
             tmem_wait_st();
             tc_fence_before();
-            // the products finish in microseconds whatever the other roles do:
-            // wait for them even after an abort (the TMEM and the staging
-            // buffer must not be reused under them)
-            if (!group_sync()) {  // S_lo in place
-                mbar_wait_bounded(&sy.mma_hi[c], mbar_parity, kWaitBudget);
-                return;
-            }
+            if (!group_sync()) return;  // the operands X and A in place
             if (ct == 0) {
                 tc_fence_after();
-                window_tc_mma_lo(tmem + 128u, smem_u32(tv.kh), tmem + 32u);
+                window_tc_mma(tmem + 128u, smem_u32(tv.kh), tmem);  // D_hi
+                umma_commit(&sy.mma_hi[c]);
+            }
+            // A takes S_lo once D_hi has read it.  The products finish in
+            // microseconds whatever the other roles do, so a product in flight
+            // is waited for before any thread leaves (TMEM must not be freed
+            // under it).
+            if (!mbar_wait_bounded(&sy.mma_hi[c], mbar_parity, kWaitBudget)) {
+                *reinterpret_cast<volatile int *>(&sy.abort) = 1;
+                flag_error(p.err, kErrWaitTimeout);
+                return;
+            }
+            tc_fence_after();
+            s_lo_in_tmem(a_cols);
+            tmem_wait_st();
+            tc_fence_before();
+            if (!group_sync()) return;  // S_lo in place (no product in flight)
+            if (ct == 0) {
+                tc_fence_after();
+                window_tc_mma(tmem + 128u, smem_u32(tv.kh), tmem + 32u);  // D_lo
                 umma_commit(&sy.mma_done[c]);
             }
-            if (!mbar_wait_bounded(&sy.mma_hi[c], mbar_parity, kWaitBudget) ||
-                !mbar_wait_bounded(&sy.mma_done[c], mbar_parity, kWaitBudget)) {
+            if (!mbar_wait_bounded(&sy.mma_done[c], mbar_parity, kWaitBudget)) {
                 *reinterpret_cast<volatile int *>(&sy.abort) = 1;
                 flag_error(p.err, kErrWaitTimeout);
                 return;
             }
             ++mma_uses;
-            mbar_arrive(&sy.empty_state[c]);  // the staging buffer is free
             tc_fence_after();
             window_tc_solve(tv, it.p, it.T, p.Q, ct, vrow, tmem + lanes,
                             p.out + ((size_t)it.bos * p.H + it.head) * kD, (size_t)p.H * kD);
