@@ -787,6 +787,45 @@ def measure_conv_compact(wl: W.Workload, device, iters: int, warmup: int, peak: 
             "gbs": b / (us / 1e6) / 1e9, "frac": b / (us / 1e6) / 1e9 / peak}
 
 
+def flush_bytes(wl: W.Workload, record_format: str = "raw") -> int:
+    """Algorithmic bytes of one flush after the first step's deferred commit:
+    every (row, head) with a pending replay (slot > 0, n > 0, not eager)
+    reads its checkpoint and its p records and writes the checkpoint."""
+    _, rec_b = format_bytes(record_format)
+    sp = wl.spec
+    lens = wl.lens.numpy().astype(np.int64)
+    live = wl.state_indices.numpy() > 0
+    acc = wl.steps[0].num_accepted.numpy().astype(np.int64)
+    n1 = np.minimum(np.maximum(acc, 0), np.minimum(lens, sp.Q))
+    eager1 = wl.steps[0].eager.numpy().astype(bool)
+    pend = np.where(live & (n1 > 0) & ~eager1, n1, 0)
+    return int(np.where(pend > 0, 2 * STATE_BYTES + pend * rec_b, 0).sum() * sp.H)
+
+
+def measure_flush(wl: W.Workload, device, iters: int, warmup: int, peak: float,
+                  record_format: str = "raw"):
+    """kda_flush after the first step's verify and deferred commit (the
+    pending replays of every deferred row), timed alone from a CUDA graph
+    replay.  Every launch folds the same pending counts, so each moves the
+    same bytes."""
+    eng = Engine(wl, device, record_format)
+    fns = dict(eng.launches())
+    fns["verify"]()
+    fns["commit_deferred"]()
+
+    def launch(_k):
+        eng.api.kda_flush(eng.A_log, eng.g_bias, eng.pool, eng.slots, eng.records, eng.pending,
+                          record_rows=eng.rr, error_word=eng.err, **eng.kw)
+
+    us, how = time_launches(launch, iters, warmup)
+    if int(eng.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(eng.err.item())} in the flush")
+    b = flush_bytes(wl, record_format)
+    del eng
+    return {"timing": how, "launches": iters, "avg_us": us, "bytes_per_launch": b,
+            "gbs": b / (us / 1e6) / 1e9, "frac": b / (us / 1e6) / 1e9 / peak}
+
+
 def align_commit_bytes(wl: W.Workload, table, num_computed, block_size: int, acc) -> int:
     """Algorithmic bytes of one align-mode commit: every committing (row,
     head) reads its checkpoint and n records and writes the final block, plus
@@ -1032,10 +1071,13 @@ def run_ours(args):
 
     # the align-mode (paged-block) commit on the same rows, timed on its own
     del hio
-    align = record = None
+    align = record = flush = None
     if not args.no_extras:
         align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
         record = measure_record_state_blocks(wl, device, max(20, args.steps // 4), args.warmup)
+        if wl.spec.deferred:
+            flush = measure_flush(wl, device, max(20, args.steps // 4), args.warmup, peak,
+                                  args.records)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1052,7 +1094,8 @@ def run_ours(args):
             "e2e": e2e, "clocks": clock_summary, "cpu_baseline": cpu,
             "extras": None if args.no_extras else {"conv_compact": conv,
                                                    "commit_align": align,
-                                                   "record_state_blocks": record}}
+                                                   "record_state_blocks": record,
+                                                   "flush": flush}}
     if world > 1:
         torch.distributed.barrier()
     if rank == 0:
@@ -1103,8 +1146,8 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the separately timed conv compaction, align commit and "
-                         "running state column")
+                    help="skip the separately timed conv compaction, align commit, "
+                         "running state column and flush")
     ap.add_argument("--reference-rows", type=int, default=8)
     ap.add_argument("--records", choices=["raw", "correction"], default="raw",
                     help="record format: raw inputs replayed (default) or fp32 deltas folded")

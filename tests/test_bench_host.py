@@ -315,3 +315,13 @@ def test_plan_fp32_ops_deferred_steps():
     assert ops["commit_deferred"] == 2 * 3 * E            # the eager row replays 2
     assert ops["verify_fused"] == 16 * 4 * E + (3 + 4) * 3 * E   # folds 3 and 4 pending
     assert ops["commit"] == 4 * 3 * E
+
+
+def test_flush_bytes_counts_pending_rows():
+    wl = W.custom(B=4, H=2, Q=4, lens=[4, 4, 2, 4], S=6, R=4, deferred=True, steps=2, seed=5,
+                  slots=[1, 2, 3, 0])
+    wl.steps[0].num_accepted[:] = torch.tensor([2, 3, 9, 4])
+    wl.steps[0].eager[:] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8)
+    # pending: row 1 (3) and row 2 (min(9, 2) = 2); row 0 is eager, row 3 a null row
+    want = 2 * ((131072 + 3 * bench.RECORD_BYTES) + (131072 + 2 * bench.RECORD_BYTES))
+    assert bench.flush_bytes(wl) == want
