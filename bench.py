@@ -933,6 +933,64 @@ def measure_commit_align(wl: W.Workload, device, iters: int, warmup: int, peak: 
             "frac": b / (us / 1e6) / 1e9 / peak}
 
 
+def conv_align_bytes(wl: W.Workload, num_computed, block_size: int, acc, conv_dim: int,
+                     hist: int, elem_bytes: int) -> int:
+    """Algorithmic bytes of one align-mode conv compaction: every committing
+    row reads its window at column n - 1 and writes it to its final block,
+    and, when the step passes the next block boundary before its last token
+    (a boundary block other than the final one), reads the window at column
+    boundary_len - 1 and writes it to the boundary block."""
+    lens = (wl.cu_seqlens[1:] - wl.cu_seqlens[:-1]).tolist()
+    slots = wl.state_indices.tolist()
+    windows = 0
+    for b in range(wl.spec.B):
+        n = min(max(int(acc[b]), 0), lens[b], wl.spec.Q)
+        if slots[b] <= 0 or n <= 0:
+            continue
+        c = int(num_computed[b])
+        windows += 2 if c + n > (c // block_size + 1) * block_size else 1
+    return windows * 2 * conv_dim * hist * elem_bytes
+
+
+def measure_conv_compact_align(wl: W.Workload, device, iters: int, warmup: int, peak: float):
+    """The align-mode conv compaction on the workload's rows, timed alone:
+    the bf16 channel-major conv pool with the rows' source slots and two
+    blocks per request, block size 16 and num_computed drawn as in
+    measure_commit_align; timed from a CUDA graph replay."""
+    from linear_attention_speculative_kda_gb300 import api
+    sp = wl.spec
+    B = sp.B
+    _, C, wconv = W.conv_shape(sp)
+    width, bs = 2, 16
+    S = 1 + B + B * width
+    gen = torch.Generator().manual_seed(17)
+    i32 = dict(dtype=torch.int32, device=device)
+    pool = W.conv_state(S, C, wconv, seed=3).to(device)
+    slots = torch.where(wl.state_indices > 0, torch.arange(1, B + 1, dtype=torch.int32),
+                        torch.zeros(B, dtype=torch.int32))
+    table = (1 + B + torch.arange(B * width, dtype=torch.int32)).reshape(B, width)
+    num_computed = torch.randint(0, bs, (B,), generator=gen, dtype=torch.int32)
+    cu, dslots = wl.cu_seqlens.to(**i32), slots.to(**i32)
+    acc = wl.steps[0].num_accepted.to(**i32)
+    dtable, dnc = table.to(**i32), num_computed.to(**i32)
+    err = torch.zeros(1, **i32)
+
+    def launch(_k):
+        api.kda_conv_compact_align(pool, cu, dslots, acc, dtable, dnc, block_size=bs,
+                                   window=sp.Q, error_word=err)
+
+    us, how = time_launches(launch, iters, warmup)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item())} in the align conv compaction")
+    b = conv_align_bytes(wl, num_computed.tolist(), bs, wl.steps[0].num_accepted.tolist(), C,
+                         wconv - sp.Q + 1, 2)
+    del pool
+    return {"shape": [S, C, wconv], "dtype": "bf16", "layout": "channel-major",
+            "blocks_per_request": width, "block_size": bs, "timing": how, "launches": iters,
+            "avg_us": us, "bytes_per_launch": b, "gbs": b / (us / 1e6) / 1e9,
+            "frac": b / (us / 1e6) / 1e9 / peak}
+
+
 def run_ours(args):
     rank, world, local = dist_env()
     device = torch.device("cuda", local)
@@ -1071,9 +1129,11 @@ def run_ours(args):
 
     # the align-mode (paged-block) commit on the same rows, timed on its own
     del hio
-    align = record = flush = None
+    align = record = flush = conv_align = None
     if not args.no_extras:
         align = measure_commit_align(wl, device, max(20, args.steps // 4), args.warmup, peak)
+        conv_align = measure_conv_compact_align(wl, device, max(20, args.steps // 4),
+                                                args.warmup, peak)
         record = measure_record_state_blocks(wl, device, max(20, args.steps // 4), args.warmup)
         if wl.spec.deferred:
             flush = measure_flush(wl, device, max(20, args.steps // 4), args.warmup, peak,
@@ -1094,6 +1154,7 @@ def run_ours(args):
             "e2e": e2e, "clocks": clock_summary, "cpu_baseline": cpu,
             "extras": None if args.no_extras else {"conv_compact": conv,
                                                    "commit_align": align,
+                                                   "conv_compact_align": conv_align,
                                                    "record_state_blocks": record,
                                                    "flush": flush}}
     if world > 1:
@@ -1146,7 +1207,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the separately timed conv compaction, align commit, "
+                    help="skip the separately timed conv compactions, align commit, "
                          "running state column and flush")
     ap.add_argument("--reference-rows", type=int, default=8)
     ap.add_argument("--records", choices=["raw", "correction"], default="raw",

@@ -208,38 +208,47 @@ __device__ __forceinline__ void flag(const Params &p, int bits) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && p.err != nullptr) atomicOr(p.err, bits);
 }
 
+// Row b's align-mode plan: its checks (flagged), n, its source slot and its
+// blocks.  False: the row writes nothing.
+__device__ __forceinline__ bool align_row(const Params &p, const AlignArgs &a, int b, int &n,
+                                          int &slot, kda_blocks::Blocks &bl) {
+    const int len = p.cu[b + 1] - p.cu[b];
+    slot = p.slots[b];
+    if (len < 0 || len > p.Q) {
+        flag(p, KDA_ROW_BAD_LENGTH);
+        return false;
+    }
+    if (slot >= p.S) {
+        flag(p, KDA_ROW_BAD_SLOT);
+        return false;
+    }
+    const int req = a.request_indices != nullptr ? a.request_indices[b] : b;
+    if (req < 0 || req >= a.num_requests) {
+        flag(p, KDA_ROW_BAD_BLOCK);
+        return false;
+    }
+    n = min(max(p.acc[req], 0), min(len, p.Q));
+    if (slot <= 0 || n <= 0) return false;
+    bl = kda_blocks::plan(a.block_table + (long long)req * a.bt_stride, a.bt_width, a.block_size,
+                          a.num_computed[req], n);
+    if (bl.bad) {
+        flag(p, KDA_ROW_BAD_BLOCK);
+        return false;
+    }
+    if (bl.final_block >= p.S || bl.boundary >= p.S) {
+        flag(p, KDA_ROW_BAD_SLOT);
+        return false;
+    }
+    return bl.final_block > 0;
+}
+
+// Any strides: one thread per channel, element by element.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) align_kernel(const Params p, const AlignArgs a) {
     for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
-        const int len = p.cu[b + 1] - p.cu[b];
-        const int slot = p.slots[b];
-        if (len < 0 || len > p.Q) {
-            flag(p, KDA_ROW_BAD_LENGTH);
-            continue;
-        }
-        if (slot >= p.S) {
-            flag(p, KDA_ROW_BAD_SLOT);
-            continue;
-        }
-        const int req = a.request_indices != nullptr ? a.request_indices[b] : b;
-        if (req < 0 || req >= a.num_requests) {
-            flag(p, KDA_ROW_BAD_BLOCK);
-            continue;
-        }
-        const int n = min(max(p.acc[req], 0), min(len, p.Q));
-        if (slot <= 0 || n <= 0) continue;
-        const kda_blocks::Blocks bl =
-            kda_blocks::plan(a.block_table + (long long)req * a.bt_stride, a.bt_width,
-                             a.block_size, a.num_computed[req], n);
-        if (bl.bad) {
-            flag(p, KDA_ROW_BAD_BLOCK);
-            continue;
-        }
-        if (bl.final_block >= p.S || bl.boundary >= p.S) {
-            flag(p, KDA_ROW_BAD_SLOT);
-            continue;
-        }
-        if (bl.final_block <= 0) continue;
+        int n, slot;
+        kda_blocks::Blocks bl;
+        if (!align_row(p, a, b, n, slot, bl)) continue;
         T *base = reinterpret_cast<T *>(p.conv);
         const long long src = (long long)slot * p.stride_slot;
         const long long fin = (long long)bl.final_block * p.stride_slot;
@@ -263,6 +272,67 @@ __global__ void __launch_bounds__(kThreads) align_kernel(const Params p, const A
 #pragma unroll
             for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
                 if (h < p.hist) base[fin + ch + (long long)h * p.stride_col] = wf[h];
+        }
+    }
+}
+
+// Channel-major and dense, units of at most kUnitMaxBytes (the fewest whole
+// channels whose bytes make 16-byte pieces): a thread loads its unit of the
+// source slot with 16-byte loads into its own slice of shared memory, then,
+// for the boundary block (when there is one) and the final block in turn,
+// loads the block's unit into a second slice, copies each channel's window
+// from the source's copy into columns [0, history) and stores the unit
+// back.  Both windows come from the source as it was before the call, and
+// a block that is the source itself, or a boundary block that is the final
+// block, ends with what the element-wise form leaves.  Piece v of a slice
+// sits at 16 * (v * kThreads + t), so a warp's 16-byte accesses fall on
+// distinct banks.
+constexpr int kUnitMaxBytes = 64;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) align_unit_kernel(const Params p, const AlignArgs a,
+                                                              int unit_chans) {
+    constexpr int kPieces = kUnitMaxBytes / 16;
+    constexpr int kPer = 16 / (int)sizeof(T);  // elements per piece
+    __shared__ __align__(16) unsigned char stage[2 * kPieces * kThreads * 16];
+    const int W = (int)p.stride_dim;  // = width
+    const int unit_bytes = unit_chans * W * (int)sizeof(T);
+    const int uv = unit_bytes / 16;
+    const int units = p.C / unit_chans;
+    uint4 *s0 = reinterpret_cast<uint4 *>(stage) + threadIdx.x;                     // source
+    uint4 *s1 = reinterpret_cast<uint4 *>(stage) + kPieces * kThreads + threadIdx.x;  // block
+    // element e of a slice: piece e / kPer, position e % kPer
+    auto at = [&](uint4 *slice, int e) -> T & {
+        return reinterpret_cast<T *>(slice + (e / kPer) * kThreads)[e % kPer];
+    };
+    for (int b = blockIdx.y; b < p.B; b += gridDim.y) {
+        int n, slot;
+        kda_blocks::Blocks bl;
+        if (!align_row(p, a, b, n, slot, bl)) continue;
+        const long long slot_bytes = p.stride_slot * (long long)sizeof(T);
+        for (int u = blockIdx.x * kThreads + threadIdx.x; u < units; u += gridDim.x * kThreads) {
+            const long long off = (long long)u * unit_bytes;
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.conv + slot * slot_bytes + off);
+#pragma unroll
+            for (int v = 0; v < kPieces; ++v)
+                if (v < uv) s0[v * kThreads] = src[v];
+            // the window at column `col` of the source's copy into `block`
+            auto merge_into = [&](long long block, int col) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.conv + block * slot_bytes + off);
+#pragma unroll
+                for (int v = 0; v < kPieces; ++v)
+                    if (v < uv) s1[v * kThreads] = dst[v];
+                for (int c = 0; c < unit_chans; ++c) {
+#pragma unroll
+                    for (int h = 0; h < KDA_MAX_CONV_HISTORY; ++h)
+                        if (h < p.hist) at(s1, c * W + h) = at(s0, c * W + col + h);
+                }
+#pragma unroll
+                for (int v = 0; v < kPieces; ++v)
+                    if (v < uv) dst[v] = s1[v * kThreads];
+            };
+            if (bl.boundary > 0) merge_into(bl.boundary, bl.boundary_len - 1);
+            merge_into(bl.final_block, n - 1);
         }
     }
 }
@@ -389,12 +459,27 @@ kda_status kda_conv_compact_align(const kda_conv_config *cc, void *conv_state,
     a.block_size = align->block_size;
     a.num_requests = align->num_requests;
     const int rows = B < kMaxRowsPerGrid ? B : kMaxRowsPerGrid;
-    const dim3 grid((cc->conv_dim + kThreads - 1) / kThreads, rows);
     cudaStream_t stv = static_cast<cudaStream_t>(stream);
-    if (cc->elem_bytes == 2)
-        align_kernel<uint16_t><<<grid, kThreads, 0, stv>>>(p, a);
-    else
-        align_kernel<uint32_t><<<grid, kThreads, 0, stv>>>(p, a);
+    const long long eb = cc->elem_bytes;
+    const bool slots16 = aligned(conv_state, 16) && (cc->stride_slot * eb) % 16 == 0;
+    const long long chan_bytes = (long long)cc->width * eb;
+    long long unit = 1;
+    while ((unit * chan_bytes) % 16 != 0) ++unit;
+    if (slots16 && cc->stride_col == 1 && cc->stride_dim == cc->width &&
+        cc->conv_dim % unit == 0 && unit * chan_bytes <= kUnitMaxBytes) {
+        const int units = (int)(cc->conv_dim / unit);
+        const dim3 grid((units + kThreads - 1) / kThreads, rows);
+        if (cc->elem_bytes == 2)
+            align_unit_kernel<uint16_t><<<grid, kThreads, 0, stv>>>(p, a, (int)unit);
+        else
+            align_unit_kernel<uint32_t><<<grid, kThreads, 0, stv>>>(p, a, (int)unit);
+    } else {
+        const dim3 grid((cc->conv_dim + kThreads - 1) / kThreads, rows);
+        if (cc->elem_bytes == 2)
+            align_kernel<uint16_t><<<grid, kThreads, 0, stv>>>(p, a);
+        else
+            align_kernel<uint32_t><<<grid, kThreads, 0, stv>>>(p, a);
+    }
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

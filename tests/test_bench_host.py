@@ -325,3 +325,26 @@ def test_flush_bytes_counts_pending_rows():
     # pending: row 1 (3) and row 2 (min(9, 2) = 2); row 0 is eager, row 3 a null row
     want = 2 * ((131072 + 3 * bench.RECORD_BYTES) + (131072 + 2 * bench.RECORD_BYTES))
     assert bench.flush_bytes(wl) == want
+
+
+def test_conv_align_bytes_against_the_oracle_moves():
+    # the rows the oracle's align conv compaction moves, and how many windows
+    import numpy as np
+    from oracle import kda_oracle as O
+    wl = W.custom(B=6, H=1, Q=4, lens=[4, 4, 2, 3, 4, 1], S=7, seed=2, slots=[1, 2, 0, 3, 4, 5])
+    acc = [3, 4, 2, 1, 0, 1]
+    # row 0 passes the boundary at 16 (two blocks); row 3 ends on it, so its
+    # boundary block is its final block (one); rows 1 and 5 stay in one block
+    num_computed = [14, 3, 5, 15, 0, 16]
+    C, width, Q = 8, 6, 4
+    hist = width - Q + 1
+    S = 1 + 6 + 6 * 2
+    table = (7 + np.arange(12)).reshape(6, 2)
+    conv = np.arange(S * C * width, dtype=np.float64).reshape(S, C, width)
+    new, issues = O.conv_compact_align(conv, wl.cu_seqlens.numpy(), wl.state_indices.numpy(),
+                                       np.array(acc), Q, table, np.array(num_computed), 16)
+    assert issues == []
+    # every window the oracle wrote is a block whose columns [0, hist) changed
+    written = sum(1 for s in range(S) if not np.array_equal(new[s, :, :hist], conv[s, :, :hist]))
+    got = bench.conv_align_bytes(wl, num_computed, 16, acc, C, hist, 2)
+    assert got == written * 2 * C * hist * 2

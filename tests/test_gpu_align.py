@@ -329,3 +329,39 @@ def test_record_state_blocks_bit_exact(with_indices):
         want_err |= api.ROW_BAD_BLOCK if i.reason == "block" else api.ROW_BAD_SLOT
     assert int(err.item()) == want_err
     assert want_err == ((api.ROW_BAD_BLOCK | api.ROW_BAD_SLOT) if with_indices else 0)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_conv_compact_align_blocks_at_the_source(dtype):
+    """Channel-major pools (the 16-byte unit form of the kernel) whose block
+    tables name the row's own source slot for some columns: the final block,
+    the boundary block or both can be the source, and every window must still
+    come from the source as it was before the call."""
+    rng = np.random.default_rng(70)
+    Q, B, C, bs = 4, 12, 256, 4
+    width_bt = 4
+    S = 1 + B + B * width_bt
+    conv_w = 3 + Q - 1
+    conv = W.conv_state(S, C, conv_w, dtype=dtype, seed=71)
+    lens = np.full(B, Q)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    slots = np.arange(1, B + 1, dtype=np.int32)
+    table = (1 + B + np.arange(B * width_bt)).reshape(B, width_bt).astype(np.int32)
+    for b in range(0, B, 2):
+        table[b, (b // 2) % width_bt] = slots[b]     # one column is the row's own slot
+    table[1, :] = slots[1]                            # every block of row 1 is its slot
+    nc = rng.integers(0, bs * (width_bt - 1), size=B).astype(np.int32)
+    acc = rng.integers(1, Q + 1, size=B).astype(np.int32)
+    dev = torch.device("cuda:0")
+    dconv = conv.to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    t = lambda a: torch.tensor(a, dtype=torch.int32, device=dev)  # noqa: E731
+    api.kda_conv_compact_align(dconv, t(cu), t(slots), t(acc), t(table), t(nc), block_size=bs,
+                               window=Q, error_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bits = {torch.bfloat16: torch.int16, torch.float32: torch.int32}[dtype]
+    raw = conv.contiguous().view(bits).numpy()
+    want, issues = O.conv_compact_align(raw, cu, slots, acc, Q, table, nc, bs)
+    assert issues == []
+    assert np.array_equal(dconv.cpu().contiguous().view(bits).numpy(), want)
