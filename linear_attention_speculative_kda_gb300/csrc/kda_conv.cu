@@ -16,7 +16,8 @@
 //    bytes of channels through the window's columns;
 //  - anything else: a thread moves one channel, element by element.
 // Align mode (paged blocks) copies from the source slot into the final and
-// boundary blocks with the element-wise form.
+// boundary blocks: for channel-major dense pools a thread moves 16-byte
+// units of channels through shared memory, otherwise element by element.
 // The public contract is in include/kda.h (kda_conv_compact).
 #include <cuda_runtime.h>
 #include <stdint.h>
