@@ -1054,6 +1054,7 @@ def run_ours(args):
         avg_ms = statistics.mean(per_kernel[n])
         b = bytes_per[n]
         kernels.append({"name": n, "launches": args.steps, "avg_us": avg_ms * 1e3,
+                        "median_us": statistics.median(per_kernel[n]) * 1e3,
                         "bytes_per_launch": b, "gbs": b / (avg_ms / 1e3) / 1e9,
                         "fp32_ops_per_launch": ops_per[n],
                         "share": sum(per_kernel[n]) / max(1e-9, sum(sum(v) for v in
@@ -1200,7 +1201,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="deferred2", choices=sorted(W.CONFIGS))
     ap.add_argument("--seed", type=int, default=0)
